@@ -36,7 +36,12 @@ class _Seq:
         self.V = np.zeros((L, 0, Hkv, d), dtype=np.float64)
         self.codes: dict[int, tuple] = {}      # pos -> (kcodes, kscale, vcodes, vscale)
 
-    def grow(self, k, v):
+    def grow(self, k, v, n=None):
+        if k is None:
+            self.tier = np.concatenate([self.tier, np.zeros(n, dtype=np.uint8)])
+            self.s = np.concatenate([self.s, np.zeros(n, dtype=np.float64)])
+            self.N += n
+            return
         n = k.shape[1]
         self.K = np.concatenate([self.K, np.asarray(k, dtype=np.float64)], axis=1)
         self.V = np.concatenate([self.V, np.asarray(v, dtype=np.float64)], axis=1)
@@ -50,7 +55,7 @@ class OracleCache:
                  n_sink=4, recent_window=128, budget_mode="percent",
                  budgets=(50, 30, 10, 10), reclassify_interval=64,
                  t2_scale_gran="token", t2_scale_dtype="f32", t2_mode="attend",
-                 page_size=16):
+                 page_size=16, track_values=True):
         self.L, self.Hq, self.Hkv, self.d = n_layers, n_q_heads, n_kv_heads, head_dim
         self.kv_dtype = kv_dtype
         self.n_sink, self.W = n_sink, recent_window
@@ -60,6 +65,9 @@ class OracleCache:
         self.seqs: list[_Seq] = []
         self.alloc = [PagedAllocator(page_size) for _ in range(3)]
         self.t = 0
+        # track_values=False keeps only tiers, scores and slots (for caches too
+        # large to hold in float64); decode_step then needs values and refuses.
+        self.track_values = track_values
 
     @classmethod
     def from_workload(cls, w, **kw):
@@ -68,17 +76,21 @@ class OracleCache:
                    w.reclassify_interval, w.t2_scale_gran, w.t2_scale_dtype, **kw)
 
     # ------------------------------------------------------------- appends
-    def append(self, b: int, k, v, is_prompt: bool) -> None:
-        """k, v: [L, n, Hkv, d] values of n new positions of request b (T0, s = 0)."""
+    def append(self, b: int, k, v, is_prompt: bool, n: int | None = None) -> None:
+        """k, v: [L, n, Hkv, d] values of n new positions of request b (T0, s = 0);
+        without value tracking pass k = v = None and the count n."""
         if b == len(self.seqs):
             self.seqs.append(_Seq(self.L, self.Hkv, self.d))
         sq = self.seqs[b]
         p0 = sq.N
-        sq.grow(np.asarray(k), np.asarray(v))
+        if self.track_values:
+            sq.grow(np.asarray(k), np.asarray(v))
+        else:
+            sq.grow(None, None, n if n is not None else k.shape[1])
         if is_prompt:
             if p0 != sq.prompt_len:
                 raise ValueError("prompt tokens must come before generated ones")
-            sq.prompt_len += k.shape[1]
+            sq.prompt_len += sq.N - p0
         self.alloc[T0].place(b, range(p0, sq.N))
 
     # ---------------------------------------------------------- the step
@@ -100,6 +112,8 @@ class OracleCache:
         """q: [B, L, Hq, d]; k_new, v_new: [B, L, Hkv, d].
 
         Returns (out [B, L, Hq, d] float64, [(R_b, delta_s_b)] per request)."""
+        if not self.track_values:
+            raise RuntimeError("decode_step needs value tracking")
         q = np.asarray(q, dtype=np.float64)
         B = q.shape[0]
         for b in range(B):
@@ -132,8 +146,9 @@ class OracleCache:
             new = self.new_tiers(b)
             old = sq.tier
             moved = np.nonzero(new != old)[0]
-            for pos in moved:
-                self._move_values(sq, int(pos), int(old[pos]), int(new[pos]))
+            if self.track_values:
+                for pos in moved:
+                    self._move_values(sq, int(pos), int(old[pos]), int(new[pos]))
             for x in (T0, T1, T2):
                 self.alloc[x].vacate(b, [p for p in moved if old[p] == x])
             for x in (T0, T1, T2):

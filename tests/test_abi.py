@@ -1,0 +1,94 @@
+"""The C-ABI library loads and exports every entry point include/tkv.h
+declares; host-only calls validate their arguments (CPU, no CUDA device)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from tiered_kv_cache_split_gb300 import _lib as L
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "tkv.h")).read()
+    return sorted(set(re.findall(r"^TKV_API [^;(]*?\b(tkv_\w+)\s*\(", src, flags=re.M)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(L.LIB_PATH):
+        from tiered_kv_cache_split_gb300 import build
+        build.build()
+    return L.load()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    declared = _declared()
+    assert len(declared) >= 20
+    for name in declared:
+        assert hasattr(lib, name), name
+    assert declared == L.exported_symbols()
+
+
+def _cfg(**kw):
+    c = L.Config()
+    c.n_layers, c.n_q_heads, c.n_kv_heads, c.head_dim = 28, 28, 4, 128
+    c.kv_dtype, c.max_batch, c.max_tokens, c.page_size = L.DTYPE_BF16, 32, 8448, 16
+    c.n_sink, c.recent_window, c.budget_mode = 4, 128, L.BUDGET_PERCENT
+    for i, b in enumerate((40, 40, 10, 10)):
+        c.budget[i] = b
+    c.reclassify_interval = 64
+    c.t2_scale_gran, c.t2_scale_dtype = L.SCALE_PER_TOKEN, L.SCALE_F32
+    for k, v in kw.items():
+        setattr(c, k, v)
+    return c
+
+
+def test_workspace_size_of_the_batch32_shape(lib):
+    d, p = ctypes.c_size_t(), ctypes.c_size_t()
+    assert lib.tkv_workspace_size(ctypes.byref(_cfg()), ctypes.byref(d), ctypes.byref(p)) == L.OK
+    kv_total = 32 * 8448 * 28 * 4 * 2 * 128 * 2      # every token can start in T0
+    assert d.value > kv_total and p.value > 0.4 * kv_total
+
+
+@pytest.mark.parametrize("field,value", [("page_size", 32), ("n_q_heads", 30), ("head_dim", 96),
+                                         ("max_batch", 65), ("reclassify_interval", 0),
+                                         ("t2_scale_dtype", L.SCALE_F16), ("budget_mode", 7)])
+def test_invalid_configs_are_rejected_with_a_message(lib, field, value):
+    d, p = ctypes.c_size_t(), ctypes.c_size_t()
+    st = lib.tkv_workspace_size(ctypes.byref(_cfg(**{field: value})), ctypes.byref(d), ctypes.byref(p))
+    assert st == L.ERR_INVALID_ARG
+    assert b"invalid config" in lib.tkv_last_error(None)
+
+
+def test_percent_budgets_must_sum_to_100(lib):
+    c = _cfg()
+    c.budget[3] = 11
+    assert lib.tkv_workspace_size(ctypes.byref(c), ctypes.byref(ctypes.c_size_t()),
+                                  ctypes.byref(ctypes.c_size_t())) == L.ERR_INVALID_ARG
+
+
+def test_create_refuses_null_or_small_workspaces(lib):
+    h = ctypes.c_void_p()
+    st = lib.tkv_create(ctypes.byref(_cfg()), None, 0, None, 0, None, None, ctypes.byref(h))
+    assert st == L.ERR_INVALID_ARG and not h.value
+    buf = (ctypes.c_char * 4096)()
+    addr = (ctypes.addressof(buf) + 255) // 256 * 256
+    st = lib.tkv_create(ctypes.byref(_cfg()), addr, 1024, addr, 1024, None, None, ctypes.byref(h))
+    assert st == L.ERR_CAPACITY and b"too small" in lib.tkv_last_error(None)
+
+
+def test_null_handle_calls_fail_cleanly(lib):
+    assert lib.tkv_reclassify(None) == L.ERR_INVALID_ARG
+    assert lib.tkv_destroy(None) == L.OK
+    assert lib.tkv_last_error(None)
+
+
+def test_stateless_shape_checks(lib):
+    n = ctypes.c_size_t()
+    assert lib.tkv_paged_attention_scratch_size(2, 28, 4, 128, 100, ctypes.byref(n)) == L.OK and n.value > 0
+    assert lib.tkv_paged_attention_scratch_size(2, 30, 4, 128, 100, ctypes.byref(n)) == L.ERR_INVALID_ARG
+    assert lib.tkv_classify_scratch_size(4, 1000, ctypes.byref(n)) == L.OK and n.value >= 32000
+    assert lib.tkv_quantize_rows(None, 1, 1, 8, None, None, 0, None) == L.ERR_INVALID_ARG

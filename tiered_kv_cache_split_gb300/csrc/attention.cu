@@ -1,0 +1,708 @@
+// Split-K paged decode attention over the retained tiers, with the cumulative
+// attention score of "Not All Thoughts Need HBM" (Methodology 2) fused into
+// the softmax epilogue.
+//
+// One CTA serves one (sequence b, KV head, chunk of pages) and all G query
+// heads that share that KV head, so every K/V byte is read from HBM once.
+// Pages come from up to three sources in page order: the T0 pool in HBM, the
+// T1 staging copy prefetched from pinned host DDR, and the T2 staging copy of
+// 8-bit codes (Methodology 1, 3, 4). Each of the CTA's consumer warps owns a
+// private ring of shared-memory stages filled by 1-D bulk TMA copies
+// (cp.async.bulk + mbarrier transaction counts); lane 0 of the warp issues
+// them, so no warp ever waits on another while streaming.
+//
+// Per page (16 tokens) a warp computes
+//   QK : lanes (r, c) = (lane / 8, lane % 8) hold 4 rows x QE elements of K
+//        in fp32 registers; each query head's slice is read from shared
+//        memory and contracted with packed fp32x2 FMAs; the 8 partial sums of
+//        a (head, row) are reduced across the 8 lanes c by a transposing
+//        butterfly that leaves each lane owning whole (head, row) logits;
+//   softmax: online max / sum per head (base-2 logits, the 1/sqrt(d) and
+//        log2(e) factors pre-applied to q); the raw logits are spilled;
+//   PV : lane l owns D/32 output elements of every head; two rows at a time
+//        are contracted with fp32x2 FMAs (row-pair accumulators).
+// The warps of a CTA then merge their (m, Z, O) in shared memory and write the
+// CTA's partial. The last CTA of each (b, KV head) to finish — found by an
+// atomic ticket, so nothing ever waits on another CTA — merges the partials
+// into the output and turns every spilled logit into its exact softmax weight
+// alpha = exp2(l - M) / Z with the global (M, Z), summing the G heads into
+// the score accumulator: the fused score epilogue.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+
+#include "tkv_internal.h"
+
+namespace tkv {
+namespace {
+
+constexpr unsigned kFull = 0xffffffffu;
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                         uint32_t bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1], %2, [%3], %4;" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Wait for phase `parity` of an mbarrier; gives up after about two seconds.
+__device__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+  if (mbar_try(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (uint32_t it = 1; it < (1u << 30); ++it) {
+    if (mbar_try(bar, parity)) return true;
+    if ((it & 1023u) == 0 && global_ns() - t0 > 2000000000ull) return false;
+  }
+  return false;
+}
+
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("{\n .reg .b64 ra, rb, rc, rd;\n"
+      " mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n mov.b64 rc, {%6, %7};\n"
+      " fma.rn.f32x2 rd, ra, rb, rc;\n mov.b64 {%0, %1}, rd;\n}\n"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+__device__ __forceinline__ float i8f(uint32_t w, int byte) {
+  return static_cast<float>(static_cast<int8_t>((w >> (8 * byte)) & 0xffu));
+}
+
+template <typename T, int G, int D>
+struct Shape {
+  static constexpr int GP = G <= 1 ? 1 : G <= 2 ? 2 : G <= 4 ? 4 : 8;
+  static constexpr int ESZ = sizeof(T);
+  static constexpr int ROWB = D * ESZ;        // bytes per full-precision row
+  static constexpr int NCH = ROWB / 16;       // 16-byte chunks per row
+  static constexpr int CPL = NCH / 8;         // chunks per lane in QK
+  static constexpr int EPC = 16 / ESZ;        // elements per chunk
+  static constexpr int QE = CPL * EPC;        // QK elements per lane
+  static constexpr int QP = QE / 2;
+  static constexpr int VPL = D / 32;          // PV output elements per lane
+  static constexpr int BLK = kPage * ROWB;    // K (or V) block of one page and head
+  static constexpr int STAGE = 2 * BLK + 128; // + T2 scale record
+  static constexpr int NV = GP * 4;           // QK partials per lane
+  static constexpr int NL = NV >= 8 ? NV / 8 : 1;
+  static_assert(CPL >= 1 && NCH % 8 == 0, "row must hold a multiple of 8 chunks");
+  static_assert(D % 32 == 0, "head_dim must be a multiple of 32");
+};
+
+// Shared-memory layout of the attention CTA.
+template <typename T, int G, int D>
+struct Smem {
+  using S = Shape<T, G, D>;
+  static constexpr int RING = kAttnWarps * kAttnStages * S::STAGE;
+  static constexpr int QS = S::GP * D * 4;
+  static constexpr int PSW = S::GP * kPage + 8;   // floats per warp: p[GP][16], corr[GP]
+  static constexpr int PS = kAttnWarps * PSW * 4;
+  static constexpr int PG = kMaxChunkPages * 8;
+  static constexpr int BARS = kAttnWarps * kAttnStages * 8;
+  static constexpr int MERGE = kAttnWarps * (G * D + 2 * S::GP) * 4;
+  static constexpr int BODY = ((RING > MERGE ? RING : MERGE) + 127) / 128 * 128;
+  static constexpr int off_q = BODY;
+  static constexpr int off_p = off_q + QS;
+  static constexpr int off_pg = off_p + PS;
+  static constexpr int off_bar = (off_pg + PG + 15) / 16 * 16;
+  static constexpr int TOTAL = off_bar + BARS;
+};
+
+// Loads the lane's QE elements of one row of a full-precision page as pairs.
+template <typename T, int G, int D>
+__device__ __forceinline__ void load_row_qk(const char* rowp, int c, float2 (&out)[Shape<T, G, D>::QP]) {
+  using S = Shape<T, G, D>;
+#pragma unroll
+  for (int j = 0; j < S::CPL; ++j) {
+    const char* cp = rowp + (c + 8 * j) * 16;
+    if constexpr (sizeof(T) == 2) {
+      const uint4 w = *reinterpret_cast<const uint4*>(cp);
+      out[j * 4 + 0] = make_float2(bf_lo(w.x), bf_hi(w.x));
+      out[j * 4 + 1] = make_float2(bf_lo(w.y), bf_hi(w.y));
+      out[j * 4 + 2] = make_float2(bf_lo(w.z), bf_hi(w.z));
+      out[j * 4 + 3] = make_float2(bf_lo(w.w), bf_hi(w.w));
+    } else {
+      const float4 f = *reinterpret_cast<const float4*>(cp);
+      out[j * 2 + 0] = make_float2(f.x, f.y);
+      out[j * 2 + 1] = make_float2(f.z, f.w);
+    }
+  }
+}
+
+// The same elements of one row of an 8-bit page (codes as floats).
+template <typename T, int G, int D>
+__device__ __forceinline__ void load_row_qk_i8(const char* rowp, int c, float2 (&out)[Shape<T, G, D>::QP]) {
+  using S = Shape<T, G, D>;
+#pragma unroll
+  for (int j = 0; j < S::CPL; ++j) {
+    const char* cp = rowp + (c + 8 * j) * S::EPC;
+    if constexpr (S::EPC == 8) {
+      const uint2 w = *reinterpret_cast<const uint2*>(cp);
+      out[j * 4 + 0] = make_float2(i8f(w.x, 0), i8f(w.x, 1));
+      out[j * 4 + 1] = make_float2(i8f(w.x, 2), i8f(w.x, 3));
+      out[j * 4 + 2] = make_float2(i8f(w.y, 0), i8f(w.y, 1));
+      out[j * 4 + 3] = make_float2(i8f(w.y, 2), i8f(w.y, 3));
+    } else {
+      const uint32_t w = *reinterpret_cast<const uint32_t*>(cp);
+      out[j * 2 + 0] = make_float2(i8f(w, 0), i8f(w, 1));
+      out[j * 2 + 1] = make_float2(i8f(w, 2), i8f(w, 3));
+    }
+  }
+}
+
+// The lane's VPL elements of one V row (full precision or 8-bit codes).
+template <typename T, int D, bool I8>
+__device__ __forceinline__ void load_row_pv(const char* rowp, int lane, float (&v)[D / 32]) {
+  constexpr int VPL = D / 32;
+  if constexpr (I8) {
+    if constexpr (VPL == 4) {
+      const uint32_t w = *reinterpret_cast<const uint32_t*>(rowp + lane * 4);
+      v[0] = i8f(w, 0); v[1] = i8f(w, 1); v[2] = i8f(w, 2); v[3] = i8f(w, 3);
+    } else {
+      const uint32_t w = *reinterpret_cast<const uint16_t*>(rowp + lane * 2);
+      v[0] = i8f(w, 0); v[1] = i8f(w, 1);
+    }
+  } else if constexpr (sizeof(T) == 2) {
+    if constexpr (VPL == 4) {
+      const uint2 w = *reinterpret_cast<const uint2*>(rowp + lane * 8);
+      v[0] = bf_lo(w.x); v[1] = bf_hi(w.x); v[2] = bf_lo(w.y); v[3] = bf_hi(w.y);
+    } else {
+      const uint32_t w = *reinterpret_cast<const uint32_t*>(rowp + lane * 4);
+      v[0] = bf_lo(w); v[1] = bf_hi(w);
+    }
+  } else {
+    if constexpr (VPL == 4) {
+      const float4 f = *reinterpret_cast<const float4*>(rowp + lane * 16);
+      v[0] = f.x; v[1] = f.y; v[2] = f.z; v[3] = f.w;
+    } else {
+      const float2 f = *reinterpret_cast<const float2*>(rowp + lane * 8);
+      v[0] = f.x; v[1] = f.y;
+    }
+  }
+}
+
+__device__ __forceinline__ void store_out(float* p, float v) { *p = v; }
+__device__ __forceinline__ void store_out(__nv_bfloat16* p, float v) { *p = __float2bfloat16_rn(v); }
+
+// Resolves page-list index k of sequence b to (source, pool page id).
+__device__ __forceinline__ void page_ref(const AttnParams& p, int b, int k, int& src, int& page) {
+  int kk = k;
+  src = 0;
+  if (kk >= p.npages[0][b]) {
+    kk -= p.npages[0][b];
+    src = 1;
+    if (kk >= p.npages[1][b]) {
+      kk -= p.npages[1][b];
+      src = 2;
+    }
+  }
+  page = p.src[src].table[static_cast<int64_t>(b) * p.table_stride + kk];
+}
+
+template <typename T, int G, int D>
+__global__ void __launch_bounds__(kAttnWarps * 32)
+    attn_split_kernel(const __grid_constant__ AttnParams p) {
+  using S = Shape<T, G, D>;
+  using L = Smem<T, G, D>;
+  extern __shared__ __align__(128) char smem[];
+  __shared__ int s_last;
+
+  const int tid = threadIdx.x;
+  const int w = tid >> 5, lane = tid & 31;
+  const int r = lane >> 3, c = lane & 7;
+  const int kvh = blockIdx.y;
+  const int chunk = blockIdx.x;
+
+  int b = 0;
+  while (b + 1 < p.B && p.chunk_first[b + 1] <= chunk) ++b;
+  const int cf = p.chunk_first[b];
+  const int jc = chunk - cf;
+  const int nch = p.chunk_first[b + 1] - cf;
+  const int ntot = p.npages[0][b] + p.npages[1][b] + p.npages[2][b];
+  const int k0 = jc * p.chunk_pages;
+  const int npg = min(k0 + p.chunk_pages, ntot) - k0;
+
+  char* ring = smem;
+  float* q_s = reinterpret_cast<float*>(smem + L::off_q);
+  float* p_s = reinterpret_cast<float*>(smem + L::off_p) + w * L::PSW;
+  float* corr_s = p_s + S::GP * kPage;
+  int* pg = reinterpret_cast<int*>(smem + L::off_pg);
+  uint32_t* pmask = reinterpret_cast<uint32_t*>(pg + kMaxChunkPages);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::off_bar);
+
+  // Stage the chunk's page references and masks, and the pre-scaled query.
+  for (int i = tid; i < npg; i += blockDim.x) {
+    int src, page;
+    page_ref(p, b, k0 + i, src, page);
+    pg[i] = (src << 28) | page;
+    pmask[i] = p.src[src].mask[page] & 0xffffu;
+  }
+  {
+    const T* q = reinterpret_cast<const T*>(p.q) + static_cast<int64_t>(b) * p.q_stride_b +
+                 static_cast<int64_t>(kvh) * G * D;
+    for (int i = tid; i < S::GP * D; i += blockDim.x) {
+      const int g = i / D;
+      float v = 0.f;
+      if (g < G) {
+        if constexpr (sizeof(T) == 2)
+          v = __bfloat162float(q[i]);
+        else
+          v = static_cast<float>(q[i]);
+      }
+      q_s[i] = v * p.qscale;
+    }
+  }
+  if (lane == 0) {
+    for (int s = 0; s < kAttnStages; ++s) mbar_init(smem_u32(bars + w * kAttnStages + s), 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  __syncthreads();
+
+  uint64_t policy;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(policy));
+
+  char* wring = ring + w * kAttnStages * S::STAGE;
+  const uint32_t wbar = smem_u32(bars + w * kAttnStages);
+  const int nmine = (w < npg) ? (npg - w + kAttnWarps - 1) / kAttnWarps : 0;
+
+  auto issue = [&](int n) {
+    const int i = w + n * kAttnWarps;
+    const int ref = pg[i];
+    const int src = ref >> 28, page = ref & 0x0fffffff;
+    const PageSource& ps = p.src[src];
+    const char* gsrc = ps.base + static_cast<int64_t>(page) * ps.page_bytes +
+                       static_cast<int64_t>(kvh) * ps.head_bytes;
+    const int st = n % kAttnStages;
+    const uint32_t dst = smem_u32(wring + st * S::STAGE);
+    const uint32_t bar = wbar + st * 8;
+    const bool i8 = ps.kind == SRC_INT8;
+    const uint32_t bytes = i8 ? 2u * kPage * D : 2u * S::BLK;
+    const uint32_t sbytes = i8 ? (ps.scale_per_head ? 64u : 128u) : 0u;
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    mbar_expect_tx(bar, bytes + sbytes);
+    bulk_g2s(dst, gsrc, bytes, bar, policy);
+    if (sbytes) {
+      const char* sg = ps.scales + static_cast<int64_t>(page) * ps.scale_page_bytes +
+                       (ps.scale_per_head ? static_cast<int64_t>(kvh) * 64 : 0);
+      bulk_g2s(dst + 2 * S::BLK, sg, sbytes, bar, policy);
+    }
+  };
+
+  if (lane == 0)
+    for (int n = 0; n < min(nmine, kAttnStages); ++n) issue(n);
+
+  float m_run = -INFINITY, z_run = 0.f;  // for the head this lane owns
+  float2 acc[G][S::VPL];
+#pragma unroll
+  for (int g = 0; g < G; ++g)
+#pragma unroll
+    for (int e = 0; e < S::VPL; ++e) acc[g][e] = make_float2(0.f, 0.f);
+
+  // Which (head, row) logits this lane owns after the butterfly.
+  const int own_g = S::NV >= 8 ? (c * S::NL) >> 2 : 0;
+  const bool own_writer = S::NV >= 8 ? true : ((c & 1) == 0);
+
+  float* spill_b = p.spill + (static_cast<int64_t>(b) * p.Hkv + kvh) * p.spill_stride;
+  bool aborted = false;
+  int fail_n = 0;
+
+  for (int n = 0; n < nmine; ++n) {
+    const int st = n % kAttnStages;
+    const bool ok = __all_sync(kFull, mbar_wait(wbar + st * 8, (n / kAttnStages) & 1));
+    if (!ok) {
+      aborted = true;
+      fail_n = n;
+      break;
+    }
+    const char* stage = wring + st * S::STAGE;
+    const int i = w + n * kAttnWarps;
+    const int k = k0 + i;
+    const int src = pg[i] >> 28;
+    const uint32_t mask = pmask[i];
+    const bool i8 = p.src[src].kind == SRC_INT8;
+    const bool per_head = p.src[src].scale_per_head != 0;
+
+    // ---- QK: 4 rows per lane, QE elements each, all heads -----------------
+    float part[S::NV];
+    {
+      float2 kf[4][S::QP];
+#pragma unroll
+      for (int ii = 0; ii < 4; ++ii) {
+        const char* rowp = stage + (r + 4 * ii) * (i8 ? D : S::ROWB);
+        if (i8)
+          load_row_qk_i8<T, G, D>(rowp, c, kf[ii]);
+        else
+          load_row_qk<T, G, D>(rowp, c, kf[ii]);
+      }
+#pragma unroll
+      for (int g = 0; g < S::GP; ++g) {
+        if (g < G) {
+          float2 qv[S::QP];
+#pragma unroll
+          for (int j = 0; j < S::CPL; ++j) {
+            const float* qp = q_s + g * D + (c + 8 * j) * S::EPC;
+#pragma unroll
+            for (int e4 = 0; e4 < S::EPC / 4; ++e4) {
+              const float4 f = *reinterpret_cast<const float4*>(qp + 4 * e4);
+              qv[j * (S::EPC / 2) + 2 * e4] = make_float2(f.x, f.y);
+              qv[j * (S::EPC / 2) + 2 * e4 + 1] = make_float2(f.z, f.w);
+            }
+          }
+#pragma unroll
+          for (int ii = 0; ii < 4; ++ii) {
+            float2 a = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int e = 0; e < S::QP; ++e) a = ffma2(qv[e], kf[ii][e], a);
+            part[g * 4 + ii] = a.x + a.y;
+          }
+        } else {
+#pragma unroll
+          for (int ii = 0; ii < 4; ++ii) part[g * 4 + ii] = 0.f;
+        }
+      }
+    }
+    // ---- transposing butterfly over the 8 lanes c --------------------------
+    {
+      int size = S::NV;
+#pragma unroll
+      for (int m = 4; m >= 1; m >>= 1) {
+        const bool up = (lane & m) != 0;
+        if (size >= 2) {
+          const int half = size >> 1;
+#pragma unroll
+          for (int t = 0; t < S::NV / 2; ++t) {
+            if (t < half) {
+              const float send = up ? part[t] : part[t + half];
+              const float keep = up ? part[t + half] : part[t];
+              part[t] = keep + __shfl_xor_sync(kFull, send, m);
+            }
+          }
+          size = half;
+        } else {
+          part[0] += __shfl_xor_sync(kFull, part[0], m);
+        }
+      }
+    }
+    // part[0 .. NL) are this lane's logits: head own_g, rows own_row(t).
+    float lg[S::NL], pv[S::NL];
+    float pmax = -INFINITY;
+#pragma unroll
+    for (int t = 0; t < S::NL; ++t) {
+      const int idx = S::NV >= 8 ? c * S::NL + t : (c >> 1);
+      const int row = r + 4 * (idx & 3);
+      float l = part[t];
+      if (i8) {
+        const char* sc = stage + 2 * S::BLK;
+        const float sk = per_head ? __half2float(reinterpret_cast<const __half*>(sc)[row])
+                                  : reinterpret_cast<const float*>(sc)[row];
+        l *= sk;
+      }
+      if (!((mask >> row) & 1u)) l = -INFINITY;
+      lg[t] = l;
+      pmax = fmaxf(pmax, l);
+    }
+#pragma unroll
+    for (int m = 1; m < 8; m <<= 1)
+      if (m < 8 / S::GP) pmax = fmaxf(pmax, __shfl_xor_sync(kFull, pmax, m));
+    pmax = fmaxf(pmax, __shfl_xor_sync(kFull, pmax, 8));
+    pmax = fmaxf(pmax, __shfl_xor_sync(kFull, pmax, 16));
+    const float m_new = fmaxf(m_run, pmax);
+    float corr = 1.f, psum = 0.f;
+    if (m_new != -INFINITY) {
+      corr = exp2f(m_run - m_new);
+#pragma unroll
+      for (int t = 0; t < S::NL; ++t) {
+        pv[t] = exp2f(lg[t] - m_new);
+        psum += pv[t];
+      }
+    } else {
+#pragma unroll
+      for (int t = 0; t < S::NL; ++t) pv[t] = 0.f;
+    }
+#pragma unroll
+    for (int m = 1; m < 8; m <<= 1)
+      if (m < 8 / S::GP) psum += __shfl_xor_sync(kFull, psum, m);
+    psum += __shfl_xor_sync(kFull, psum, 8);
+    psum += __shfl_xor_sync(kFull, psum, 16);
+    z_run = z_run * corr + psum;
+    m_run = m_new;
+
+    // spill raw logits, publish p (times the V scale for 8-bit rows) and corr
+    if (own_writer && own_g < G) {
+#pragma unroll
+      for (int t = 0; t < S::NL; ++t) {
+        const int idx = S::NV >= 8 ? c * S::NL + t : (c >> 1);
+        const int row = r + 4 * (idx & 3);
+        spill_b[(static_cast<int64_t>(k) * G + own_g) * kPage + row] = lg[t];
+        float pw = pv[t];
+        if (i8) {
+          const char* sc = stage + 2 * S::BLK;
+          const float sv = per_head ? __half2float(reinterpret_cast<const __half*>(sc)[kPage + row])
+                                    : reinterpret_cast<const float*>(sc)[kPage + row];
+          pw = ((mask >> row) & 1u) ? pw * sv : 0.f;
+        }
+        p_s[own_g * kPage + row] = pw;
+      }
+      if (r == 0 && (S::NV < 8 ? c == 0 : (c & ((8 / S::GP) - 1)) == 0)) corr_s[own_g] = corr;
+    }
+    __syncwarp();
+
+    // ---- PV ---------------------------------------------------------------
+    {
+      const bool rescale = __any_sync(kFull, own_g < G && corr != 1.f);
+      if (rescale) {
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          const float cg = corr_s[g];
+#pragma unroll
+          for (int e = 0; e < S::VPL; ++e) {
+            acc[g][e].x *= cg;
+            acc[g][e].y *= cg;
+          }
+        }
+      }
+      const char* vblk = stage + (i8 ? kPage * D : S::BLK);
+      const int vrow = i8 ? D : S::ROWB;
+      const bool partial = mask != 0xffffu && !i8;
+#pragma unroll 2
+      for (int j = 0; j < kPage / 2; ++j) {
+        float va[S::VPL], vb[S::VPL];
+        if (i8) {
+          load_row_pv<T, D, true>(vblk + (2 * j) * vrow, lane, va);
+          load_row_pv<T, D, true>(vblk + (2 * j + 1) * vrow, lane, vb);
+        } else {
+          load_row_pv<T, D, false>(vblk + (2 * j) * vrow, lane, va);
+          load_row_pv<T, D, false>(vblk + (2 * j + 1) * vrow, lane, vb);
+        }
+        if (partial) {  // holes may hold anything: weight 0 must not meet a NaN
+          const bool oka = (mask >> (2 * j)) & 1u, okb = (mask >> (2 * j + 1)) & 1u;
+#pragma unroll
+          for (int e = 0; e < S::VPL; ++e) {
+            va[e] = oka ? va[e] : 0.f;
+            vb[e] = okb ? vb[e] : 0.f;
+          }
+        }
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          const float2 pp = *reinterpret_cast<const float2*>(p_s + g * kPage + 2 * j);
+#pragma unroll
+          for (int e = 0; e < S::VPL; ++e) acc[g][e] = ffma2(pp, make_float2(va[e], vb[e]), acc[g][e]);
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0 && n + kAttnStages < nmine) issue(n + kAttnStages);
+  }
+
+  if (aborted) {
+    atomicExch(p.err, DEV_TIMEOUT);
+    // let the copies this warp issued but did not consume land before the CTA exits
+    const int hi = min(fail_n + kAttnStages, nmine);
+    for (int n = fail_n; n < hi; ++n)
+      (void)mbar_wait(wbar + (n % kAttnStages) * 8, (n / kAttnStages) & 1);
+    m_run = -INFINITY;
+    z_run = 0.f;
+#pragma unroll
+    for (int g = 0; g < G; ++g)
+#pragma unroll
+      for (int e = 0; e < S::VPL; ++e) acc[g][e] = make_float2(0.f, 0.f);
+  }
+
+  // ---- merge the CTA's warps ----------------------------------------------
+  __syncthreads();
+  float* mo = reinterpret_cast<float*>(ring);           // [warps][G][D]
+  float* mm = mo + kAttnWarps * G * D;                  // [warps][GP]
+  float* mz = mm + kAttnWarps * S::GP;                  // [warps][GP]
+#pragma unroll
+  for (int g = 0; g < G; ++g)
+#pragma unroll
+    for (int e = 0; e < S::VPL; ++e)
+      mo[(w * G + g) * D + lane * S::VPL + e] = acc[g][e].x + acc[g][e].y;
+  if (own_writer && own_g < G && r == 0 && (S::NV < 8 ? c == 0 : (c & ((8 / S::GP) - 1)) == 0)) {
+    mm[w * S::GP + own_g] = m_run;
+    mz[w * S::GP + own_g] = z_run;
+  }
+  __syncthreads();
+  const int64_t pidx = static_cast<int64_t>(cf + jc) * p.Hkv + kvh;
+  for (int idx = tid; idx < G * D; idx += blockDim.x) {
+    const int g = idx / D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int ww = 0; ww < kAttnWarps; ++ww) M = fmaxf(M, mm[ww * S::GP + g]);
+    float o = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int ww = 0; ww < kAttnWarps; ++ww) {
+        const float mw = mm[ww * S::GP + g];
+        if (mw != -INFINITY) o += mo[(ww * G) * D + idx] * exp2f(mw - M);
+      }
+    }
+    p.part_o[pidx * G * D + idx] = o;
+  }
+  if (tid < G) {
+    float M = -INFINITY;
+    for (int ww = 0; ww < kAttnWarps; ++ww) M = fmaxf(M, mm[ww * S::GP + tid]);
+    float Z = 0.f;
+    if (M != -INFINITY)
+      for (int ww = 0; ww < kAttnWarps; ++ww) {
+        const float mw = mm[ww * S::GP + tid];
+        if (mw != -INFINITY) Z += mz[ww * S::GP + tid] * exp2f(mw - M);
+      }
+    p.part_m[pidx * G + tid] = M;
+    p.part_z[pidx * G + tid] = Z;
+  }
+
+  // ---- ticket: the last CTA of (b, kvh) runs the epilogue -----------------
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) {
+    const int t = atomicAdd(p.tickets + b * p.Hkv + kvh, 1);
+    s_last = (t == nch - 1);
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  if (tid == 0) p.tickets[b * p.Hkv + kvh] = 0;
+
+  float* cM = reinterpret_cast<float*>(ring);
+  float* cIZ = cM + S::GP;
+  if (tid < G) {
+    float M = -INFINITY;
+    for (int j = 0; j < nch; ++j)
+      M = fmaxf(M, __ldcg(p.part_m + (static_cast<int64_t>(cf + j) * p.Hkv + kvh) * G + tid));
+    float Z = 0.f;
+    if (M != -INFINITY)
+      for (int j = 0; j < nch; ++j) {
+        const int64_t pj = (static_cast<int64_t>(cf + j) * p.Hkv + kvh) * G + tid;
+        const float mj = __ldcg(p.part_m + pj);
+        if (mj != -INFINITY) Z += __ldcg(p.part_z + pj) * exp2f(mj - M);
+      }
+    cM[tid] = M;
+    cIZ[tid] = Z > 0.f ? 1.f / Z : 0.f;
+  }
+  __syncthreads();
+  {
+    T* out = reinterpret_cast<T*>(p.out) + static_cast<int64_t>(b) * p.out_stride_b +
+             static_cast<int64_t>(kvh) * G * D;
+    for (int idx = tid; idx < G * D; idx += blockDim.x) {
+      const int g = idx / D;
+      const float M = cM[g];
+      float o = 0.f;
+      if (M != -INFINITY)
+        for (int j = 0; j < nch; ++j) {
+          const int64_t pj = static_cast<int64_t>(cf + j) * p.Hkv + kvh;
+          const float mj = __ldcg(p.part_m + pj * G + g);
+          if (mj != -INFINITY) o += __ldcg(p.part_o + pj * G * D + idx) * exp2f(mj - M);
+        }
+      store_out(out + idx, o * cIZ[g]);
+    }
+  }
+  if (p.acc != nullptr) {
+    float* accb = p.acc + static_cast<int64_t>(b) * p.acc_stride_b +
+                  static_cast<int64_t>(kvh) * p.acc_stride_h;
+    float M[G], IZ[G];
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      M[g] = cM[g];
+      IZ[g] = cIZ[g];
+    }
+    for (int item = tid; item < ntot * kPage; item += blockDim.x) {
+      const int k = item >> 4, row = item & 15;
+      int src, page;
+      page_ref(p, b, k, src, page);
+      if (!((p.src[src].mask[page] >> row) & 1u)) continue;
+      float a = 0.f;
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        const float l = __ldcg(spill_b + (static_cast<int64_t>(k) * G + g) * kPage + row);
+        a += exp2f(l - M[g]) * IZ[g];
+      }
+      const int64_t at = p.acc_by_position
+                             ? static_cast<int64_t>(p.src[src].posmap[static_cast<int64_t>(page) * kPage + row])
+                             : static_cast<int64_t>(item);
+      if (at >= 0) accb[at] += a;
+    }
+  }
+}
+
+template <typename T, int G, int D>
+cudaError_t launch_typed(const AttnParams& p, int total_chunks, cudaStream_t s) {
+  using L = Smem<T, G, D>;
+  auto kern = attn_split_kernel<T, G, D>;
+  static bool configured = false;  // per instantiation; the attribute is per function
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::TOTAL);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  dim3 grid(total_chunks, p.Hkv);
+  kern<<<grid, kAttnWarps * 32, L::TOTAL, s>>>(p);
+  return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t dispatch_g(const AttnParams& p, int total_chunks, cudaStream_t s) {
+  const int G = p.G, D = p.D;
+#define TKV_CASE(GG, DD) \
+  if (G == GG && D == DD) return launch_typed<T, GG, DD>(p, total_chunks, s);
+  TKV_CASE(1, 64) TKV_CASE(1, 128)
+  TKV_CASE(2, 64) TKV_CASE(2, 128)
+  TKV_CASE(4, 64) TKV_CASE(4, 128)
+  TKV_CASE(7, 64) TKV_CASE(7, 128)
+  TKV_CASE(8, 64) TKV_CASE(8, 128)
+#undef TKV_CASE
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+int attention_supported(int kv_dtype, int G, int D) {
+  (void)kv_dtype;
+  const bool g_ok = G == 1 || G == 2 || G == 4 || G == 7 || G == 8;
+  return g_ok && (D == 64 || D == 128);
+}
+
+cudaError_t launch_attention(const AttnParams& p, int kv_dtype, int total_chunks, cudaStream_t s) {
+  if (total_chunks <= 0) return cudaSuccess;
+  if (kv_dtype == 1) return dispatch_g<__nv_bfloat16>(p, total_chunks, s);
+  return dispatch_g<float>(p, total_chunks, s);
+}
+
+}  // namespace tkv

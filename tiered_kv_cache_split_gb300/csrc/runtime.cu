@@ -1,0 +1,1228 @@
+// Host runtime of libtkv: the C ABI of include/tkv.h.
+//
+// It owns the bookkeeping of the four-tier cache of "Not All Thoughts Need
+// HBM" — which tier and which (page, slot) every position occupies, the page
+// lists of each sequence, the pools' page counters — and orchestrates one
+// decode step: append (Methodology 1: the recent window is in T0), per-layer
+// prefetch of T1 and T2 on the copy stream overlapped with the previous
+// layer's attention (Methodology 4), split-K attention with the fused score
+// epilogue (Methodology 2, 3), the float64 score fold, and every Delta steps
+// the reassignment (classifier kernel) and the differential data movement
+// (only tokens whose tier changed move; Methodology 4).
+//
+// Slot rule (the page fixes none; this is the reading used throughout): a
+// token that keeps its tier keeps its slot; arrivals, in ascending position,
+// fill the sequence's holes in ascending (page, slot) order, then take the
+// pool's next never-used page; sequences are served in ascending order.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <chrono>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <functional>
+#include <new>
+#include <queue>
+#include <string>
+#include <vector>
+
+#include "../../include/tkv.h"
+#include "tkv_internal.h"
+
+using namespace tkv;
+
+namespace {
+
+thread_local std::string g_last_error = "no error";
+
+constexpr size_t kAlign = 256;
+size_t align_up(size_t x, size_t a = kAlign) { return (x + a - 1) / a * a; }
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+using MinHeap = std::priority_queue<int64_t, std::vector<int64_t>, std::greater<int64_t>>;
+
+struct Seq {
+  int64_t N = 0, prompt_len = 0;
+  std::vector<uint8_t> tier;
+  std::vector<int32_t> loc;      // page * 16 + slot in the pool of its tier; -1 when T3
+  std::vector<int32_t> pages[3]; // page ids per tier, in acquisition (= ascending) order
+  MinHeap holes[3];              // page * 16 + slot of free slots in those pages
+};
+
+// Sizes derived from a configuration; shared by tkv_workspace_size and tkv_create.
+struct Layout {
+  int L, Hq, Hkv, D, G, esz, maxb;
+  int64_t maxtok, maxp;
+  int64_t cap[3];
+  int64_t plb[3];        // bytes of one page record per layer (T2: int8 codes)
+  int64_t scale_rec;     // bytes of one T2 scale record per page per layer
+  int64_t max_chunks, spill_stride, temp_rows;
+  // device offsets
+  size_t o_pool0, o_stage1, o_stage2c, o_stage2s, o_table, o_mask, o_posmap, o_tier, o_tier_new,
+      o_s, o_acc, o_part_o, o_part_m, o_part_z, o_spill, o_tickets, o_keys, o_err, o_movers,
+      o_temp, o_locs, o_io, dev_bytes;
+  size_t io_q, io_k, io_out;
+  // pinned offsets
+  size_t p_pool1, p_pool2c, p_pool2s, p_arena, arena_bytes, pinned_bytes;
+};
+
+bool budget_pages(const tkv_config& c, int tier, int64_t maxtok, int64_t* pages) {
+  int64_t count;
+  if (c.budget_mode == TKV_BUDGET_PERCENT)
+    count = c.budget[tier] * maxtok / 100;
+  else
+    count = tier < 3 ? c.budget[tier] : maxtok;
+  count = std::min(count, maxtok);
+  *pages = ceil_div(std::max<int64_t>(count, 0), kPage) + 1;
+  return true;
+}
+
+std::string validate(const tkv_config& c) {
+  char buf[256];
+  auto bad = [&](const char* what) { std::snprintf(buf, sizeof buf, "invalid config: %s", what); return std::string(buf); };
+  if (c.n_layers < 1 || c.n_layers > 4096) return bad("n_layers out of range");
+  if (c.n_q_heads < 1 || c.n_kv_heads < 1 || c.n_q_heads % c.n_kv_heads) return bad("n_q_heads must be a multiple of n_kv_heads");
+  if (!attention_supported(c.kv_dtype, c.n_q_heads / c.n_kv_heads, c.head_dim))
+    return bad("unsupported (Hq/Hkv, head_dim): group size must be 1, 2, 4, 7 or 8 and head_dim 64 or 128");
+  if (c.kv_dtype != TKV_DTYPE_F32 && c.kv_dtype != TKV_DTYPE_BF16) return bad("kv_dtype");
+  if (c.max_batch < 1 || c.max_batch > kMaxBatch) return bad("max_batch must be 1..64");
+  if (c.max_tokens < 1 || c.max_tokens > (int64_t(1) << 27)) return bad("max_tokens out of range");
+  if (c.page_size != kPage) return bad("page_size must be 16");
+  if (c.n_sink < 0 || c.recent_window < 0) return bad("n_sink / recent_window negative");
+  if (c.budget_mode == TKV_BUDGET_PERCENT) {
+    int64_t s = 0;
+    for (int i = 0; i < 4; ++i) {
+      if (c.budget[i] < 0 || c.budget[i] > 100) return bad("percent budgets must be 0..100");
+      s += c.budget[i];
+    }
+    if (s != 100) return bad("percent budgets must sum to 100");
+  } else if (c.budget_mode == TKV_BUDGET_COUNT) {
+    for (int i = 0; i < 3; ++i)
+      if (c.budget[i] < 0) return bad("count budgets must be >= 0");
+  } else {
+    return bad("budget_mode");
+  }
+  if (c.reclassify_interval < 1) return bad("reclassify_interval must be >= 1");
+  const bool combo_ok = (c.t2_scale_gran == TKV_SCALE_PER_TOKEN && c.t2_scale_dtype == TKV_SCALE_F32) ||
+                        (c.t2_scale_gran == TKV_SCALE_PER_TOKEN_HEAD && c.t2_scale_dtype == TKV_SCALE_F16);
+  if (!combo_ok) return bad("T2 scales: per-token scales are float32, per-token-head scales float16");
+  if (c.t2_mode != TKV_T2_ATTEND && c.t2_mode != TKV_T2_MASK) return bad("t2_mode");
+  if (c.t0_pages < 0 || c.t1_pages < 0 || c.t2_pages < 0 || c.max_staged_movers < 0) return bad("negative capacity");
+  if (c.split_pages < 0 || c.split_pages > kMaxChunkPages) return bad("split_pages must be 0..128");
+  return std::string();
+}
+
+Layout make_layout(const tkv_config& c) {
+  Layout y{};
+  y.L = c.n_layers; y.Hq = c.n_q_heads; y.Hkv = c.n_kv_heads; y.D = c.head_dim;
+  y.G = y.Hq / y.Hkv; y.esz = c.kv_dtype == TKV_DTYPE_BF16 ? 2 : 4; y.maxb = c.max_batch;
+  y.maxtok = c.max_tokens;
+  y.maxp = ceil_div(y.maxtok, kPage) + 1;
+  int64_t per[3];
+  per[0] = y.maxp;
+  budget_pages(c, 1, y.maxtok, &per[1]);
+  budget_pages(c, 2, y.maxtok, &per[2]);
+  y.cap[0] = c.t0_pages ? c.t0_pages : y.maxb * per[0];
+  y.cap[1] = c.t1_pages ? c.t1_pages : y.maxb * per[1];
+  y.cap[2] = c.t2_pages ? c.t2_pages : y.maxb * per[2];
+  y.plb[0] = y.plb[1] = int64_t(y.Hkv) * 2 * kPage * y.D * y.esz;
+  y.plb[2] = int64_t(y.Hkv) * 2 * kPage * y.D;
+  y.scale_rec = c.t2_scale_gran == TKV_SCALE_PER_TOKEN ? 2 * kPage * 4 : int64_t(y.Hkv) * 2 * kPage * 2;
+  y.max_chunks = int64_t(y.maxb) * (ceil_div(3 * y.maxp, 8) + 1);
+  y.spill_stride = 3 * y.maxp * y.G * kPage;
+  y.temp_rows = c.max_staged_movers ? c.max_staged_movers
+                                    : std::max<int64_t>(4096, int64_t(y.maxb) * y.maxtok / 10);
+  size_t o = 0;
+  auto take = [&](size_t bytes) { size_t at = o; o = align_up(o + bytes); return at; };
+  y.o_pool0 = take(size_t(y.L) * y.cap[0] * y.plb[0]);
+  y.o_stage1 = take(2 * size_t(y.cap[1]) * y.plb[1]);
+  y.o_stage2c = take(2 * size_t(y.cap[2]) * y.plb[2]);
+  y.o_stage2s = take(2 * size_t(y.cap[2]) * y.scale_rec);
+  y.o_table = take(3 * size_t(y.maxb) * y.maxp * 4);
+  y.o_mask = take(size_t(y.cap[0] + y.cap[1] + y.cap[2]) * 4);
+  y.o_posmap = take(size_t(y.cap[0] + y.cap[1] + y.cap[2]) * kPage * 4);
+  y.o_tier = take(size_t(y.maxb) * y.maxtok);
+  y.o_tier_new = take(size_t(y.maxb) * y.maxtok);
+  y.o_s = take(size_t(y.maxb) * y.maxtok * 8);
+  y.o_acc = take(size_t(y.maxb) * y.Hkv * y.maxtok * 4);
+  y.o_part_o = take(size_t(y.max_chunks) * y.Hkv * y.G * y.D * 4);
+  y.o_part_m = take(size_t(y.max_chunks) * y.Hkv * y.G * 4);
+  y.o_part_z = take(size_t(y.max_chunks) * y.Hkv * y.G * 4);
+  y.o_spill = take(size_t(y.maxb) * y.Hkv * y.spill_stride * 4);
+  y.o_tickets = take(size_t(y.maxb) * y.Hkv * 4);
+  y.o_keys = take(size_t(y.maxb) * y.maxtok * 8);
+  y.o_err = take(64);
+  y.o_movers = take(size_t(y.maxb) * y.maxtok * sizeof(Mover));
+  y.o_temp = take(size_t(y.temp_rows) * y.L * 2 * y.Hkv * y.D * y.esz);
+  y.o_locs = take(size_t(y.maxtok) * 4);
+  const size_t q_bytes = size_t(y.maxb) * y.L * y.Hq * y.D * y.esz;
+  const size_t kv_bytes = size_t(y.maxb) * y.L * y.Hkv * y.D * y.esz;
+  y.io_q = 0;
+  y.io_k = align_up(q_bytes);
+  y.io_out = y.io_k + 2 * align_up(kv_bytes);
+  y.o_io = take(y.io_out + q_bytes);
+  y.dev_bytes = o;
+  o = 0;
+  y.p_pool1 = take(size_t(y.L) * y.cap[1] * y.plb[1]);
+  y.p_pool2c = take(size_t(y.L) * y.cap[2] * y.plb[2]);
+  y.p_pool2s = take(size_t(y.L) * y.cap[2] * y.scale_rec);
+  const size_t arena = align_up(size_t(y.maxb) * y.maxtok) +                       // tier read-back
+                       align_up(size_t(y.maxb) * y.maxtok * sizeof(Mover)) +       // movers
+                       align_up(3 * size_t(y.maxb) * y.maxp * 4) +                 // page tables
+                       align_up(size_t(y.cap[0] + y.cap[1] + y.cap[2]) * 4) +      // masks
+                       align_up(size_t(y.cap[0] + y.cap[1] + y.cap[2]) * kPage * 4) +  // posmaps
+                       align_up(size_t(y.maxtok) * 4);                              // prefill slots
+  y.arena_bytes = arena;
+  y.p_arena = take(arena);
+  y.pinned_bytes = o;
+  return y;
+}
+
+struct TimedPair {
+  cudaEvent_t a, b;
+  int kind;  // 0 attention, 1 prefetch
+};
+
+}  // namespace
+
+struct tkv_ctx {
+  tkv_config cfg;
+  Layout y;
+  int device = 0;
+  char* dev = nullptr;
+  char* pin = nullptr;       // host address of the pinned workspace
+  char* pin_dev = nullptr;   // the same memory as seen by kernels
+  cudaStream_t cs = nullptr, xs = nullptr;
+  cudaEvent_t ev_ready[2] = {nullptr, nullptr}, ev_free[2] = {nullptr, nullptr};
+  int slot_rr = 0;
+  int64_t steps = 0;
+  int64_t next_page[3] = {0, 0, 0};
+  std::vector<Seq> seqs;
+  std::vector<uint32_t> mask[3];
+  std::vector<int32_t> posmap[3];
+  std::vector<int32_t> table[3];  // [maxb][maxp]
+  bool broken = false;
+  std::string err = "no error";
+  tkv_stats stats{};
+  std::vector<TimedPair> pending, spare;
+  uint8_t* d_tier = nullptr;
+  uint8_t* d_tier_new = nullptr;
+
+  char* D(size_t off) const { return dev + off; }
+  char* P(size_t off) const { return pin + off; }
+  char* PD(size_t off) const { return pin_dev + off; }
+};
+
+namespace {
+
+tkv_status fail(tkv_ctx* h, tkv_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  std::vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  if (h) h->err = buf;
+  return st;
+}
+
+tkv_status fail_cuda(tkv_ctx* h, const char* what, cudaError_t e) {
+  if (h) h->broken = true;
+  return fail(h, TKV_ERR_CUDA, "%s failed: %s", what, cudaGetErrorString(e));
+}
+
+#define CK(h, call)                                            \
+  do {                                                         \
+    cudaError_t e_ = (call);                                   \
+    if (e_ != cudaSuccess) return fail_cuda((h), #call, e_);   \
+  } while (0)
+
+tkv_status check_usable(tkv_ctx* h) {
+  if (!h) return fail(nullptr, TKV_ERR_INVALID_ARG, "null handle");
+  if (h->broken) return fail(h, TKV_ERR_STATE, "handle is broken by an earlier CUDA failure: %s", h->err.c_str());
+  return TKV_OK;
+}
+
+// Harvest finished timing events into the stats.
+void harvest(tkv_ctx* h) {
+  for (auto& tp : h->pending) {
+    float ms = 0.f;
+    if (cudaEventElapsedTime(&ms, tp.a, tp.b) == cudaSuccess) {
+      if (tp.kind == 0)
+        h->stats.attn_ms += ms;
+      else
+        h->stats.prefetch_ms += ms;
+    }
+    h->spare.push_back(tp);
+  }
+  h->pending.clear();
+  (void)cudaGetLastError();
+}
+
+tkv_status timed_pair(tkv_ctx* h, int kind, TimedPair* out) {
+  if (h->spare.empty()) {
+    TimedPair tp{};
+    CK(h, cudaEventCreate(&tp.a));
+    CK(h, cudaEventCreate(&tp.b));
+    h->spare.push_back(tp);
+  }
+  *out = h->spare.back();
+  h->spare.pop_back();
+  out->kind = kind;
+  return TKV_OK;
+}
+
+tkv_status sync_all(tkv_ctx* h) {
+  CK(h, cudaStreamSynchronize(h->cs));
+  if (h->xs != h->cs) CK(h, cudaStreamSynchronize(h->xs));
+  int32_t e = 0;
+  CK(h, cudaMemcpy(&e, h->D(h->y.o_err), 4, cudaMemcpyDeviceToHost));
+  harvest(h);
+  if (e == DEV_TIMEOUT) {
+    h->broken = true;
+    return fail(h, TKV_ERR_TIMEOUT, "a bounded device wait gave up (copy never landed)");
+  }
+  if (e != 0) {
+    h->broken = true;
+    return fail(h, TKV_ERR_INTERNAL, "device reported error code %d", e);
+  }
+  return TKV_OK;
+}
+
+// Places `positions` (ascending) of sequence b in tier t: holes first, then new pages.
+// Returns false (leaving the pool counter untouched beyond what was used) on capacity.
+bool place(tkv_ctx* h, Seq& sq, int b, int t, const std::vector<int64_t>& positions,
+           std::vector<int32_t>* locs_out) {
+  for (int64_t pos : positions) {
+    int64_t code;
+    if (!sq.holes[t].empty()) {
+      code = sq.holes[t].top();
+      sq.holes[t].pop();
+    } else {
+      if (h->next_page[t] >= h->y.cap[t] || int64_t(sq.pages[t].size()) >= h->y.maxp) return false;
+      const int64_t page = h->next_page[t]++;
+      sq.pages[t].push_back(static_cast<int32_t>(page));
+      h->table[t][size_t(b) * h->y.maxp + sq.pages[t].size() - 1] = static_cast<int32_t>(page);
+      for (int s = 1; s < kPage; ++s) sq.holes[t].push(page * kPage + s);
+      code = page * kPage;
+    }
+    const int64_t page = code / kPage, slot = code % kPage;
+    h->mask[t][page] |= 1u << slot;
+    h->posmap[t][page * kPage + slot] = static_cast<int32_t>(pos);
+    sq.loc[pos] = static_cast<int32_t>(code);
+    sq.tier[pos] = static_cast<uint8_t>(t);
+    if (locs_out) locs_out->push_back(static_cast<int32_t>(code));
+  }
+  return true;
+}
+
+void vacate(tkv_ctx* h, Seq& sq, int t, int64_t pos) {
+  const int64_t code = sq.loc[pos];
+  const int64_t page = code / kPage, slot = code % kPage;
+  h->mask[t][page] &= ~(1u << slot);
+  h->posmap[t][page * kPage + slot] = -1;
+  sq.holes[t].push(code);
+  sq.loc[pos] = -1;
+}
+
+int64_t total_pages(const Seq& sq, bool with_t2) {
+  return int64_t(sq.pages[0].size() + sq.pages[1].size()) + (with_t2 ? int64_t(sq.pages[2].size()) : 0);
+}
+
+tkv_status upload_metadata(tkv_ctx* h) {
+  const Layout& y = h->y;
+  char* arena = h->P(y.p_arena);
+  size_t off = align_up(size_t(y.maxb) * y.maxtok) + align_up(size_t(y.maxb) * y.maxtok * sizeof(Mover));
+  const size_t tbytes = size_t(y.maxb) * y.maxp * 4;
+  for (int t = 0; t < 3; ++t) {
+    std::memcpy(arena + off + t * tbytes, h->table[t].data(), tbytes);
+    CK(h, cudaMemcpyAsync(h->D(y.o_table) + t * tbytes, arena + off + t * tbytes, tbytes,
+                          cudaMemcpyHostToDevice, h->cs));
+  }
+  off += align_up(3 * tbytes);
+  size_t moff = off, poff = off + align_up(size_t(y.cap[0] + y.cap[1] + y.cap[2]) * 4);
+  int64_t base = 0;
+  for (int t = 0; t < 3; ++t) {
+    const size_t n = size_t(h->next_page[t]);
+    if (n) {
+      std::memcpy(arena + moff + base * 4, h->mask[t].data(), n * 4);
+      CK(h, cudaMemcpyAsync(h->D(y.o_mask) + base * 4, arena + moff + base * 4, n * 4,
+                            cudaMemcpyHostToDevice, h->cs));
+      std::memcpy(arena + poff + base * kPage * 4, h->posmap[t].data(), n * kPage * 4);
+      CK(h, cudaMemcpyAsync(h->D(y.o_posmap) + base * kPage * 4, arena + poff + base * kPage * 4,
+                            n * kPage * 4, cudaMemcpyHostToDevice, h->cs));
+    }
+    base += y.cap[t];
+  }
+  return TKV_OK;
+}
+
+uint32_t* d_mask(tkv_ctx* h, int t) {
+  int64_t base = 0;
+  for (int i = 0; i < t; ++i) base += h->y.cap[i];
+  return reinterpret_cast<uint32_t*>(h->D(h->y.o_mask)) + base;
+}
+int32_t* d_posmap(tkv_ctx* h, int t) {
+  int64_t base = 0;
+  for (int i = 0; i < t; ++i) base += h->y.cap[i];
+  return reinterpret_cast<int32_t*>(h->D(h->y.o_posmap)) + base * kPage;
+}
+int32_t* d_table(tkv_ctx* h, int t) {
+  return reinterpret_cast<int32_t*>(h->D(h->y.o_table)) + size_t(t) * h->y.maxb * h->y.maxp;
+}
+
+int choose_chunk_pages(const tkv_ctx* h, const std::vector<int64_t>& ntot) {
+  if (h->cfg.split_pages > 0) return h->cfg.split_pages;
+  int64_t sum = 0;
+  for (int64_t n : ntot) sum += n;
+  sum *= h->y.Hkv;
+  // about four waves of two resident CTAs per SM on 152 SMs
+  const int64_t target = 4 * 2 * 152;
+  int64_t cp = ceil_div(std::max<int64_t>(sum, 1), target);
+  cp = std::max<int64_t>(16, std::min<int64_t>(cp, kMaxChunkPages));
+  return static_cast<int>(ceil_div(cp, kAttnWarps) * kAttnWarps);
+}
+
+tkv_status enqueue_prefetch(tkv_ctx* h, int layer, int slot) {
+  const Layout& y = h->y;
+  const bool timing = h->cfg.flags & TKV_FLAG_TIMING;
+  TimedPair tp{};
+  if (h->xs != h->cs) CK(h, cudaStreamWaitEvent(h->xs, h->ev_free[slot], 0));
+  if (timing) {
+    tkv_status st = timed_pair(h, 1, &tp);
+    if (st) return st;
+    CK(h, cudaEventRecord(tp.a, h->xs));
+  }
+  const int64_t n1 = h->next_page[1], n2 = h->next_page[2];
+  if (n1 > 0) {
+    CK(h, cudaMemcpyAsync(h->D(y.o_stage1) + size_t(slot) * y.cap[1] * y.plb[1],
+                          h->P(y.p_pool1) + size_t(layer) * y.cap[1] * y.plb[1], size_t(n1) * y.plb[1],
+                          cudaMemcpyHostToDevice, h->xs));
+    h->stats.prefetch_bytes += n1 * y.plb[1];
+  }
+  const bool t2_read = h->cfg.t2_mode == TKV_T2_ATTEND;
+  if (n2 > 0 && t2_read) {
+    CK(h, cudaMemcpyAsync(h->D(y.o_stage2c) + size_t(slot) * y.cap[2] * y.plb[2],
+                          h->P(y.p_pool2c) + size_t(layer) * y.cap[2] * y.plb[2], size_t(n2) * y.plb[2],
+                          cudaMemcpyHostToDevice, h->xs));
+    CK(h, cudaMemcpyAsync(h->D(y.o_stage2s) + size_t(slot) * y.cap[2] * y.scale_rec,
+                          h->P(y.p_pool2s) + size_t(layer) * y.cap[2] * y.scale_rec,
+                          size_t(n2) * y.scale_rec, cudaMemcpyHostToDevice, h->xs));
+    h->stats.prefetch_bytes += n2 * (y.plb[2] + y.scale_rec);
+  }
+  if (timing) {
+    CK(h, cudaEventRecord(tp.b, h->xs));
+    h->pending.push_back(tp);
+  }
+  CK(h, cudaEventRecord(h->ev_ready[slot], h->xs));
+  return TKV_OK;
+}
+
+void fill_sources(tkv_ctx* h, int layer, int slot, AttnParams& p) {
+  const Layout& y = h->y;
+  const int64_t head_full = int64_t(2) * kPage * y.D * y.esz;
+  p.src[0] = PageSource{h->D(y.o_pool0) + size_t(layer) * y.cap[0] * y.plb[0], y.plb[0], head_full,
+                        d_table(h, 0), d_mask(h, 0), d_posmap(h, 0), nullptr, 0, 0, SRC_FULL};
+  p.src[1] = PageSource{h->D(y.o_stage1) + size_t(slot) * y.cap[1] * y.plb[1], y.plb[1], head_full,
+                        d_table(h, 1), d_mask(h, 1), d_posmap(h, 1), nullptr, 0, 0, SRC_FULL};
+  p.src[2] = PageSource{h->D(y.o_stage2c) + size_t(slot) * y.cap[2] * y.plb[2], y.plb[2],
+                        int64_t(2) * kPage * y.D, d_table(h, 2), d_mask(h, 2), d_posmap(h, 2),
+                        h->D(y.o_stage2s) + size_t(slot) * y.cap[2] * y.scale_rec, y.scale_rec,
+                        h->cfg.t2_scale_gran == TKV_SCALE_PER_TOKEN_HEAD ? 1 : 0, SRC_INT8};
+  p.nsrc = 3;
+}
+
+int64_t attn_bytes_per_layer(tkv_ctx* h) {
+  const Layout& y = h->y;
+  const int64_t full = int64_t(2) * y.Hkv * y.D * y.esz;
+  const int64_t i8 = int64_t(2) * y.Hkv * y.D +
+                     (h->cfg.t2_scale_gran == TKV_SCALE_PER_TOKEN ? 8 : int64_t(2) * y.Hkv * 2);
+  const bool t2_read = h->cfg.t2_mode == TKV_T2_ATTEND;
+  int64_t bytes = 0;
+  for (const Seq& sq : h->seqs)
+    for (int64_t i = 0; i < sq.N; ++i) {
+      const int t = sq.tier[i];
+      if (t <= 1) bytes += full;
+      else if (t == 2 && t2_read) bytes += i8;
+    }
+  return bytes;
+}
+
+tkv_status do_reclassify(tkv_ctx* h);
+
+tkv_status decode_step_device(tkv_ctx* h, const void* q, const void* k_new, const void* v_new, void* out) {
+  const Layout& y = h->y;
+  const int B = static_cast<int>(h->seqs.size());
+  // ---- capacity checks before any mutation
+  int need_pages = 0;
+  for (int b = 0; b < B; ++b) {
+    const Seq& sq = h->seqs[b];
+    if (sq.N + 1 > y.maxtok) return fail(h, TKV_ERR_CAPACITY, "sequence %d is full (%lld tokens)", b, (long long)sq.N);
+    if (sq.holes[0].empty()) {
+      ++need_pages;
+      if (int64_t(sq.pages[0].size()) + 1 > y.maxp) return fail(h, TKV_ERR_CAPACITY, "sequence %d: T0 page list full", b);
+    }
+  }
+  if (h->next_page[0] + need_pages > y.cap[0]) return fail(h, TKV_ERR_CAPACITY, "T0 pool full");
+
+  // ---- append: every sequence's new token goes to T0 (recent window)
+  AppendParams ap{};
+  ap.B = B; ap.L = y.L; ap.Hkv = y.Hkv; ap.D = y.D; ap.esz = y.esz;
+  ap.k = static_cast<const char*>(k_new); ap.v = static_cast<const char*>(v_new);
+  ap.pool0 = h->D(y.o_pool0); ap.layer_bytes = y.cap[0] * y.plb[0]; ap.page_bytes = y.plb[0];
+  ap.mask0 = d_mask(h, 0); ap.posmap0 = d_posmap(h, 0); ap.table0 = d_table(h, 0);
+  ap.table_stride = static_cast<int32_t>(y.maxp);
+  for (int b = 0; b < B; ++b) {
+    Seq& sq = h->seqs[b];
+    const int64_t pos = sq.N;
+    sq.tier.push_back(0);
+    sq.loc.push_back(-1);
+    sq.N += 1;
+    const size_t np_before = sq.pages[0].size();
+    std::vector<int32_t> loc;
+    place(h, sq, b, 0, {pos}, &loc);
+    ap.page[b] = loc[0] / kPage;
+    ap.slot[b] = loc[0] % kPage;
+    ap.new_page[b] = sq.pages[0].size() != np_before;
+    ap.np0[b] = static_cast<int32_t>(np_before);
+    ap.pos[b] = pos;
+  }
+  CK(h, launch_append(ap, h->cs));
+
+  // ---- per layer: prefetch T1/T2 (copy stream), attention + fused scores (compute stream)
+  AttnParams p{};
+  p.B = B; p.Hq = y.Hq; p.Hkv = y.Hkv; p.D = y.D; p.G = y.G;
+  p.table_stride = static_cast<int32_t>(y.maxp);
+  const bool t2_read = h->cfg.t2_mode == TKV_T2_ATTEND;
+  std::vector<int64_t> ntot(B);
+  for (int b = 0; b < B; ++b) {
+    const Seq& sq = h->seqs[b];
+    p.npages[0][b] = static_cast<int32_t>(sq.pages[0].size());
+    p.npages[1][b] = static_cast<int32_t>(sq.pages[1].size());
+    p.npages[2][b] = t2_read ? static_cast<int32_t>(sq.pages[2].size()) : 0;
+    ntot[b] = p.npages[0][b] + p.npages[1][b] + p.npages[2][b];
+  }
+  p.chunk_pages = choose_chunk_pages(h, ntot);
+  p.chunk_first[0] = 0;
+  for (int b = 0; b < B; ++b)
+    p.chunk_first[b + 1] = p.chunk_first[b] + static_cast<int32_t>(ceil_div(ntot[b], p.chunk_pages));
+  const int total_chunks = p.chunk_first[B];
+  if (total_chunks > y.max_chunks) return fail(h, TKV_ERR_INTERNAL, "chunk table overflow");
+  p.q_stride_b = int64_t(y.L) * y.Hq * y.D;
+  p.out_stride_b = int64_t(y.L) * y.Hq * y.D;
+  p.qscale = static_cast<float>(1.4426950408889634 / std::sqrt(double(y.D)));
+  p.part_o = reinterpret_cast<float*>(h->D(y.o_part_o));
+  p.part_m = reinterpret_cast<float*>(h->D(y.o_part_m));
+  p.part_z = reinterpret_cast<float*>(h->D(y.o_part_z));
+  p.spill = reinterpret_cast<float*>(h->D(y.o_spill));
+  p.spill_stride = y.spill_stride;
+  p.tickets = reinterpret_cast<int32_t*>(h->D(y.o_tickets));
+  p.acc = reinterpret_cast<float*>(h->D(y.o_acc));
+  p.acc_stride_b = int64_t(y.Hkv) * y.maxtok;
+  p.acc_stride_h = y.maxtok;
+  p.acc_by_position = 1;
+  p.err = reinterpret_cast<int32_t*>(h->D(y.o_err));
+  const bool timing = h->cfg.flags & TKV_FLAG_TIMING;
+  const int64_t abytes = attn_bytes_per_layer(h);
+
+  for (int l = 0; l < y.L; ++l) {
+    const int slot = h->slot_rr;
+    h->slot_rr ^= 1;
+    tkv_status st = enqueue_prefetch(h, l, slot);
+    if (st) return st;
+    if (h->xs != h->cs) CK(h, cudaStreamWaitEvent(h->cs, h->ev_ready[slot], 0));
+    fill_sources(h, l, slot, p);
+    p.q = static_cast<const char*>(q) + size_t(l) * y.Hq * y.D * y.esz;
+    p.out = static_cast<char*>(out) + size_t(l) * y.Hq * y.D * y.esz;
+    TimedPair tp{};
+    if (timing) {
+      st = timed_pair(h, 0, &tp);
+      if (st) return st;
+      CK(h, cudaEventRecord(tp.a, h->cs));
+    }
+    CK(h, launch_attention(p, h->cfg.kv_dtype, total_chunks, h->cs));
+    if (timing) {
+      CK(h, cudaEventRecord(tp.b, h->cs));
+      h->pending.push_back(tp);
+    }
+    CK(h, cudaEventRecord(h->ev_free[slot], h->cs));
+    h->stats.attn_launches += 1;
+    h->stats.attn_bytes += abytes;
+  }
+
+  // ---- fold this step's score increments into s (float64)
+  FoldParams fp{};
+  fp.B = B; fp.Hkv = y.Hkv;
+  for (int b = 0; b < B; ++b) fp.N[b] = h->seqs[b].N;
+  fp.s = reinterpret_cast<double*>(h->D(y.o_s));
+  fp.acc = reinterpret_cast<float*>(h->D(y.o_acc));
+  fp.stride = y.maxtok;
+  fp.inv_lh = 1.0 / (double(y.L) * double(y.Hq));
+  CK(h, launch_fold(fp, h->cs));
+
+  h->steps += 1;
+  h->stats.steps += 1;
+  if (h->pending.size() > 4096) {
+    CK(h, cudaStreamSynchronize(h->cs));
+    CK(h, cudaStreamSynchronize(h->xs));
+    harvest(h);
+  }
+  if (h->steps % h->cfg.reclassify_interval == 0) return do_reclassify(h);
+  return TKV_OK;
+}
+
+tkv_status do_reclassify(tkv_ctx* h) {
+  const Layout& y = h->y;
+  const int B = static_cast<int>(h->seqs.size());
+  if (B == 0) return fail(h, TKV_ERR_STATE, "no sequence to reclassify");
+  const auto t_start = std::chrono::steady_clock::now();
+
+  // ---- classifier kernel: new tiers on the device
+  ClassifyParams cp{};
+  cp.B = B;
+  cp.s = reinterpret_cast<const double*>(h->D(y.o_s));
+  cp.old_tier = h->d_tier;
+  cp.new_tier = h->d_tier_new;
+  cp.stride = y.maxtok;
+  for (int b = 0; b < B; ++b) {
+    const Seq& sq = h->seqs[b];
+    const int64_t N = sq.N;
+    int64_t n0, n1, n2;
+    if (h->cfg.budget_mode == TKV_BUDGET_PERCENT) {
+      n1 = h->cfg.budget[1] * N / 100;
+      n2 = h->cfg.budget[2] * N / 100;
+      const int64_t n3 = h->cfg.budget[3] * N / 100;
+      n0 = N - n1 - n2 - n3;
+    } else {
+      n0 = h->cfg.budget[0]; n1 = h->cfg.budget[1]; n2 = h->cfg.budget[2];
+    }
+    cp.N[b] = N; cp.prompt_len[b] = sq.prompt_len; cp.n0[b] = n0; cp.n1[b] = n1; cp.n2[b] = n2;
+  }
+  cp.n_sink = h->cfg.n_sink;
+  cp.recent_window = h->cfg.recent_window;
+  cp.keys = reinterpret_cast<unsigned long long*>(h->D(y.o_keys));
+  cp.err = reinterpret_cast<int32_t*>(h->D(y.o_err));
+  // the device tier array must reflect appends since the last reassignment
+  {
+    char* arena = h->P(y.p_arena);
+    for (int b = 0; b < B; ++b) std::memcpy(arena + size_t(b) * y.maxtok, h->seqs[b].tier.data(), h->seqs[b].N);
+    int64_t nmax = 0;
+    for (const Seq& sq : h->seqs) nmax = std::max(nmax, sq.N);
+    CK(h, cudaMemcpy2DAsync(h->d_tier, y.maxtok, arena, y.maxtok, nmax, B, cudaMemcpyHostToDevice, h->cs));
+    CK(h, launch_classify(cp, h->cs));
+    CK(h, cudaMemcpy2DAsync(arena, y.maxtok, h->d_tier_new, y.maxtok, nmax, B, cudaMemcpyDeviceToHost, h->cs));
+    tkv_status st = sync_all(h);
+    if (st) return st;
+  }
+  const uint8_t* new_tiers = reinterpret_cast<const uint8_t*>(h->P(y.p_arena));
+
+  // ---- allocator on a copy of the bookkeeping: a capacity failure changes nothing
+  std::vector<Seq> seqs = h->seqs;
+  int64_t next_page_save[3] = {h->next_page[0], h->next_page[1], h->next_page[2]};
+  std::vector<uint32_t> mask_save[3];
+  std::vector<int32_t> posmap_save[3], table_save[3];
+  for (int t = 0; t < 3; ++t) {
+    mask_save[t] = h->mask[t];
+    posmap_save[t] = h->posmap[t];
+    table_save[t] = h->table[t];
+  }
+  auto restore = [&]() {
+    for (int t = 0; t < 3; ++t) {
+      h->next_page[t] = next_page_save[t];
+      h->mask[t].swap(mask_save[t]);
+      h->posmap[t].swap(posmap_save[t]);
+      h->table[t].swap(table_save[t]);
+    }
+  };
+
+  std::vector<Mover> phase1, phase2;
+  int64_t d2h = 0, h2d = 0;
+  const int64_t row_full = int64_t(y.L) * 2 * y.Hkv * y.D * y.esz;
+  const int64_t row_i8 = int64_t(y.L) * (2 * y.Hkv * y.D + (h->cfg.t2_scale_gran == TKV_SCALE_PER_TOKEN ? 8 : 4 * y.Hkv));
+  for (int b = 0; b < B; ++b) {
+    Seq& sq = seqs[b];
+    const uint8_t* nt = new_tiers + size_t(b) * y.maxtok;
+    std::vector<int64_t> moved;
+    for (int64_t i = 0; i < sq.N; ++i)
+      if (nt[i] != sq.tier[i]) {
+        if (sq.tier[i] == 3 || nt[i] > 3) {
+          restore();
+          return fail(h, TKV_ERR_INTERNAL, "classifier revived an evicted token or wrote tier %d", int(nt[i]));
+        }
+        moved.push_back(i);
+      }
+    // source locations before vacating; slots vacated by tokens whose data moves
+    std::vector<int32_t> src_loc(moved.size());
+    std::vector<uint8_t> src_tier(moved.size());
+    std::vector<int64_t> busy;  // tier * 2^40 + loc of slots whose old data still has to be read
+    for (size_t m = 0; m < moved.size(); ++m) {
+      src_loc[m] = sq.loc[moved[m]];
+      src_tier[m] = sq.tier[moved[m]];
+      if (nt[moved[m]] != 3) busy.push_back((int64_t(src_tier[m]) << 40) | src_loc[m]);
+    }
+    std::sort(busy.begin(), busy.end());
+    for (int t = 0; t < 3; ++t)
+      for (size_t m = 0; m < moved.size(); ++m)
+        if (src_tier[m] == t) vacate(h, sq, t, moved[m]);
+    std::vector<int32_t> dst_loc(moved.size(), -1);
+    for (int t = 0; t < 3; ++t) {
+      std::vector<int64_t> arrivals;
+      std::vector<size_t> idx;
+      for (size_t m = 0; m < moved.size(); ++m)
+        if (nt[moved[m]] == t) {
+          arrivals.push_back(moved[m]);
+          idx.push_back(m);
+        }
+      std::vector<int32_t> locs;
+      if (!place(h, sq, b, t, arrivals, &locs)) {
+        restore();
+        return fail(h, TKV_ERR_CAPACITY, "tier %d pool or page list full during reassignment", t);
+      }
+      for (size_t a = 0; a < idx.size(); ++a) dst_loc[idx[a]] = locs[a];
+    }
+    for (size_t m = 0; m < moved.size(); ++m) {
+      const int64_t pos = moved[m];
+      const int dt = nt[pos];
+      if (dt == 3) {
+        sq.tier[pos] = 3;
+        sq.loc[pos] = -1;
+        continue;
+      }
+      Mover mv{b, src_tier[m], src_loc[m], dt, dst_loc[m], -1};
+      const bool recycled = std::binary_search(busy.begin(), busy.end(), (int64_t(dt) << 40) | dst_loc[m]);
+      if (recycled) {
+        mv.temp_row = static_cast<int32_t>(phase2.size());
+        phase2.push_back(mv);
+      } else {
+        phase1.push_back(mv);
+      }
+      if (src_tier[m] == 1) h2d += row_full;
+      if (src_tier[m] == 2) h2d += row_i8;
+      if (dt == 1) d2h += row_full;
+      if (dt == 2) d2h += row_i8;
+    }
+  }
+  if (int64_t(phase2.size()) > y.temp_rows) {
+    restore();
+    return fail(h, TKV_ERR_CAPACITY, "%zu movers need staging but max_staged_movers is %lld",
+                phase2.size(), (long long)y.temp_rows);
+  }
+
+  // ---- commit the bookkeeping, then move the data
+  h->seqs.swap(seqs);
+  char* arena = h->P(y.p_arena);
+  const size_t moff = align_up(size_t(y.maxb) * y.maxtok);
+  Mover* hm = reinterpret_cast<Mover*>(arena + moff);
+  std::memcpy(hm, phase2.data(), phase2.size() * sizeof(Mover));
+  std::memcpy(hm + phase2.size(), phase1.data(), phase1.size() * sizeof(Mover));
+  const size_t nmov = phase1.size() + phase2.size();
+  Mover* dm = reinterpret_cast<Mover*>(h->D(y.o_movers));
+  if (nmov) CK(h, cudaMemcpyAsync(dm, hm, nmov * sizeof(Mover), cudaMemcpyHostToDevice, h->cs));
+  MoveParams mp{};
+  mp.L = y.L; mp.Hkv = y.Hkv; mp.D = y.D; mp.kv_dtype = h->cfg.kv_dtype;
+  mp.pools.base[0] = h->D(y.o_pool0);
+  mp.pools.base[1] = h->PD(y.p_pool1);
+  mp.pools.base[2] = h->PD(y.p_pool2c);
+  for (int t = 0; t < 3; ++t) {
+    mp.pools.layer_bytes[t] = y.cap[t] * y.plb[t];
+    mp.pools.page_bytes[t] = y.plb[t];
+  }
+  mp.pools.t2_scales = h->PD(y.p_pool2s);
+  mp.pools.t2_scale_layer_bytes = y.cap[2] * y.scale_rec;
+  mp.pools.t2_scale_page_bytes = y.scale_rec;
+  mp.pools.scale_per_head = h->cfg.t2_scale_gran == TKV_SCALE_PER_TOKEN_HEAD;
+  mp.pools.scale_f16 = h->cfg.t2_scale_dtype == TKV_SCALE_F16;
+  mp.temp = h->D(y.o_temp);
+  mp.mode = MOVE_GATHER;
+  CK(h, launch_move(mp, dm, int64_t(phase2.size()), h->cs));
+  mp.mode = MOVE_DIRECT;
+  CK(h, launch_move(mp, dm + phase2.size(), int64_t(phase1.size()), h->cs));
+  mp.mode = MOVE_SCATTER;
+  CK(h, launch_move(mp, dm, int64_t(phase2.size()), h->cs));
+  tkv_status st = upload_metadata(h);
+  if (st) return st;
+  std::swap(h->d_tier, h->d_tier_new);
+  st = sync_all(h);
+  if (st) return st;
+
+  h->stats.reclassifies += 1;
+  h->stats.movers += int64_t(nmov);
+  h->stats.d2h_move_bytes += d2h;
+  h->stats.h2d_move_bytes += h2d;
+  if (h->cfg.flags & TKV_FLAG_TIMING)
+    h->stats.reclassify_ms +=
+        std::chrono::duration<double, std::milli>(std::chrono::steady_clock::now() - t_start).count();
+  return TKV_OK;
+}
+
+tkv_status seq_ok(tkv_ctx* h, int32_t seq) {
+  if (seq < 0 || seq >= int32_t(h->seqs.size())) return fail(h, TKV_ERR_INVALID_ARG, "no sequence %d", seq);
+  return TKV_OK;
+}
+
+}  // namespace
+
+// ============================================================ C ABI
+extern "C" {
+
+tkv_status tkv_workspace_size(const tkv_config* cfg, size_t* dev_bytes, size_t* pinned_bytes) {
+  if (!cfg || !dev_bytes || !pinned_bytes) return fail(nullptr, TKV_ERR_INVALID_ARG, "null argument");
+  const std::string why = validate(*cfg);
+  if (!why.empty()) return fail(nullptr, TKV_ERR_INVALID_ARG, "%s", why.c_str());
+  const Layout y = make_layout(*cfg);
+  *dev_bytes = y.dev_bytes;
+  *pinned_bytes = y.pinned_bytes;
+  return TKV_OK;
+}
+
+tkv_status tkv_create(const tkv_config* cfg, void* dev_ws, size_t dev_bytes, void* pinned_ws,
+                      size_t pinned_bytes, tkv_stream compute, tkv_stream copy, tkv_handle* out) {
+  if (!cfg || !out) return fail(nullptr, TKV_ERR_INVALID_ARG, "null argument");
+  *out = nullptr;
+  const std::string why = validate(*cfg);
+  if (!why.empty()) return fail(nullptr, TKV_ERR_INVALID_ARG, "%s", why.c_str());
+  const Layout y = make_layout(*cfg);
+  if (!dev_ws || !pinned_ws) return fail(nullptr, TKV_ERR_INVALID_ARG, "null workspace");
+  if (reinterpret_cast<uintptr_t>(dev_ws) % kAlign || reinterpret_cast<uintptr_t>(pinned_ws) % 64)
+    return fail(nullptr, TKV_ERR_INVALID_ARG, "workspace not aligned (device 256 B, pinned 64 B)");
+  if (dev_bytes < y.dev_bytes || pinned_bytes < y.pinned_bytes)
+    return fail(nullptr, TKV_ERR_CAPACITY, "workspace too small: need %zu device and %zu pinned bytes",
+                y.dev_bytes, y.pinned_bytes);
+  tkv_ctx* h = new (std::nothrow) tkv_ctx();
+  if (!h) return fail(nullptr, TKV_ERR_INTERNAL, "out of host memory");
+  h->cfg = *cfg;
+  h->y = y;
+  h->dev = static_cast<char*>(dev_ws);
+  h->pin = static_cast<char*>(pinned_ws);
+  h->cs = static_cast<cudaStream_t>(compute);
+  h->xs = copy ? static_cast<cudaStream_t>(copy) : h->cs;
+  auto bail = [&](tkv_status st) {
+    for (int i = 0; i < 2; ++i) {
+      if (h->ev_ready[i]) cudaEventDestroy(h->ev_ready[i]);
+      if (h->ev_free[i]) cudaEventDestroy(h->ev_free[i]);
+    }
+    delete h;
+    return st;
+  };
+  cudaError_t e = cudaGetDevice(&h->device);
+  if (e != cudaSuccess) return bail(fail_cuda(nullptr, "cudaGetDevice", e));
+  void* mapped = nullptr;
+  e = cudaHostGetDevicePointer(&mapped, pinned_ws, 0);
+  if (e != cudaSuccess) return bail(fail_cuda(nullptr, "cudaHostGetDevicePointer (pinned workspace must be page-locked)", e));
+  h->pin_dev = static_cast<char*>(mapped);
+  for (int i = 0; i < 2; ++i) {
+    if ((e = cudaEventCreateWithFlags(&h->ev_ready[i], cudaEventDisableTiming)) != cudaSuccess ||
+        (e = cudaEventCreateWithFlags(&h->ev_free[i], cudaEventDisableTiming)) != cudaSuccess)
+      return bail(fail_cuda(nullptr, "cudaEventCreate", e));
+  }
+  h->d_tier = reinterpret_cast<uint8_t*>(h->D(y.o_tier));
+  h->d_tier_new = reinterpret_cast<uint8_t*>(h->D(y.o_tier_new));
+  // zero what must start at zero: pools (holes must hold finite values), tables,
+  // masks, tickets, accumulators, scores, the error word; posmaps start at -1
+  struct Z { size_t off, bytes; int val; } zs[] = {
+      {y.o_pool0, size_t(y.L) * y.cap[0] * y.plb[0], 0},
+      {y.o_table, 3 * size_t(y.maxb) * y.maxp * 4, 0},
+      {y.o_mask, size_t(y.cap[0] + y.cap[1] + y.cap[2]) * 4, 0},
+      {y.o_posmap, size_t(y.cap[0] + y.cap[1] + y.cap[2]) * kPage * 4, 0xff},
+      {y.o_tier, size_t(y.maxb) * y.maxtok, 0},
+      {y.o_s, size_t(y.maxb) * y.maxtok * 8, 0},
+      {y.o_acc, size_t(y.maxb) * y.Hkv * y.maxtok * 4, 0},
+      {y.o_tickets, size_t(y.maxb) * y.Hkv * 4, 0},
+      {y.o_err, 64, 0}};
+  for (const Z& z : zs)
+    if ((e = cudaMemsetAsync(h->D(z.off), z.val, z.bytes, h->cs)) != cudaSuccess)
+      return bail(fail_cuda(nullptr, "cudaMemsetAsync", e));
+  if ((e = cudaStreamSynchronize(h->cs)) != cudaSuccess) return bail(fail_cuda(nullptr, "cudaStreamSynchronize", e));
+  for (int t = 0; t < 3; ++t) {
+    h->mask[t].assign(size_t(y.cap[t]), 0u);
+    h->posmap[t].assign(size_t(y.cap[t]) * kPage, -1);
+    h->table[t].assign(size_t(y.maxb) * y.maxp, 0);
+  }
+  *out = h;
+  return TKV_OK;
+}
+
+tkv_status tkv_destroy(tkv_handle h) {
+  if (!h) return TKV_OK;
+  cudaStreamSynchronize(h->cs);
+  if (h->xs != h->cs) cudaStreamSynchronize(h->xs);
+  harvest(h);
+  for (auto& tp : h->spare) {
+    cudaEventDestroy(tp.a);
+    cudaEventDestroy(tp.b);
+  }
+  for (int i = 0; i < 2; ++i) {
+    cudaEventDestroy(h->ev_ready[i]);
+    cudaEventDestroy(h->ev_free[i]);
+  }
+  delete h;
+  return TKV_OK;
+}
+
+tkv_status tkv_append(tkv_handle h, int32_t seq, const void* k, const void* v, int64_t n_tokens,
+                      int32_t is_prompt) {
+  if (tkv_status st = check_usable(h)) return st;
+  const Layout& y = h->y;
+  if (!k || !v || n_tokens < 0) return fail(h, TKV_ERR_INVALID_ARG, "bad k/v or n_tokens");
+  if (seq < 0 || seq > int32_t(h->seqs.size())) return fail(h, TKV_ERR_INVALID_ARG, "sequence %d does not exist and is not the next one", seq);
+  if (seq == int32_t(h->seqs.size()) && seq >= y.maxb) return fail(h, TKV_ERR_CAPACITY, "max_batch sequences already exist");
+  if (n_tokens == 0) return TKV_OK;
+  const int64_t N0 = seq < int32_t(h->seqs.size()) ? h->seqs[seq].N : 0;
+  const int64_t P0 = seq < int32_t(h->seqs.size()) ? h->seqs[seq].prompt_len : 0;
+  if (N0 + n_tokens > y.maxtok) return fail(h, TKV_ERR_CAPACITY, "sequence %d would exceed max_tokens", seq);
+  if (is_prompt && N0 != P0) return fail(h, TKV_ERR_INVALID_ARG, "prompt tokens must precede generated tokens");
+  {
+    const int64_t holes = seq < int32_t(h->seqs.size()) ? int64_t(h->seqs[seq].holes[0].size()) : 0;
+    const int64_t newp = ceil_div(std::max<int64_t>(0, n_tokens - holes), kPage);
+    const int64_t have = seq < int32_t(h->seqs.size()) ? int64_t(h->seqs[seq].pages[0].size()) : 0;
+    if (h->next_page[0] + newp > y.cap[0] || have + newp > y.maxp)
+      return fail(h, TKV_ERR_CAPACITY, "T0 pool too small for the prefill");
+  }
+  if (seq == int32_t(h->seqs.size())) h->seqs.emplace_back();
+  Seq& sq = h->seqs[seq];
+  std::vector<int64_t> pos(static_cast<size_t>(n_tokens));
+  for (int64_t i = 0; i < n_tokens; ++i) pos[i] = N0 + i;
+  sq.tier.resize(size_t(N0 + n_tokens), 0);
+  sq.loc.resize(size_t(N0 + n_tokens), -1);
+  sq.N = N0 + n_tokens;
+  if (is_prompt) sq.prompt_len += n_tokens;
+  std::vector<int32_t> locs;
+  if (!place(h, sq, seq, 0, pos, &locs)) return fail(h, TKV_ERR_INTERNAL, "T0 placement failed after the capacity check");
+  char* arena = h->P(y.p_arena);
+  const size_t loff = y.arena_bytes - align_up(size_t(y.maxtok) * 4);
+  std::memcpy(arena + loff, locs.data(), locs.size() * 4);
+  int32_t* dl = reinterpret_cast<int32_t*>(h->D(y.o_locs));
+  CK(h, cudaMemcpyAsync(dl, arena + loff, locs.size() * 4, cudaMemcpyHostToDevice, h->cs));
+  PrefillParams pp{};
+  pp.L = y.L; pp.Hkv = y.Hkv; pp.D = y.D; pp.esz = y.esz; pp.n = n_tokens;
+  pp.k = static_cast<const char*>(k); pp.v = static_cast<const char*>(v); pp.loc = dl;
+  pp.pool0 = h->D(y.o_pool0); pp.layer_bytes = y.cap[0] * y.plb[0]; pp.page_bytes = y.plb[0];
+  CK(h, launch_prefill(pp, h->cs));
+  if (tkv_status st = upload_metadata(h)) return st;
+  return sync_all(h);
+}
+
+tkv_status tkv_decode_step(tkv_handle h, const void* q, const void* k_new, const void* v_new, void* out) {
+  if (tkv_status st = check_usable(h)) return st;
+  if (!q || !k_new || !v_new || !out) return fail(h, TKV_ERR_INVALID_ARG, "null pointer");
+  if (h->seqs.empty()) return fail(h, TKV_ERR_STATE, "no sequence: append a prefill first");
+  return decode_step_device(h, q, k_new, v_new, out);
+}
+
+tkv_status tkv_decode_step_host(tkv_handle h, const void* q, const void* k_new, const void* v_new, void* out) {
+  if (tkv_status st = check_usable(h)) return st;
+  if (!q || !k_new || !v_new || !out) return fail(h, TKV_ERR_INVALID_ARG, "null pointer");
+  if (h->seqs.empty()) return fail(h, TKV_ERR_STATE, "no sequence: append a prefill first");
+  const Layout& y = h->y;
+  const int B = static_cast<int>(h->seqs.size());
+  const size_t qb = size_t(B) * y.L * y.Hq * y.D * y.esz;
+  const size_t kb = size_t(B) * y.L * y.Hkv * y.D * y.esz;
+  char* io = h->D(y.o_io);
+  char* dq = io + y.io_q;
+  char* dk = io + y.io_k;
+  char* dv = dk + align_up(size_t(y.maxb) * y.L * y.Hkv * y.D * y.esz);
+  char* dout = io + y.io_out;
+  CK(h, cudaMemcpyAsync(dq, q, qb, cudaMemcpyHostToDevice, h->cs));
+  CK(h, cudaMemcpyAsync(dk, k_new, kb, cudaMemcpyHostToDevice, h->cs));
+  CK(h, cudaMemcpyAsync(dv, v_new, kb, cudaMemcpyHostToDevice, h->cs));
+  if (tkv_status st = decode_step_device(h, dq, dk, dv, dout)) return st;
+  CK(h, cudaMemcpyAsync(out, dout, qb, cudaMemcpyDeviceToHost, h->cs));
+  CK(h, cudaStreamSynchronize(h->cs));
+  return TKV_OK;
+}
+
+tkv_status tkv_reclassify(tkv_handle h) {
+  if (tkv_status st = check_usable(h)) return st;
+  return do_reclassify(h);
+}
+
+tkv_status tkv_prefetch(tkv_handle h, int32_t layer, int32_t slot) {
+  if (tkv_status st = check_usable(h)) return st;
+  if (layer < 0 || layer >= h->y.L || slot < 0 || slot > 1) return fail(h, TKV_ERR_INVALID_ARG, "bad layer or slot");
+  return enqueue_prefetch(h, layer, slot);
+}
+
+tkv_status tkv_synchronize(tkv_handle h) {
+  if (tkv_status st = check_usable(h)) return st;
+  return sync_all(h);
+}
+
+tkv_status tkv_num_sequences(tkv_handle h, int32_t* n) {
+  if (!h || !n) return fail(h, TKV_ERR_INVALID_ARG, "null argument");
+  *n = static_cast<int32_t>(h->seqs.size());
+  return TKV_OK;
+}
+
+tkv_status tkv_seq_len(tkv_handle h, int32_t seq, int64_t* n) {
+  if (!h || !n) return fail(h, TKV_ERR_INVALID_ARG, "null argument");
+  if (tkv_status st = seq_ok(h, seq)) return st;
+  *n = h->seqs[seq].N;
+  return TKV_OK;
+}
+
+tkv_status tkv_get_scores(tkv_handle h, int32_t seq, double* host_out, int64_t n) {
+  if (tkv_status st = check_usable(h)) return st;
+  if (tkv_status st = seq_ok(h, seq)) return st;
+  if (!host_out || n < 0 || n > h->seqs[seq].N) return fail(h, TKV_ERR_INVALID_ARG, "bad output or n");
+  if (tkv_status st = sync_all(h)) return st;
+  CK(h, cudaMemcpy(host_out, h->D(h->y.o_s) + size_t(seq) * h->y.maxtok * 8, size_t(n) * 8, cudaMemcpyDeviceToHost));
+  return TKV_OK;
+}
+
+tkv_status tkv_set_scores(tkv_handle h, int32_t seq, const double* host_in, int64_t n) {
+  if (tkv_status st = check_usable(h)) return st;
+  if (tkv_status st = seq_ok(h, seq)) return st;
+  if (!host_in || n < 0 || n > h->seqs[seq].N) return fail(h, TKV_ERR_INVALID_ARG, "bad input or n");
+  std::vector<double> s(host_in, host_in + n);
+  for (double& x : s) {
+    if (std::isnan(x)) return fail(h, TKV_ERR_INVALID_ARG, "NaN score");
+    if (x == 0.0) x = 0.0;
+  }
+  if (tkv_status st = sync_all(h)) return st;
+  CK(h, cudaMemcpy(h->D(h->y.o_s) + size_t(seq) * h->y.maxtok * 8, s.data(), size_t(n) * 8, cudaMemcpyHostToDevice));
+  return TKV_OK;
+}
+
+tkv_status tkv_get_tiers(tkv_handle h, int32_t seq, uint8_t* host_out, int64_t n) {
+  if (!h) return fail(nullptr, TKV_ERR_INVALID_ARG, "null handle");
+  if (tkv_status st = seq_ok(h, seq)) return st;
+  if (!host_out || n < 0 || n > h->seqs[seq].N) return fail(h, TKV_ERR_INVALID_ARG, "bad output or n");
+  std::memcpy(host_out, h->seqs[seq].tier.data(), size_t(n));
+  return TKV_OK;
+}
+
+tkv_status tkv_get_page_table(tkv_handle h, int32_t seq, int32_t tier, int32_t* pages, uint16_t* valid_mask,
+                              int32_t* positions, int64_t cap, int64_t* n_out) {
+  if (!h || !n_out) return fail(h, TKV_ERR_INVALID_ARG, "null argument");
+  if (tkv_status st = seq_ok(h, seq)) return st;
+  if (tier < 0 || tier > 2) return fail(h, TKV_ERR_INVALID_ARG, "tier must be 0, 1 or 2");
+  const std::vector<int32_t>& pl = h->seqs[seq].pages[tier];
+  *n_out = int64_t(pl.size());
+  const int64_t n = std::min<int64_t>(cap, int64_t(pl.size()));
+  for (int64_t i = 0; i < n; ++i) {
+    const int32_t pg = pl[i];
+    if (pages) pages[i] = pg;
+    if (valid_mask) valid_mask[i] = static_cast<uint16_t>(h->mask[tier][pg]);
+    if (positions)
+      for (int j = 0; j < kPage; ++j) positions[i * kPage + j] = h->posmap[tier][size_t(pg) * kPage + j];
+  }
+  return TKV_OK;
+}
+
+tkv_status tkv_get_t2_row(tkv_handle h, int32_t seq, int64_t pos, int8_t* codes, void* scales) {
+  if (tkv_status st = check_usable(h)) return st;
+  if (tkv_status st = seq_ok(h, seq)) return st;
+  const Seq& sq = h->seqs[seq];
+  if (pos < 0 || pos >= sq.N || sq.tier[pos] != 2) return fail(h, TKV_ERR_INVALID_ARG, "position %lld is not in T2", (long long)pos);
+  if (!codes || !scales) return fail(h, TKV_ERR_INVALID_ARG, "null output");
+  if (tkv_status st = sync_all(h)) return st;
+  const Layout& y = h->y;
+  const int64_t page = sq.loc[pos] / kPage, slot = sq.loc[pos] % kPage;
+  const bool per_head = h->cfg.t2_scale_gran == TKV_SCALE_PER_TOKEN_HEAD;
+  for (int l = 0; l < y.L; ++l) {
+    const char* pg = h->P(y.p_pool2c) + (size_t(l) * y.cap[2] + page) * y.plb[2];
+    const char* sc = h->P(y.p_pool2s) + (size_t(l) * y.cap[2] + page) * y.scale_rec;
+    for (int kv = 0; kv < 2; ++kv) {
+      for (int hh = 0; hh < y.Hkv; ++hh)
+        std::memcpy(codes + ((size_t(l) * 2 + kv) * y.Hkv + hh) * y.D,
+                    pg + ((size_t(hh) * 2 + kv) * kPage + slot) * y.D, size_t(y.D));
+      if (per_head) {
+        for (int hh = 0; hh < y.Hkv; ++hh)
+          std::memcpy(static_cast<char*>(scales) + ((size_t(l) * 2 + kv) * y.Hkv + hh) * 2,
+                      sc + ((size_t(hh) * 2 + kv) * kPage + slot) * 2, 2);
+      } else {
+        std::memcpy(static_cast<char*>(scales) + (size_t(l) * 2 + kv) * 4, sc + (size_t(kv) * kPage + slot) * 4, 4);
+      }
+    }
+  }
+  return TKV_OK;
+}
+
+tkv_status tkv_get_kv_row(tkv_handle h, int32_t seq, int64_t pos, void* k, void* v) {
+  if (tkv_status st = check_usable(h)) return st;
+  if (tkv_status st = seq_ok(h, seq)) return st;
+  const Seq& sq = h->seqs[seq];
+  if (pos < 0 || pos >= sq.N || sq.tier[pos] > 1) return fail(h, TKV_ERR_INVALID_ARG, "position %lld is not in T0 or T1", (long long)pos);
+  if (!k || !v) return fail(h, TKV_ERR_INVALID_ARG, "null output");
+  if (tkv_status st = sync_all(h)) return st;
+  const Layout& y = h->y;
+  const int t = sq.tier[pos];
+  const int64_t page = sq.loc[pos] / kPage, slot = sq.loc[pos] % kPage;
+  const size_t rb = size_t(y.D) * y.esz;
+  for (int l = 0; l < y.L; ++l)
+    for (int kv = 0; kv < 2; ++kv)
+      for (int hh = 0; hh < y.Hkv; ++hh) {
+        char* dst = static_cast<char*>(kv ? v : k) + (size_t(l) * y.Hkv + hh) * rb;
+        const size_t off = (size_t(l) * y.cap[t] + page) * y.plb[t] + ((size_t(hh) * 2 + kv) * kPage + slot) * rb;
+        if (t == 0)
+          CK(h, cudaMemcpy(dst, h->D(y.o_pool0) + off, rb, cudaMemcpyDeviceToHost));
+        else
+          std::memcpy(dst, h->P(y.p_pool1) + off, rb);
+      }
+  return TKV_OK;
+}
+
+tkv_status tkv_get_stats(tkv_handle h, tkv_stats* out) {
+  if (!h || !out) return fail(h, TKV_ERR_INVALID_ARG, "null argument");
+  if (!h->broken) {
+    if (tkv_status st = sync_all(h)) return st;
+  }
+  for (int t = 0; t < 4; ++t) h->stats.tier_counts[t] = 0;
+  for (const Seq& sq : h->seqs)
+    for (int64_t i = 0; i < sq.N; ++i) h->stats.tier_counts[sq.tier[i]] += 1;
+  *out = h->stats;
+  return TKV_OK;
+}
+
+tkv_status tkv_reset_stats(tkv_handle h) {
+  if (!h) return fail(nullptr, TKV_ERR_INVALID_ARG, "null handle");
+  if (!h->broken) {
+    if (tkv_status st = sync_all(h)) return st;
+  }
+  h->stats = tkv_stats{};
+  return TKV_OK;
+}
+
+const char* tkv_last_error(tkv_handle h) {
+  if (h) return h->err.c_str();
+  return g_last_error.c_str();
+}
+
+// ------------------------------------------------------------ stateless kernels
+namespace {
+struct PagedScratch {
+  size_t o_err, o_part_o, o_part_m, o_part_z, o_spill, o_tickets, bytes;
+  int64_t max_chunks, spill_stride;
+};
+PagedScratch paged_scratch(int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int32_t max_pages) {
+  PagedScratch s{};
+  const int G = Hq / Hkv;
+  s.max_chunks = int64_t(B) * (ceil_div(max_pages, 8) + 1);
+  s.spill_stride = int64_t(max_pages) * G * kPage;
+  size_t o = 0;
+  auto take = [&](size_t bytes) { size_t at = o; o = align_up(o + bytes); return at; };
+  s.o_err = take(64);
+  s.o_part_o = take(size_t(s.max_chunks) * Hkv * G * D * 4);
+  s.o_part_m = take(size_t(s.max_chunks) * Hkv * G * 4);
+  s.o_part_z = take(size_t(s.max_chunks) * Hkv * G * 4);
+  s.o_spill = take(size_t(B) * Hkv * s.spill_stride * 4);
+  s.o_tickets = take(size_t(B) * Hkv * 4);
+  s.bytes = o;
+  return s;
+}
+}  // namespace
+
+tkv_status tkv_paged_attention_scratch_size(int32_t batch, int32_t n_q_heads, int32_t n_kv_heads,
+                                            int32_t head_dim, int32_t max_pages, size_t* scratch_bytes) {
+  if (!scratch_bytes || batch < 1 || batch > kMaxBatch || n_kv_heads < 1 || n_q_heads % n_kv_heads ||
+      max_pages < 1)
+    return fail(nullptr, TKV_ERR_INVALID_ARG, "bad paged-attention shape");
+  *scratch_bytes = paged_scratch(batch, n_q_heads, n_kv_heads, head_dim, max_pages).bytes;
+  return TKV_OK;
+}
+
+tkv_status tkv_paged_attention(int32_t batch, int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim,
+                               int32_t kv_dtype, const void* q, const void* pool, const int32_t* page_table,
+                               const uint32_t* slot_mask, const int32_t* page_counts, int32_t max_pages,
+                               void* out, float* alpha_sum, void* scratch, size_t scratch_bytes,
+                               tkv_stream stream) {
+  if (batch < 1 || batch > kMaxBatch || n_kv_heads < 1 || n_q_heads % n_kv_heads || max_pages < 1)
+    return fail(nullptr, TKV_ERR_INVALID_ARG, "bad paged-attention shape");
+  if (kv_dtype != TKV_DTYPE_F32 && kv_dtype != TKV_DTYPE_BF16) return fail(nullptr, TKV_ERR_INVALID_ARG, "kv_dtype");
+  const int G = n_q_heads / n_kv_heads;
+  if (!attention_supported(kv_dtype, G, head_dim)) return fail(nullptr, TKV_ERR_INVALID_ARG, "unsupported group size or head_dim");
+  if (!q || !pool || !page_table || !slot_mask || !page_counts || !out || !scratch)
+    return fail(nullptr, TKV_ERR_INVALID_ARG, "null pointer");
+  const PagedScratch s = paged_scratch(batch, n_q_heads, n_kv_heads, head_dim, max_pages);
+  if (scratch_bytes < s.bytes) return fail(nullptr, TKV_ERR_CAPACITY, "scratch too small: need %zu bytes", s.bytes);
+  if (reinterpret_cast<uintptr_t>(scratch) % kAlign) return fail(nullptr, TKV_ERR_INVALID_ARG, "scratch not 256-byte aligned");
+  const int esz = kv_dtype == TKV_DTYPE_BF16 ? 2 : 4;
+  AttnParams p{};
+  p.B = batch; p.Hq = n_q_heads; p.Hkv = n_kv_heads; p.D = head_dim; p.G = G;
+  p.table_stride = max_pages;
+  std::vector<int64_t> ntot(batch);
+  for (int b = 0; b < batch; ++b) {
+    if (page_counts[b] < 1 || page_counts[b] > max_pages) return fail(nullptr, TKV_ERR_INVALID_ARG, "page_counts[%d] out of 1..max_pages", b);
+    p.npages[0][b] = page_counts[b];
+    ntot[b] = page_counts[b];
+  }
+  int64_t sum = 0;
+  for (int64_t n : ntot) sum += n;
+  int64_t cp = ceil_div(sum * n_kv_heads, 4 * 2 * 152);
+  cp = std::max<int64_t>(16, std::min<int64_t>(cp, kMaxChunkPages));
+  p.chunk_pages = static_cast<int32_t>(ceil_div(cp, kAttnWarps) * kAttnWarps);
+  p.chunk_first[0] = 0;
+  for (int b = 0; b < batch; ++b) p.chunk_first[b + 1] = p.chunk_first[b] + static_cast<int32_t>(ceil_div(ntot[b], p.chunk_pages));
+  const int64_t head_full = int64_t(2) * kPage * head_dim * esz;
+  p.src[0] = PageSource{static_cast<const char*>(pool), head_full * n_kv_heads, head_full, page_table, slot_mask,
+                        nullptr, nullptr, 0, 0, SRC_FULL};
+  p.nsrc = 1;
+  p.q = q; p.q_stride_b = int64_t(n_q_heads) * head_dim;
+  p.out = out; p.out_stride_b = int64_t(n_q_heads) * head_dim;
+  p.qscale = static_cast<float>(1.4426950408889634 / std::sqrt(double(head_dim)));
+  char* sc = static_cast<char*>(scratch);
+  p.part_o = reinterpret_cast<float*>(sc + s.o_part_o);
+  p.part_m = reinterpret_cast<float*>(sc + s.o_part_m);
+  p.part_z = reinterpret_cast<float*>(sc + s.o_part_z);
+  p.spill = reinterpret_cast<float*>(sc + s.o_spill);
+  p.spill_stride = s.spill_stride;
+  p.tickets = reinterpret_cast<int32_t*>(sc + s.o_tickets);
+  p.acc = alpha_sum;
+  p.acc_stride_b = int64_t(n_kv_heads) * max_pages * kPage;
+  p.acc_stride_h = int64_t(max_pages) * kPage;
+  p.acc_by_position = 0;
+  p.err = reinterpret_cast<int32_t*>(sc + s.o_err);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemsetAsync(sc + s.o_tickets, 0, size_t(batch) * n_kv_heads * 4, st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(sc + s.o_err, 0, 64, st);
+  if (e != cudaSuccess) return fail_cuda(nullptr, "cudaMemsetAsync", e);
+  e = launch_attention(p, kv_dtype, p.chunk_first[batch], st);
+  if (e != cudaSuccess) return fail_cuda(nullptr, "attention launch", e);
+  return TKV_OK;
+}
+
+tkv_status tkv_classify_scratch_size(int32_t batch, int64_t stride, size_t* scratch_bytes) {
+  if (!scratch_bytes || batch < 1 || batch > kMaxBatch || stride < 1) return fail(nullptr, TKV_ERR_INVALID_ARG, "bad shape");
+  *scratch_bytes = align_up(size_t(batch) * stride * 8);
+  return TKV_OK;
+}
+
+tkv_status tkv_classify(int32_t batch, const double* scores, const uint8_t* old_tier, uint8_t* new_tier,
+                        int64_t stride, const int64_t* params, int32_t n_sink, int32_t recent_window,
+                        void* scratch, size_t scratch_bytes, tkv_stream stream) {
+  if (batch < 1 || batch > kMaxBatch || stride < 1 || !scores || !old_tier || !new_tier || !params || !scratch)
+    return fail(nullptr, TKV_ERR_INVALID_ARG, "bad classify arguments");
+  if (scratch_bytes < size_t(batch) * stride * 8) return fail(nullptr, TKV_ERR_CAPACITY, "scratch too small");
+  if (n_sink < 0 || recent_window < 0) return fail(nullptr, TKV_ERR_INVALID_ARG, "negative protection");
+  ClassifyParams cp{};
+  cp.B = batch;
+  cp.s = scores; cp.old_tier = old_tier; cp.new_tier = new_tier; cp.stride = stride;
+  for (int b = 0; b < batch; ++b) {
+    const int64_t* r = params + 5 * b;
+    if (r[0] < 0 || r[0] > stride || r[1] < 0 || r[2] < 0 || r[3] < 0 || r[4] < 0)
+      return fail(nullptr, TKV_ERR_INVALID_ARG, "bad params for sequence %d", b);
+    cp.N[b] = r[0]; cp.prompt_len[b] = r[1]; cp.n0[b] = r[2]; cp.n1[b] = r[3]; cp.n2[b] = r[4];
+  }
+  cp.n_sink = n_sink; cp.recent_window = recent_window;
+  cp.keys = static_cast<unsigned long long*>(scratch);
+  cp.err = nullptr;
+  cudaError_t e = launch_classify(cp, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail_cuda(nullptr, "classify launch", e);
+  return TKV_OK;
+}
+
+tkv_status tkv_quantize_rows(const void* x, int32_t kv_dtype, int64_t rows, int32_t row_len, int8_t* codes,
+                             void* scales, int32_t scale_dtype, tkv_stream stream) {
+  if (!x || !codes || !scales || rows < 0 || row_len < 1) return fail(nullptr, TKV_ERR_INVALID_ARG, "bad quantize arguments");
+  if (kv_dtype != TKV_DTYPE_F32 && kv_dtype != TKV_DTYPE_BF16) return fail(nullptr, TKV_ERR_INVALID_ARG, "kv_dtype");
+  if (scale_dtype != TKV_SCALE_F32 && scale_dtype != TKV_SCALE_F16) return fail(nullptr, TKV_ERR_INVALID_ARG, "scale_dtype");
+  cudaError_t e = launch_quantize_rows(x, kv_dtype, rows, row_len, codes, scales, scale_dtype == TKV_SCALE_F16,
+                                       static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail_cuda(nullptr, "quantize launch", e);
+  return TKV_OK;
+}
+
+}  // extern "C"

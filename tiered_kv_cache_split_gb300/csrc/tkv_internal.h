@@ -1,0 +1,144 @@
+// Internal declarations shared by the translation units of libtkv.so.
+// Not part of the public interface (include/tkv.h is).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cstddef>
+#include <cstdint>
+
+namespace tkv {
+
+constexpr int kPage = 16;          // tokens per page
+constexpr int kMaxBatch = 64;      // sequences per handle (kernel parameters carry per-sequence arrays)
+constexpr int kAttnWarps = 4;      // consumer warps per attention CTA
+constexpr int kAttnStages = 3;     // smem pages in flight per warp
+constexpr int kMaxChunkPages = 128;
+
+// Device-side error codes written into the handle's error word.
+enum DevError : int { DEV_OK = 0, DEV_TIMEOUT = 1, DEV_BAD_INDEX = 2 };
+
+enum SrcKind : int { SRC_FULL = 0, SRC_INT8 = 1 };
+
+// One page source of the attention kernel: a page pool (or one layer of it).
+struct PageSource {
+  const char* base;          // page 0 of this source at the attended layer
+  int64_t page_bytes;        // bytes per page record (all KV heads)
+  int64_t head_bytes;        // bytes per KV head in a page record (its K block then V block)
+  const int32_t* table;      // [B][table_stride] page ids in page order
+  const uint32_t* mask;      // [pages] valid-slot bits
+  const int32_t* posmap;     // [pages][16] position held by each slot (-1 hole); may be null
+  const char* scales;        // int8 sources: scale records of page 0
+  int64_t scale_page_bytes;  // bytes per page of scale records
+  int32_t scale_per_head;    // 0: [2][16] float32 per page; 1: [Hkv][2][16] float16
+  int32_t kind;              // SrcKind
+};
+
+struct AttnParams {
+  int32_t B, Hq, Hkv, D, G;
+  int32_t nsrc;
+  PageSource src[3];
+  int32_t table_stride;
+  int32_t npages[3][kMaxBatch];
+  int32_t chunk_first[kMaxBatch + 1];   // prefix sums of chunks per sequence
+  int32_t chunk_pages;
+  const void* q;          // element (b, h, e) at q[b * q_stride_b + h * D + e]
+  int64_t q_stride_b;
+  void* out;
+  int64_t out_stride_b;
+  float qscale;           // log2(e) / sqrt(D): logits are kept in base 2
+  float* part_o;          // [chunk * Hkv + kvh][G][D]
+  float* part_m;          // [chunk * Hkv + kvh][G]
+  float* part_z;          // [chunk * Hkv + kvh][G]
+  float* spill;           // per (b, kvh) region of spill_stride floats: [page k][G][16]
+  int64_t spill_stride;
+  int32_t* tickets;       // [B * Hkv], zero between launches
+  float* acc;             // score accumulator (may be null)
+  int64_t acc_stride_b, acc_stride_h;
+  int32_t acc_by_position;  // 1: index = position from posmap; 0: index = 16 * k + slot
+  int32_t* err;
+};
+
+// attention.cu
+cudaError_t launch_attention(const AttnParams& p, int kv_dtype, int total_chunks, cudaStream_t s);
+int attention_supported(int kv_dtype, int G, int D);
+
+// classify.cu
+struct ClassifyParams {
+  int32_t B;
+  const double* s;
+  const uint8_t* old_tier;
+  uint8_t* new_tier;
+  int64_t stride;
+  int64_t N[kMaxBatch], prompt_len[kMaxBatch], n0[kMaxBatch], n1[kMaxBatch], n2[kMaxBatch];
+  int32_t n_sink, recent_window;
+  unsigned long long* keys;  // scratch [B][stride]
+  int32_t* err;
+};
+cudaError_t launch_classify(const ClassifyParams& p, cudaStream_t s);
+
+// movement.cu
+struct AppendParams {
+  int32_t B, L, Hkv, D, esz;
+  const char* k;           // [B][L][Hkv][D]
+  const char* v;
+  char* pool0;             // T0 pool, layer-major [L][pages][Hkv][2][16][D]
+  int64_t layer_bytes;     // bytes of one layer of the T0 pool
+  int64_t page_bytes;      // bytes of one page record
+  uint32_t* mask0;
+  int32_t* posmap0;
+  int32_t* table0;
+  int32_t table_stride;
+  int32_t page[kMaxBatch], slot[kMaxBatch], np0[kMaxBatch], new_page[kMaxBatch];
+  int64_t pos[kMaxBatch];
+};
+cudaError_t launch_append(const AppendParams& p, cudaStream_t s);
+
+struct PrefillParams {
+  int32_t L, Hkv, D, esz;
+  int64_t n;               // tokens
+  const char* k;           // [L][n][Hkv][D]
+  const char* v;
+  const int32_t* loc;      // [n] page * 16 + slot
+  char* pool0;
+  int64_t layer_bytes, page_bytes;
+};
+cudaError_t launch_prefill(const PrefillParams& p, cudaStream_t s);
+
+// A token whose tier changes; loc = page * 16 + slot in that tier's pool.
+struct Mover {
+  int32_t b, src_tier, src_loc, dst_tier, dst_loc, temp_row;
+};
+
+struct TierPools {
+  char* base[3];           // layer-major page pools (T1, T2 in host memory, device-mapped)
+  int64_t layer_bytes[3];
+  int64_t page_bytes[3];   // page record bytes (T2: int8 codes)
+  char* t2_scales;         // layer-major scale records
+  int64_t t2_scale_layer_bytes, t2_scale_page_bytes;
+  int32_t scale_per_head, scale_f16;
+};
+
+enum MoveMode : int { MOVE_DIRECT = 0, MOVE_GATHER = 1, MOVE_SCATTER = 2 };
+
+struct MoveParams {
+  int32_t L, Hkv, D, kv_dtype;
+  TierPools pools;
+  char* temp;              // [rows][L][2][Hkv][D] in the KV dtype
+  int32_t mode;
+};
+cudaError_t launch_move(const MoveParams& p, const Mover* movers, int64_t count, cudaStream_t s);
+
+struct FoldParams {
+  int32_t B, Hkv;
+  int64_t N[kMaxBatch];
+  double* s;               // [B][stride]
+  float* acc;              // [B][Hkv][stride]
+  int64_t stride;
+  double inv_lh;           // 1 / (L * Hq)
+};
+cudaError_t launch_fold(const FoldParams& p, cudaStream_t s);
+
+cudaError_t launch_quantize_rows(const void* x, int kv_dtype, int64_t rows, int row_len,
+                                 int8_t* codes, void* scales, int scale_f16, cudaStream_t s);
+
+}  // namespace tkv
