@@ -1,0 +1,352 @@
+"""Benchmark of the tiered KV-cache decode step on GB300.
+
+One step = one decode step of every request through all layers: append the new
+token to T0, prefetch T1 and T2 of each layer on the copy stream, split-K
+attention over T0 + T1 + T2 with the cumulative score fused into the softmax
+epilogue, the float64 score fold, and (every Delta steps) tier reassignment with
+differential data movement. The default workload is the batch-32 serving case:
+32 requests of 1k-8k tokens (uniform), 28 layers, 28 query / 4 KV heads,
+d = 128, bf16, 16-token pages, budgets T0/T1/T2/T3 = 40/40/10/10, Delta = 64.
+
+Prints one JSON line (rank 0). `--impl reference` times the CPU oracle instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode steps/s (KV-read GB/s as fraction of HBM peak in roofline)"
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def _workload(name):
+    from synth import WORKLOADS
+    return WORKLOADS[name]
+
+
+def _config(w, n_ranks):
+    lens = w.context_lens()
+    return {"workload": w.name, "batch": w.batch, "layers": w.n_layers, "q_heads": w.n_q_heads,
+            "kv_heads": w.n_kv_heads, "head_dim": w.head_dim, "kv_dtype": w.kv_dtype,
+            "context_tokens": {"min": min(lens), "max": max(lens), "mean": sum(lens) / len(lens)},
+            "budgets": list(w.budgets), "budget_mode": w.budget_mode, "delta": w.reclassify_interval,
+            "page_size": 16, "parallelism": f"replicas x{n_ranks}",
+            "l2": "inputs larger than L2: each step streams GBs of KV through the 129 MB L2"}
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        if self.path and os.path.exists(self.path):
+            for line in open(self.path):
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+            os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ------------------------------------------------------------------ dist
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def _barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def _max_over_ranks(ws, x, device):
+    if ws == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ GPU arm
+def run_gpu(args):
+    import torch
+    ws, rank, local = _dist()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", init_method="env://")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    from tiered_kv_cache_split_gb300 import TieredKVCache
+
+    w = _workload(args.workload)
+    delta = w.reclassify_interval
+    K, W = args.steps, args.warmup
+    # untimed prefix: reach the tiered steady state (first reassignment at step
+    # Delta), then W warm-up steps, and align so the timed window ends on a
+    # multiple of Delta: it then holds ceil(K / Delta) reassignments.
+    untimed = math.ceil((delta + W + K) / delta) * delta - K
+    e2e_untimed = math.ceil(K / delta) * delta - K   # the e2e window also ends on a multiple of Delta
+    total_steps = untimed + K + e2e_untimed + K
+    w = w.replace(n_steps=total_steps + 1)
+
+    cache = TieredKVCache.from_workload(w, timing=True)
+    t0 = time.time()
+    for b in range(w.batch):
+        n, P = w.context_lens()[b], w.prompt_lens()[b]
+        for lo, hi, prompt in ((0, P, True), (P, n, False)):
+            if hi > lo:
+                cache.append(b, w.kv_layers("k", b, lo, hi, dev), w.kv_layers("v", b, lo, hi, dev), prompt)
+    torch.cuda.synchronize()
+    prefill_s = time.time() - t0
+
+    def inputs(t):
+        return w.queries(t, dev), w.kv_new("k", t, dev), w.kv_new("v", t, dev)
+
+    out = None
+    step = 0
+    for _ in range(untimed):
+        step += 1
+        q, k, v = inputs(step)
+        out = cache.decode_step(q, k, v, out)
+    timed_inputs = [inputs(step + i + 1) for i in range(K)]
+    torch.cuda.synchronize()
+    cache.reset_stats()
+    stream = cache.compute
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        _barrier(ws)
+        torch.cuda.synchronize()
+        ev0.record(stream)
+        for i in range(K):
+            q, k, v = timed_inputs[i]
+            out = cache.decode_step(q, k, v, out)
+        ev1.record(stream)
+        cache.synchronize()
+        torch.cuda.synchronize()
+        _barrier(ws)
+    step += K
+    ms = ev0.elapsed_time(ev1)
+    st = cache.stats()
+    ms_max = _max_over_ranks(ws, ms, dev)
+    del timed_inputs
+
+    # ---- end to end through the host-buffer entry point (pinned host in and out)
+    for _ in range(e2e_untimed):
+        step += 1
+        q, k, v = inputs(step)
+        out = cache.decode_step(q, k, v, out)
+    host = []
+    for i in range(K):
+        q, k, v = inputs(step + i + 1)
+        host.append((q.cpu().pin_memory(), k.cpu().pin_memory(), v.cpu().pin_memory()))
+    out_h = torch.empty_like(host[0][0]).pin_memory()
+    cache.synchronize()
+    _barrier(ws)
+    t0 = time.perf_counter()
+    for i in range(K):
+        q, k, v = host[i]
+        cache.decode_step_host(q, k, v, out_h)
+    cache.synchronize()
+    e2e_s = time.perf_counter() - t0
+    _barrier(ws)
+    e2e_s = _max_over_ranks(ws, e2e_s, dev)
+    h2d = sum(x.numel() * x.element_size() for x in host[0])
+    d2h = out_h.numel() * out_h.element_size()
+
+    # ---- host link probe: a plain pinned host -> device copy
+    probe_h = torch.empty(2 << 30, dtype=torch.uint8).pin_memory()
+    probe_d = torch.empty_like(probe_h, device=dev)
+    probe_d.copy_(probe_h, non_blocking=True)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    best = 1e30
+    for _ in range(3):
+        e0.record()
+        probe_d.copy_(probe_h, non_blocking=True)
+        e1.record()
+        torch.cuda.synchronize()
+        best = min(best, e0.elapsed_time(e1))
+    link_gbs = probe_h.numel() / best / 1e6
+    del probe_h, probe_d
+
+    peak, peak_kind = _peaks()
+    attn_ms = st["attn_ms"] / max(st["attn_launches"], 1)
+    bytes_per_launch = st["attn_bytes"] / max(st["attn_launches"], 1)
+    achieved = bytes_per_launch / (attn_ms * 1e6) if attn_ms > 0 else 0.0
+    prefetch_gbs = st["prefetch_bytes"] / (st["prefetch_ms"] * 1e6) if st["prefetch_ms"] > 0 else None
+    launches = K * (w.n_layers + 2) + st["reclassifies"] * 4
+    clocks = clk.summary()
+    traffic = None
+    tp = os.path.join(ROOT, "profiles", "attention_traffic.json")
+    if os.path.exists(tp):
+        traffic = json.load(open(tp)).get(w.name)
+    line = {
+        "metric": METRIC, "value": ws * K / (ms_max / 1000.0), "unit": "steps/s", "n_gpus": ws,
+        "steps": K, "warmup": W, "ms_per_step": ms_max / K, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": w.kv_dtype, "data": "synthetic",
+        "config": _config(w, ws),
+        "roofline": {"bound": "hbm", "kernel": "attn_split_kernel", "achieved": achieved, "peak": peak,
+                     "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": traffic, "bytes_per_launch": bytes_per_launch,
+                     "launch_ms": attn_ms},
+        "kv_read_gbs": achieved,
+        "link": {"prefetch_gbs": prefetch_gbs, "probe_h2d_gbs": link_gbs,
+                 "frac": (prefetch_gbs / link_gbs) if prefetch_gbs else None,
+                 "prefetch_bytes_per_step": st["prefetch_bytes"] / K},
+        "reclassify_ms": st["reclassify_ms"] / max(st["reclassifies"], 1) if st["reclassifies"] else None,
+        "reclassifies_in_timed_region": st["reclassifies"],
+        "tier_counts": st["tier_counts"],
+        "e2e": {"value": ws * K / e2e_s, "unit": "steps/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches,
+        "clocks": clocks,
+        "prefill_s": prefill_s,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
+    cache.close()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ CPU oracle
+_ORACLE_CHILD = r"""
+import json, sys, time
+sys.path.insert(0, {root!r})
+import numpy as np
+from synth import WORKLOADS
+from oracle import OracleCache
+from oracle.classify import T0
+w = WORKLOADS[{name!r}]
+budget = {budget}
+# one request at a time at the workload's full shape: prefill, then decode
+# steps of the oracle as it stands, until the time budget is used
+lens = w.context_lens()
+order = sorted(range(w.batch), key=lambda b: lens[b])
+b = order[len(order) // 2]
+one = w.replace(batch=1, context=("fixed", lens[b]), n_steps=64)
+oc = OracleCache.from_workload(one)
+n = lens[b]
+oc.append(0, one.kv_layers("k", 0, 0, n).float().numpy(), one.kv_layers("v", 0, 0, n).float().numpy(), False)
+t0 = time.perf_counter()
+steps = 0
+while time.perf_counter() - t0 < budget and steps < 64:
+    steps += 1
+    oc.decode_step(one.queries(steps).float().numpy(), one.kv_new("k", steps).float().numpy(), one.kv_new("v", steps).float().numpy())
+el = time.perf_counter() - t0
+print(json.dumps({{"seconds": el, "request_steps": steps, "tokens": n}}))
+"""
+
+
+def cpu_baseline(w, seconds):
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               CUDA_VISIBLE_DEVICES="")
+    code = _ORACLE_CHILD.format(root=ROOT, name=w.name, budget=seconds)
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env,
+                       timeout=seconds * 10 + 600)
+    if r.returncode != 0:
+        return {"value": None, "unit": "steps/s", "cores": 1, "kind": "oracle",
+                "sample": "failed: " + r.stderr.strip().splitlines()[-1] if r.stderr else "failed"}
+    d = json.loads(r.stdout.strip().splitlines()[-1])
+    # one full-batch step = w.batch request-steps (the sampled request is the median length)
+    per_request_step = d["seconds"] / d["request_steps"]
+    return {"value": 1.0 / (per_request_step * w.batch), "unit": "steps/s", "cores": 1, "kind": "oracle",
+            "sample": f"{d['request_steps']} decode steps of one median-length request "
+                      f"({d['tokens']} tokens, all {w.n_layers} layers) in {d['seconds']:.1f} s, "
+                      f"scaled to the {w.batch}-request batch"}
+
+
+def run_reference(args):
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return
+    w = _workload(args.workload)
+    K = args.steps
+    cb = cpu_baseline(w, args.cpu_seconds)
+    v = cb["value"]
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "steps/s", "n_gpus": ws,
+            "steps": K, "warmup": args.warmup, "ms_per_step": 1000.0 / v if v else None,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": _config(w, ws), "cpu_baseline": cb,
+            "e2e": {"value": v, "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=64)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["gpu", "reference"], default="gpu")
+    ap.add_argument("--workload", default="batch32")
+    ap.add_argument("--cpu-seconds", type=float, default=20.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

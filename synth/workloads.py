@@ -153,21 +153,31 @@ class Workload:
 
     def kv_new(self, which: str, step: int, device="cpu") -> torch.Tensor:
         """[B, L, Hkv, d]: the key or value appended at decode step `step`."""
-        out = torch.empty(self.batch, self.n_layers, self.n_kv_heads, self.head_dim,
-                          dtype=self.torch_dtype, device=device)
+        d, hk, L = self.head_dim, self.n_kv_heads, self.n_layers
+        out = torch.empty(self.batch, L, hk, d, dtype=self.torch_dtype, device=device)
+        stream = S_K if which == "k" else S_V
+        layers = torch.arange(L, dtype=torch.int64).view(L, 1)
+        heads = torch.arange(hk, dtype=torch.int64).view(1, hk)
         for b, p in enumerate(self.step_positions(step)):
-            for layer in range(self.n_layers):
-                out[b, layer] = self.kv(which, b, layer, p, p + 1, device)[:, 0, :]
+            if which == "k" and self.key_scale[0] == "delayed_spikes":
+                for layer in range(L):
+                    out[b, layer] = self.kv(which, b, layer, p, p + 1, device)[:, 0, :]
+                continue
+            z = normal_f32(self.seed, stream, (b << 16) | layers, heads, p * d, d, device)  # [L, Hkv, d]
+            if which == "k":
+                z = z * self.key_scales(b)[p].to(device)
+            out[b] = z.to(self.torch_dtype)
         return out
 
     # --------------------------------------------------------------- queries
     def queries(self, step: int, device="cpu") -> torch.Tensor:
         """[B, L, Hq, d]: the queries of decode step `step` (from 1)."""
         B, L, H, d = self.batch, self.n_layers, self.n_q_heads, self.head_dim
-        z = normal_f32(self.seed, S_Q, step, 0, 0, B * L * H * d, "cpu").reshape(B, L, H, d)
         if self.key_scale[0] == "delayed_spikes":
-            z = _delayed_spike_queries(self, step, z)
-        return z.to(self.torch_dtype).to(device)
+            z = normal_f32(self.seed, S_Q, step, 0, 0, B * L * H * d, "cpu").reshape(B, L, H, d)
+            return _delayed_spike_queries(self, step, z).to(self.torch_dtype).to(device)
+        z = normal_f32(self.seed, S_Q, step, 0, 0, B * L * H * d, device).reshape(B, L, H, d)
+        return z.to(self.torch_dtype)
 
     # ----------------------------------------------------------------- scores
     def synthetic_scores(self, b: int, n: int, ties: bool = True) -> torch.Tensor:

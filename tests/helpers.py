@@ -25,7 +25,7 @@ def prefill_oracle(oc, w, values=True):
         for lo, hi, prompt in ((0, P, True), (P, n, False)):
             if hi > lo:
                 if values:
-                    oc.append(b, w.kv_layers("k", b, lo, hi).numpy(), w.kv_layers("v", b, lo, hi).numpy(), prompt)
+                    oc.append(b, w.kv_layers("k", b, lo, hi).float().numpy(), w.kv_layers("v", b, lo, hi).float().numpy(), prompt)
                 else:
                     oc.append(b, None, None, prompt, n=hi - lo)
 

@@ -30,7 +30,7 @@ def _run(w, steps, check_rows=True, **kw):
     for t in range(1, steps + 1):
         q, kn, vn = w.queries(t), w.kv_new("k", t), w.kv_new("v", t)
         out = cache.decode_step(q.to(DEV), kn.to(DEV), vn.to(DEV))
-        ref, deltas = oc.decode_step(q.numpy(), kn.numpy(), vn.numpy())
+        ref, deltas = oc.decode_step(q.float().numpy(), kn.float().numpy(), vn.float().numpy())
         err = float(np.max(np.abs(out.float().cpu().numpy() - ref)))
         worst = max(worst, err)
         assert err <= OUT_ATOL, f"step {t}: output error {err}"
