@@ -134,6 +134,8 @@ def run_gpu(args):
     from tiered_kv_cache_split_gb300 import TieredKVCache
 
     w = _workload(args.workload)
+    if args.layers:
+        w = w.replace(n_layers=args.layers)   # a smaller case of the same kernels, for profiling
     delta = w.reclassify_interval
     K, W = args.steps, args.warmup
     # untimed prefix: reach the tiered steady state (first reassignment at step
@@ -339,6 +341,7 @@ def main():
     ap.add_argument("--workload", default="batch32")
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", type=int, default=0, help="override the layer count (profiling a small case)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -456,9 +456,10 @@ __global__ void __launch_bounds__(kAttnWarps * 32)
 #pragma unroll
       for (int t = 0; t < S::NL; ++t) pv[t] = 0.f;
     }
+    // with one head, lanes c and c ^ 1 hold the same logits: sum each row once
 #pragma unroll
     for (int m = 1; m < 8; m <<= 1)
-      if (m < 8 / S::GP) psum += __shfl_xor_sync(kFull, psum, m);
+      if (m < 8 / S::GP && !(S::NV < 8 && m == 1)) psum += __shfl_xor_sync(kFull, psum, m);
     psum += __shfl_xor_sync(kFull, psum, 8);
     psum += __shfl_xor_sync(kFull, psum, 16);
     z_run = z_run * corr + psum;
