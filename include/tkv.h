@@ -203,6 +203,31 @@ TKV_API tkv_status tkv_paged_attention(int32_t batch, int32_t n_q_heads, int32_t
                                float* alpha_sum, void* scratch, size_t scratch_bytes,
                                tkv_stream stream);
 
+/* Allocation-free form of tkv_paged_attention. The paper has no counterpart:
+ * this entry point exists for callers that cannot call cudaMalloc — for
+ * example an inference-engine plugin whose per-step hook must not allocate, or
+ * a process whose framework has already reserved all device memory for its own
+ * pool — and so cannot provide the scratch buffer tkv_paged_attention needs.
+ * Arguments are those of tkv_paged_attention without scratch and
+ * scratch_bytes; the caller still passes every input and output.
+ *   Scratch: a fixed 16 MiB array in the library's device code, which every
+ *   GPU that loads the library holds until the process exits. Shapes whose
+ *   scratch (tkv_paged_attention_scratch_size) exceeds 16 MiB are rejected
+ *   with TKV_ERR_CAPACITY and nothing is launched.
+ *   Set-up: the first call on a device looks up the array's device address
+ *   (cudaGetSymbolAddress, with that device current); make that first call
+ *   before any stream capture.
+ *   Sharing: every call on a device uses the same array and the array keeps
+ *   the last call's contents; each call clears the parts that must start at
+ *   zero. Calls that overlap on the GPU (other streams, other threads) race on
+ *   it: serialise them. */
+TKV_API tkv_status tkv_paged_attention_noalloc(int32_t batch, int32_t n_q_heads, int32_t n_kv_heads,
+                                               int32_t head_dim, int32_t kv_dtype, const void* q,
+                                               const void* pool, const int32_t* page_table,
+                                               const uint32_t* slot_mask, const int32_t* page_counts,
+                                               int32_t max_pages, void* out, float* alpha_sum,
+                                               tkv_stream stream);
+
 /* Tier reassignment of Methodology 1 for B sequences (device buffers):
  *   scores   double [B][stride], old_tier uint8 [B][stride], new_tier uint8 [B][stride]
  *   params   HOST int64 [B][5] = {N, prompt_len, n0, n1, n2} per sequence

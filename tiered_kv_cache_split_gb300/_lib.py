@@ -72,6 +72,8 @@ _SIGS = {
     "tkv_paged_attention_scratch_size": [c_i32, c_i32, c_i32, c_i32, c_i32, ctypes.POINTER(c_sz)],
     "tkv_paged_attention": [c_i32, c_i32, c_i32, c_i32, c_i32, c_vp, c_vp, c_vp, c_vp, c_vp, c_i32,
                             c_vp, c_vp, c_vp, c_sz, c_vp],
+    "tkv_paged_attention_noalloc": [c_i32, c_i32, c_i32, c_i32, c_i32, c_vp, c_vp, c_vp, c_vp, c_vp, c_i32,
+                                    c_vp, c_vp, c_vp],
     "tkv_classify_scratch_size": [c_i32, c_i64, ctypes.POINTER(c_sz)],
     "tkv_classify": [c_i32, c_vp, c_vp, c_vp, c_i64, c_vp, c_i32, c_i32, c_vp, c_sz, c_vp],
     "tkv_quantize_rows": [c_vp, c_i32, c_i64, c_i32, c_vp, c_vp, c_i32, c_vp],

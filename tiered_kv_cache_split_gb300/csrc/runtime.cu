@@ -23,6 +23,7 @@
 #include <cstdio>
 #include <cstring>
 #include <functional>
+#include <mutex>
 #include <new>
 #include <queue>
 #include <string>
@@ -1182,6 +1183,51 @@ tkv_status tkv_paged_attention(int32_t batch, int32_t n_q_heads, int32_t n_kv_he
   e = launch_attention(p, kv_dtype, p.chunk_first[batch], st);
   if (e != cudaSuccess) return fail_cuda(nullptr, "attention launch", e);
   return TKV_OK;
+}
+
+// ------------------------------------------------------------ allocation-free form
+// For callers that cannot allocate device memory: the scratch of the paged
+// attention lives in a fixed array of this file, set up once per device.
+}  // extern "C"
+namespace {
+constexpr size_t kStaticScratchBytes = size_t(16) << 20;  // 16 MiB per device
+__device__ __align__(256) char g_static_scratch[kStaticScratchBytes];
+constexpr int kMaxDevices = 256;
+std::mutex g_static_mu;
+void* g_static_addr[kMaxDevices] = {};
+}  // namespace
+extern "C" {
+
+tkv_status tkv_paged_attention_noalloc(int32_t batch, int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim,
+                                       int32_t kv_dtype, const void* q, const void* pool,
+                                       const int32_t* page_table, const uint32_t* slot_mask,
+                                       const int32_t* page_counts, int32_t max_pages, void* out,
+                                       float* alpha_sum, tkv_stream stream) {
+  if (batch < 1 || batch > kMaxBatch || n_kv_heads < 1 || n_q_heads % n_kv_heads || max_pages < 1)
+    return fail(nullptr, TKV_ERR_INVALID_ARG, "bad paged-attention shape");
+  const size_t need = paged_scratch(batch, n_q_heads, n_kv_heads, head_dim, max_pages).bytes;
+  if (need > kStaticScratchBytes)
+    return fail(nullptr, TKV_ERR_CAPACITY,
+                "this shape needs %zu bytes of scratch; the allocation-free form has %zu: use "
+                "tkv_paged_attention with a caller buffer", need, kStaticScratchBytes);
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail_cuda(nullptr, "cudaGetDevice", e);
+  if (dev < 0 || dev >= kMaxDevices) return fail(nullptr, TKV_ERR_INVALID_ARG, "device index out of range");
+  void* scratch = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_static_mu);
+    if (!g_static_addr[dev]) {
+      // once per device, with that device current: the array's device address
+      void* ptr = nullptr;
+      e = cudaGetSymbolAddress(&ptr, g_static_scratch);
+      if (e != cudaSuccess) return fail_cuda(nullptr, "cudaGetSymbolAddress(static scratch)", e);
+      g_static_addr[dev] = ptr;
+    }
+    scratch = g_static_addr[dev];
+  }
+  return tkv_paged_attention(batch, n_q_heads, n_kv_heads, head_dim, kv_dtype, q, pool, page_table, slot_mask,
+                             page_counts, max_pages, out, alpha_sum, scratch, kStaticScratchBytes, stream);
 }
 
 tkv_status tkv_classify_scratch_size(int32_t batch, int64_t stride, size_t* scratch_bytes) {
