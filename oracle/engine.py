@@ -153,6 +153,9 @@ class OracleCache:
                 self.alloc[x].vacate(b, [p for p in moved if old[p] == x])
             for x in (T0, T1, T2):
                 self.alloc[x].place(b, [p for p in moved if new[p] == x])
+            # T0 lives in HBM: repack it so attention reads no empty slots (the
+            # moves stay on the device; values are position-indexed here)
+            self.alloc[T0].compact(b)
             sq.tier = new
 
     def _move_values(self, sq: _Seq, pos: int, src: int, dst: int) -> None:

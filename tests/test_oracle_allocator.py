@@ -20,6 +20,21 @@ def test_hand_worked_two_pages(golden_dir):
         assert [[p, s] for p, s in a.table(int(b))] == table
 
 
+def test_hand_worked_compaction_and_page_reuse(golden_dir):
+    g = json.load(open(os.path.join(golden_dir, "allocator_compact.json")))
+    a = PagedAllocator(16)
+    moves = None
+    for op, b, pos in g["ops"]:
+        if op == "compact":
+            moves = a.compact(b)
+        else:
+            getattr(a, op)(b, pos)
+    assert [[m[0], list(m[1]), list(m[2])] for m in moves] == g["moves"]
+    for b, table in g["tables"].items():
+        assert [[p, s] for p, s in a.table(int(b))] == table
+    assert a.next_page == g["next_page"]
+
+
 def test_random_operations_keep_invariants():
     rng = np.random.default_rng(0)
     a = PagedAllocator(16)
@@ -27,7 +42,11 @@ def test_random_operations_keep_invariants():
     nxt = {0: 0, 1: 0, 2: 0}
     for _ in range(300):
         b = int(rng.integers(0, 3))
-        if held[b] and rng.random() < 0.4:
+        if held[b] and rng.random() < 0.1:
+            a.compact(b)
+            n = len(held[b])
+            assert len(a.pages[b]) == -(-n // 16)
+        elif held[b] and rng.random() < 0.4:
             out = rng.choice(sorted(held[b]), size=min(len(held[b]), int(rng.integers(1, 9))), replace=False)
             a.vacate(b, out)
             held[b] -= set(int(x) for x in out)
@@ -46,4 +65,5 @@ def test_random_operations_keep_invariants():
         occupied = [x for _, slots in table for x in slots if x >= 0]
         assert sorted(occupied) == sorted(held[b])                  # popcount == count
         assert len(occupied) == len(set(occupied))                  # no double booking
-    assert seen_pages == set(range(a.next_page))
+    assert seen_pages | set(a.free) == set(range(a.next_page))
+    assert not (seen_pages & set(a.free))

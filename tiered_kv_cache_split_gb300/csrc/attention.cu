@@ -6,27 +6,29 @@
 // heads that share that KV head, so every K/V byte is read from HBM once.
 // Pages come from up to three sources in page order: the T0 pool in HBM, the
 // T1 staging copy prefetched from pinned host DDR, and the T2 staging copy of
-// 8-bit codes (Methodology 1, 3, 4). Each of the CTA's consumer warps owns a
-// private ring of shared-memory stages filled by 1-D bulk TMA copies
-// (cp.async.bulk + mbarrier transaction counts); lane 0 of the warp issues
-// them, so no warp ever waits on another while streaming.
+// 8-bit codes (Methodology 1, 3, 4). Each consumer warp owns a private ring of
+// shared-memory stages filled by 1-D bulk TMA copies (cp.async.bulk with an
+// mbarrier transaction count, L2 evict-first); lane 0 of the warp issues them,
+// so no warp ever waits on another while streaming.
 //
-// Per page (16 tokens) a warp computes
-//   QK : lanes (r, c) = (lane / 8, lane % 8) hold 4 rows x QE elements of K
-//        in fp32 registers; each query head's slice is read from shared
-//        memory and contracted with packed fp32x2 FMAs; the 8 partial sums of
-//        a (head, row) are reduced across the 8 lanes c by a transposing
-//        butterfly that leaves each lane owning whole (head, row) logits;
-//   softmax: online max / sum per head (base-2 logits, the 1/sqrt(d) and
-//        log2(e) factors pre-applied to q); the raw logits are spilled;
-//   PV : lane l owns D/32 output elements of every head; two rows at a time
-//        are contracted with fp32x2 FMAs (row-pair accumulators).
-// The warps of a CTA then merge their (m, Z, O) in shared memory and write the
-// CTA's partial. The last CTA of each (b, KV head) to finish — found by an
-// atomic ticket, so nothing ever waits on another CTA — merges the partials
-// into the output and turns every spilled logit into its exact softmax weight
-// alpha = exp2(l - M) / Z with the global (M, Z), summing the G heads into
-// the score accumulator: the fused score epilogue.
+// Two page processors share that pipeline and the epilogue:
+//  * attn_split_mma_kernel (bf16 KV, G >= 2): the G query heads of a KV head
+//    form the M side of bf16 tensor-core MMAs (mma.sync m16n8k16, fp32
+//    accumulate): S^T = Q K^T over 16-key pages, then O^T += V^T P^T, with the
+//    QK accumulators reused as the PV operand in registers. K and V tiles are
+//    read with ldmatrix from the swizzled page layout (conflict-free). 8-bit
+//    pages are widened to bf16 in shared memory first (the codes are exact in
+//    bf16); their scales multiply the logits and the probabilities.
+//  * attn_split_fma_kernel (fp32 KV, or one query head per KV head): fp32
+//    registers and packed fp32x2 FMAs; the partial dot products of a
+//    (head, row) are reduced across 8 lanes by a transposing butterfly.
+// Per page both keep an online softmax per head in base 2 (log2(e)/sqrt(d)
+// applied to the logits) and spill the raw logits. The warps of a CTA then
+// merge (m, Z, O) in shared memory and write the CTA's partial. The last CTA
+// of each (b, KV head) to finish — found by an atomic ticket, so no CTA ever
+// waits on another — merges the partials into the output and turns every
+// spilled logit into its exact softmax weight alpha = exp2(l - M) / Z with the
+// global (M, Z), summing the G heads into the score accumulator.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -100,11 +102,41 @@ __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
   return d;
 }
 
+// D = A * B + D for one m16n8k16 bf16 tile with fp32 accumulators.
+__device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7},"
+      " {%8, %9}, {%0, %1, %2, %3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                        uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];\n"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                          uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];\n"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 __device__ __forceinline__ float i8f(uint32_t w, int byte) {
   return static_cast<float>(static_cast<int8_t>((w >> (8 * byte)) & 0xffu));
 }
+__device__ __forceinline__ int swz_chunk(int chunk, int row, int swz) { return chunk ^ (row & swz); }
 
 template <typename T, int G, int D>
 struct Shape {
@@ -112,14 +144,14 @@ struct Shape {
   static constexpr int ESZ = sizeof(T);
   static constexpr int ROWB = D * ESZ;        // bytes per full-precision row
   static constexpr int NCH = ROWB / 16;       // 16-byte chunks per row
-  static constexpr int CPL = NCH / 8;         // chunks per lane in QK
+  static constexpr int CPL = NCH / 8;         // chunks per lane in the fp32 QK
   static constexpr int EPC = 16 / ESZ;        // elements per chunk
-  static constexpr int QE = CPL * EPC;        // QK elements per lane
+  static constexpr int QE = CPL * EPC;        // fp32-QK elements per lane
   static constexpr int QP = QE / 2;
-  static constexpr int VPL = D / 32;          // PV output elements per lane
+  static constexpr int VPL = D / 32;          // fp32-PV output elements per lane
   static constexpr int BLK = kPage * ROWB;    // K (or V) block of one page and head
   static constexpr int STAGE = 2 * BLK + 128; // + T2 scale record
-  static constexpr int NV = GP * 4;           // QK partials per lane
+  static constexpr int NV = GP * 4;           // fp32-QK partials per lane
   static constexpr int NL = NV >= 8 ? NV / 8 : 1;
   static_assert(CPL >= 1 && NCH % 8 == 0, "row must hold a multiple of 8 chunks");
   static_assert(D % 32 == 0, "head_dim must be a multiple of 32");
@@ -144,13 +176,451 @@ struct Smem {
   static constexpr int TOTAL = off_bar + BARS;
 };
 
+// Resolves page-list index k of sequence b to (source, pool page id).
+__device__ __forceinline__ void page_ref(const AttnParams& p, int b, int k, int& src, int& page) {
+  int kk = k;
+  src = 0;
+  if (kk >= p.npages[0][b]) {
+    kk -= p.npages[0][b];
+    src = 1;
+    if (kk >= p.npages[1][b]) {
+      kk -= p.npages[1][b];
+      src = 2;
+    }
+  }
+  page = p.src[src].table[static_cast<int64_t>(b) * p.table_stride + kk];
+}
+
+// What a CTA needs to know about its work item.
+struct Work {
+  int b, kvh, cf, jc, nch, ntot, k0, npg;
+};
+
+__device__ __forceinline__ Work find_work(const AttnParams& p) {
+  Work wk;
+  wk.kvh = blockIdx.y;
+  const int chunk = blockIdx.x;
+  int b = 0;
+  while (b + 1 < p.B && p.chunk_first[b + 1] <= chunk) ++b;
+  wk.b = b;
+  wk.cf = p.chunk_first[b];
+  wk.jc = chunk - wk.cf;
+  wk.nch = p.chunk_first[b + 1] - wk.cf;
+  wk.ntot = p.npages[0][b] + p.npages[1][b] + p.npages[2][b];
+  wk.k0 = wk.jc * p.chunk_pages;
+  wk.npg = min(wk.k0 + p.chunk_pages, wk.ntot) - wk.k0;
+  return wk;
+}
+
+// Stages the chunk's page references and masks, and initialises each warp's barriers.
+template <typename L>
+__device__ __forceinline__ void stage_pages(const AttnParams& p, const Work& wk, char* smem) {
+  int* pg = reinterpret_cast<int*>(smem + L::off_pg);
+  uint32_t* pmask = reinterpret_cast<uint32_t*>(pg + kMaxChunkPages);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::off_bar);
+  for (int i = threadIdx.x; i < wk.npg; i += blockDim.x) {
+    int src, page;
+    page_ref(p, wk.b, wk.k0 + i, src, page);
+    pg[i] = (src << 28) | page;
+    pmask[i] = p.src[src].mask[page] & 0xffffu;
+  }
+  if ((threadIdx.x & 31) == 0) {
+    const int w = threadIdx.x >> 5;
+    for (int s = 0; s < kAttnStages; ++s) mbar_init(smem_u32(bars + w * kAttnStages + s), 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+}
+
+// Lane 0 of warp w: bulk-copy the n-th page of the warp into its ring stage.
+template <typename S>
+__device__ __forceinline__ void issue_page(const AttnParams& p, int kvh, const int* pg, int w, int n,
+                                           char* wring, uint32_t wbar, uint64_t policy) {
+  const int i = w + n * kAttnWarps;
+  const int ref = pg[i];
+  const int src = ref >> 28, page = ref & 0x0fffffff;
+  const PageSource& ps = p.src[src];
+  const char* gsrc = ps.base + static_cast<int64_t>(page) * ps.page_bytes +
+                     static_cast<int64_t>(kvh) * ps.head_bytes;
+  const int st = n % kAttnStages;
+  const uint32_t dst = smem_u32(wring + st * S::STAGE);
+  const uint32_t bar = wbar + st * 8;
+  const bool i8 = ps.kind == SRC_INT8;
+  const uint32_t bytes = i8 ? 2u * kPage * (S::ROWB / S::ESZ) : 2u * S::BLK;
+  const uint32_t sbytes = i8 ? (ps.scale_per_head ? 64u : 128u) : 0u;
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  mbar_expect_tx(bar, bytes + sbytes);
+  bulk_g2s(dst, gsrc, bytes, bar, policy);
+  if (sbytes) {
+    const char* sg = ps.scales + static_cast<int64_t>(page) * ps.scale_page_bytes +
+                     (ps.scale_per_head ? static_cast<int64_t>(kvh) * 64 : 0);
+    bulk_g2s(dst + 2 * S::BLK, sg, sbytes, bar, policy);
+  }
+}
+
+__device__ __forceinline__ float t2_scale(const char* stage_scales, bool per_head, int idx) {
+  return per_head ? __half2float(reinterpret_cast<const __half*>(stage_scales)[idx])
+                  : reinterpret_cast<const float*>(stage_scales)[idx];
+}
+
+__device__ __forceinline__ void store_out(float* p, float v) { *p = v; }
+__device__ __forceinline__ void store_out(__nv_bfloat16* p, float v) { *p = __float2bfloat16_rn(v); }
+
+// Merges the warps' (m, Z, O) — already in the MERGE area of `smem` — into the
+// CTA partial, takes the ticket, and if last runs the combine + score epilogue.
+template <typename T, int G, int D>
+__device__ void finish_cta(const AttnParams& p, const Work& wk, char* smem, int* s_last) {
+  using S = Shape<T, G, D>;
+  const int tid = threadIdx.x;
+  float* mo = reinterpret_cast<float*>(smem);           // [warps][G][D]
+  float* mm = mo + kAttnWarps * G * D;                  // [warps][GP]
+  float* mz = mm + kAttnWarps * S::GP;                  // [warps][GP]
+  const int64_t pidx = static_cast<int64_t>(wk.cf + wk.jc) * p.Hkv + wk.kvh;
+  for (int idx = tid; idx < G * D; idx += blockDim.x) {
+    const int g = idx / D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int ww = 0; ww < kAttnWarps; ++ww) M = fmaxf(M, mm[ww * S::GP + g]);
+    float o = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int ww = 0; ww < kAttnWarps; ++ww) {
+        const float mw = mm[ww * S::GP + g];
+        if (mw != -INFINITY) o += mo[(ww * G) * D + idx] * exp2f(mw - M);
+      }
+    }
+    p.part_o[pidx * G * D + idx] = o;
+  }
+  if (tid < G) {
+    float M = -INFINITY;
+    for (int ww = 0; ww < kAttnWarps; ++ww) M = fmaxf(M, mm[ww * S::GP + tid]);
+    float Z = 0.f;
+    if (M != -INFINITY)
+      for (int ww = 0; ww < kAttnWarps; ++ww) {
+        const float mw = mm[ww * S::GP + tid];
+        if (mw != -INFINITY) Z += mz[ww * S::GP + tid] * exp2f(mw - M);
+      }
+    p.part_m[pidx * G + tid] = M;
+    p.part_z[pidx * G + tid] = Z;
+  }
+
+  // ---- ticket: the last CTA of (b, kvh) runs the epilogue -----------------
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) {
+    const int t = atomicAdd(p.tickets + wk.b * p.Hkv + wk.kvh, 1);
+    *s_last = (t == wk.nch - 1);
+  }
+  __syncthreads();
+  if (!*s_last) return;
+  __threadfence();
+  if (tid == 0) p.tickets[wk.b * p.Hkv + wk.kvh] = 0;
+
+  float* cM = reinterpret_cast<float*>(smem);
+  float* cIZ = cM + S::GP;
+  if (tid < G) {
+    float M = -INFINITY;
+    for (int j = 0; j < wk.nch; ++j)
+      M = fmaxf(M, __ldcg(p.part_m + (static_cast<int64_t>(wk.cf + j) * p.Hkv + wk.kvh) * G + tid));
+    float Z = 0.f;
+    if (M != -INFINITY)
+      for (int j = 0; j < wk.nch; ++j) {
+        const int64_t pj = (static_cast<int64_t>(wk.cf + j) * p.Hkv + wk.kvh) * G + tid;
+        const float mj = __ldcg(p.part_m + pj);
+        if (mj != -INFINITY) Z += __ldcg(p.part_z + pj) * exp2f(mj - M);
+      }
+    cM[tid] = M;
+    cIZ[tid] = Z > 0.f ? 1.f / Z : 0.f;
+  }
+  __syncthreads();
+  {
+    T* out = reinterpret_cast<T*>(p.out) + static_cast<int64_t>(wk.b) * p.out_stride_b +
+             static_cast<int64_t>(wk.kvh) * G * D;
+    for (int idx = tid; idx < G * D; idx += blockDim.x) {
+      const int g = idx / D;
+      const float M = cM[g];
+      float o = 0.f;
+      if (M != -INFINITY)
+        for (int j = 0; j < wk.nch; ++j) {
+          const int64_t pj = static_cast<int64_t>(wk.cf + j) * p.Hkv + wk.kvh;
+          const float mj = __ldcg(p.part_m + pj * G + g);
+          if (mj != -INFINITY) o += __ldcg(p.part_o + pj * G * D + idx) * exp2f(mj - M);
+        }
+      store_out(out + idx, o * cIZ[g]);
+    }
+  }
+  if (p.acc != nullptr) {
+    const float* spill_b = p.spill + (static_cast<int64_t>(wk.b) * p.Hkv + wk.kvh) * p.spill_stride;
+    float* accb = p.acc + static_cast<int64_t>(wk.b) * p.acc_stride_b +
+                  static_cast<int64_t>(wk.kvh) * p.acc_stride_h;
+    float M[G], IZ[G];
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      M[g] = cM[g];
+      IZ[g] = cIZ[g];
+    }
+    for (int item = tid; item < wk.ntot * kPage; item += blockDim.x) {
+      const int k = item >> 4, row = item & 15;
+      int src, page;
+      page_ref(p, wk.b, k, src, page);
+      if (!((p.src[src].mask[page] >> row) & 1u)) continue;
+      float a = 0.f;
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        const float l = __ldcg(spill_b + (static_cast<int64_t>(k) * G + g) * kPage + row);
+        a += exp2f(l - M[g]) * IZ[g];
+      }
+      const int64_t at = p.acc_by_position
+                             ? static_cast<int64_t>(p.src[src].posmap[static_cast<int64_t>(page) * kPage + row])
+                             : static_cast<int64_t>(item);
+      if (at >= 0) accb[at] += a;
+    }
+  }
+}
+
+// ===================================================================== MMA
+// Widens an 8-bit page (codes at stage + 0: K block then V block, unswizzled)
+// into bf16 K and V blocks in the swizzled layout, in place.
+template <int D>
+__device__ __forceinline__ void widen_i8_page(char* stage, int lane) {
+  constexpr int ROWB = D * 2;
+  constexpr int CODE_VECS = 2 * kPage * D / 16;  // uint4 of codes in the page-head record
+  constexpr int PER_LANE = CODE_VECS / 32;
+  uint4 v[PER_LANE];
+#pragma unroll
+  for (int i = 0; i < PER_LANE; ++i) v[i] = reinterpret_cast<const uint4*>(stage)[lane + 32 * i];
+  __syncwarp();
+#pragma unroll
+  for (int i = 0; i < PER_LANE; ++i) {
+    const int vec = lane + 32 * i;                 // 16 codes: block kv, row r, columns [16c, 16c + 16)
+    const int per_block = kPage * D / 16;
+    const int kv = vec / per_block;
+    const int rem = vec % per_block;
+    const int r = rem / (D / 16), c = rem % (D / 16);
+    const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+    uint4 lo, hi;
+    lo.x = pack_bf16(i8f(w[0], 0), i8f(w[0], 1));
+    lo.y = pack_bf16(i8f(w[0], 2), i8f(w[0], 3));
+    lo.z = pack_bf16(i8f(w[1], 0), i8f(w[1], 1));
+    lo.w = pack_bf16(i8f(w[1], 2), i8f(w[1], 3));
+    hi.x = pack_bf16(i8f(w[2], 0), i8f(w[2], 1));
+    hi.y = pack_bf16(i8f(w[2], 2), i8f(w[2], 3));
+    hi.z = pack_bf16(i8f(w[3], 0), i8f(w[3], 1));
+    hi.w = pack_bf16(i8f(w[3], 2), i8f(w[3], 3));
+    char* rowp = stage + kv * kPage * ROWB + r * ROWB;
+    *reinterpret_cast<uint4*>(rowp + swz_chunk(2 * c, r, kSwizzle) * 16) = lo;
+    *reinterpret_cast<uint4*>(rowp + swz_chunk(2 * c + 1, r, kSwizzle) * 16) = hi;
+  }
+  __syncwarp();
+}
+
+template <int G, int D>
+__global__ void __launch_bounds__(kAttnWarps * 32)
+    attn_split_mma_kernel(const __grid_constant__ AttnParams p) {
+  using T = __nv_bfloat16;
+  using S = Shape<T, G, D>;
+  using L = Smem<T, G, D>;
+  constexpr int KS = D / 16;  // k-steps of QK over d, and m-tiles of PV over d
+  static_assert(G >= 2 && G <= 8, "tensor-core path serves 2..8 query heads per KV head");
+  extern __shared__ __align__(128) char smem[];
+  __shared__ int s_last;
+
+  const int tid = threadIdx.x;
+  const int w = tid >> 5, lane = tid & 31;
+  const int g = lane >> 2, t = lane & 3;  // fragment row group and column pair
+  const Work wk = find_work(p);
+  stage_pages<L>(p, wk, smem);
+
+  // Q fragments (A operand, heads as rows; rows 8..15 of the tile are zero)
+  uint32_t qa[KS][2];
+  {
+    const T* q = reinterpret_cast<const T*>(p.q) + static_cast<int64_t>(wk.b) * p.q_stride_b +
+                 static_cast<int64_t>(wk.kvh) * G * D;
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      if (g < G) {
+        qa[ks][0] = *reinterpret_cast<const uint32_t*>(q + g * D + 16 * ks + 2 * t);
+        qa[ks][1] = *reinterpret_cast<const uint32_t*>(q + g * D + 16 * ks + 2 * t + 8);
+      } else {
+        qa[ks][0] = qa[ks][1] = 0u;
+      }
+    }
+  }
+  __syncthreads();
+
+  const int* pg = reinterpret_cast<const int*>(smem + L::off_pg);
+  const uint32_t* pmask = reinterpret_cast<const uint32_t*>(pg + kMaxChunkPages);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::off_bar);
+  uint64_t policy;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(policy));
+  char* wring = smem + w * kAttnStages * S::STAGE;
+  const uint32_t wbar = smem_u32(bars + w * kAttnStages);
+  const int nmine = (w < wk.npg) ? (wk.npg - w + kAttnWarps - 1) / kAttnWarps : 0;
+  if (lane == 0)
+    for (int n = 0; n < min(nmine, kAttnStages); ++n) issue_page<S>(p, wk.kvh, pg, w, n, wring, wbar, policy);
+
+  float m_run = -INFINITY, z_run = 0.f;  // softmax state of head g
+  float o[KS][4];                        // O^T tiles: d rows, head columns
+#pragma unroll
+  for (int mt = 0; mt < KS; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+  float* spill_b = p.spill + (static_cast<int64_t>(wk.b) * p.Hkv + wk.kvh) * p.spill_stride;
+  // per-lane ldmatrix row / chunk selectors (matrix = lane / 8)
+  const int lrow = ((lane >> 4) << 3) | (lane & 7);
+  const int lchunk = (lane >> 3) & 1;
+  bool aborted = false;
+  int fail_n = 0;
+
+  for (int n = 0; n < nmine; ++n) {
+    const int st = n % kAttnStages;
+    const bool ok = __all_sync(kFull, mbar_wait(wbar + st * 8, (n / kAttnStages) & 1));
+    if (!ok) {
+      aborted = true;
+      fail_n = n;
+      break;
+    }
+    char* stage = wring + st * S::STAGE;
+    const int i = w + n * kAttnWarps;
+    const int k = wk.k0 + i;
+    const int src = pg[i] >> 28;
+    const uint32_t mask = pmask[i];
+    const PageSource& ps = p.src[src];
+    const bool i8 = ps.kind == SRC_INT8;
+    const int swz = i8 ? kSwizzle : ps.swz;
+    if (i8) widen_i8_page<D>(stage, lane);
+    const uint32_t kbase = smem_u32(stage), vbase = kbase + S::BLK;
+
+    // ---- S^T = Q K^T: two n-tiles of 8 keys -----------------------------------
+    float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      uint32_t b0, b1, b2, b3;
+      ldsm_x4(kbase + lrow * S::ROWB + swz_chunk(2 * ks + lchunk, lrow, swz) * 16, b0, b1, b2, b3);
+      mma_bf16(s0, qa[ks][0], 0u, qa[ks][1], 0u, b0, b1);
+      mma_bf16(s1, qa[ks][0], 0u, qa[ks][1], 0u, b2, b3);
+    }
+    // this lane's logits: head g, keys 2t, 2t+1, 8+2t, 9+2t
+    float l[4] = {s0[0], s0[1], s1[0], s1[1]};
+    const int rows[4] = {2 * t, 2 * t + 1, 8 + 2 * t, 9 + 2 * t};
+    const char* sc = stage + 2 * S::BLK;
+    const bool per_head = ps.scale_per_head != 0;
+    float pmax = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      float x = l[j] * p.qscale;
+      if (i8) x *= t2_scale(sc, per_head, rows[j]);
+      if (!((mask >> rows[j]) & 1u)) x = -INFINITY;
+      l[j] = x;
+      pmax = fmaxf(pmax, x);
+    }
+    pmax = fmaxf(pmax, __shfl_xor_sync(kFull, pmax, 1));
+    pmax = fmaxf(pmax, __shfl_xor_sync(kFull, pmax, 2));
+    const float m_new = fmaxf(m_run, pmax);
+    float corr = 1.f, psum = 0.f, pr[4];
+    if (m_new != -INFINITY) {
+      corr = exp2f(m_run - m_new);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        pr[j] = exp2f(l[j] - m_new);
+        psum += pr[j];
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) pr[j] = 0.f;
+    }
+    psum += __shfl_xor_sync(kFull, psum, 1);
+    psum += __shfl_xor_sync(kFull, psum, 2);
+    z_run = z_run * corr + psum;
+    m_run = m_new;
+    if (g < G) {
+      float* sp = spill_b + (static_cast<int64_t>(k) * G + g) * kPage;
+      *reinterpret_cast<float2*>(sp + 2 * t) = make_float2(l[0], l[1]);
+      *reinterpret_cast<float2*>(sp + 8 + 2 * t) = make_float2(l[2], l[3]);
+    }
+    if (i8) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        pr[j] = ((mask >> rows[j]) & 1u) ? pr[j] * t2_scale(sc, per_head, kPage + rows[j]) : 0.f;
+    }
+    const uint32_t pb0 = pack_bf16(pr[0], pr[1]), pb1 = pack_bf16(pr[2], pr[3]);
+
+    // ---- rescale O^T columns (heads 2t, 2t+1) by their correction -------------
+    const float ca = __shfl_sync(kFull, corr, 8 * t);
+    const float cb = __shfl_sync(kFull, corr, 8 * t + 4);
+    if (__any_sync(kFull, ca != 1.f || cb != 1.f)) {
+#pragma unroll
+      for (int mt = 0; mt < KS; ++mt) {
+        o[mt][0] *= ca;
+        o[mt][1] *= cb;
+        o[mt][2] *= ca;
+        o[mt][3] *= cb;
+      }
+    }
+    // holes may hold anything: a weight of 0 must not meet a NaN, so the V rows
+    // of empty slots are zeroed in shared memory (partial pages only)
+    if (mask != 0xffffu && !i8) {
+      for (int e = lane; e < kPage * (S::ROWB / 16); e += 32) {
+        const int r = e / (S::ROWB / 16);
+        if (!((mask >> r) & 1u))
+          *reinterpret_cast<uint4*>(stage + S::BLK + r * S::ROWB + (e % (S::ROWB / 16)) * 16) =
+              make_uint4(0u, 0u, 0u, 0u);
+      }
+      __syncwarp();
+    }
+    // ---- O^T += V^T P^T ----------------------------------------------------------
+#pragma unroll
+    for (int mt = 0; mt < KS; ++mt) {
+      uint32_t a0, a1, a2, a3;
+      ldsm_x4_t(vbase + lrow * S::ROWB + swz_chunk(2 * mt + lchunk, lrow, swz) * 16, a0, a1, a2, a3);
+      mma_bf16(o[mt], a0, a1, a2, a3, pb0, pb1);
+    }
+    __syncwarp();
+    if (lane == 0 && n + kAttnStages < nmine) issue_page<S>(p, wk.kvh, pg, w, n + kAttnStages, wring, wbar, policy);
+  }
+
+  if (aborted) {
+    atomicExch(p.err, DEV_TIMEOUT);
+    const int hi = min(fail_n + kAttnStages, nmine);
+    for (int n = fail_n; n < hi; ++n) (void)mbar_wait(wbar + (n % kAttnStages) * 8, (n / kAttnStages) & 1);
+    m_run = -INFINITY;
+    z_run = 0.f;
+#pragma unroll
+    for (int mt = 0; mt < KS; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+  }
+
+  // ---- hand the warp's (m, Z, O) to the CTA merge ------------------------------
+  __syncthreads();
+  float* mo = reinterpret_cast<float*>(smem);
+  float* mm = mo + kAttnWarps * G * D;
+  float* mz = mm + kAttnWarps * S::GP;
+#pragma unroll
+  for (int mt = 0; mt < KS; ++mt) {
+    const int d0 = 16 * mt + g;
+    if (2 * t < G) {
+      mo[(w * G + 2 * t) * D + d0] = o[mt][0];
+      mo[(w * G + 2 * t) * D + d0 + 8] = o[mt][2];
+    }
+    if (2 * t + 1 < G) {
+      mo[(w * G + 2 * t + 1) * D + d0] = o[mt][1];
+      mo[(w * G + 2 * t + 1) * D + d0 + 8] = o[mt][3];
+    }
+  }
+  if (t == 0 && g < G) {
+    mm[w * S::GP + g] = m_run;
+    mz[w * S::GP + g] = z_run;
+  }
+  __syncthreads();
+  finish_cta<T, G, D>(p, wk, smem, &s_last);
+}
+
+// ===================================================================== FP32
 // Loads the lane's QE elements of one row of a full-precision page as pairs.
 template <typename T, int G, int D>
-__device__ __forceinline__ void load_row_qk(const char* rowp, int c, float2 (&out)[Shape<T, G, D>::QP]) {
+__device__ __forceinline__ void load_row_qk(const char* rowp, int row, int c, int swz,
+                                            float2 (&out)[Shape<T, G, D>::QP]) {
   using S = Shape<T, G, D>;
 #pragma unroll
   for (int j = 0; j < S::CPL; ++j) {
-    const char* cp = rowp + (c + 8 * j) * 16;
+    const char* cp = rowp + swz_chunk(c + 8 * j, row, swz) * 16;
     if constexpr (sizeof(T) == 2) {
       const uint4 w = *reinterpret_cast<const uint4*>(cp);
       out[j * 4 + 0] = make_float2(bf_lo(w.x), bf_hi(w.x));
@@ -165,7 +635,7 @@ __device__ __forceinline__ void load_row_qk(const char* rowp, int c, float2 (&ou
   }
 }
 
-// The same elements of one row of an 8-bit page (codes as floats).
+// The same elements of one row of an 8-bit page (codes as floats, unswizzled).
 template <typename T, int G, int D>
 __device__ __forceinline__ void load_row_qk_i8(const char* rowp, int c, float2 (&out)[Shape<T, G, D>::QP]) {
   using S = Shape<T, G, D>;
@@ -186,9 +656,9 @@ __device__ __forceinline__ void load_row_qk_i8(const char* rowp, int c, float2 (
   }
 }
 
-// The lane's VPL elements of one V row (full precision or 8-bit codes).
+// The lane's VPL elements of one V row (full precision, swizzled, or 8-bit codes).
 template <typename T, int D, bool I8>
-__device__ __forceinline__ void load_row_pv(const char* rowp, int lane, float (&v)[D / 32]) {
+__device__ __forceinline__ void load_row_pv(const char* rowp, int row, int lane, int swz, float (&v)[D / 32]) {
   constexpr int VPL = D / 32;
   if constexpr (I8) {
     if constexpr (VPL == 4) {
@@ -198,46 +668,32 @@ __device__ __forceinline__ void load_row_pv(const char* rowp, int lane, float (&
       const uint32_t w = *reinterpret_cast<const uint16_t*>(rowp + lane * 2);
       v[0] = i8f(w, 0); v[1] = i8f(w, 1);
     }
-  } else if constexpr (sizeof(T) == 2) {
-    if constexpr (VPL == 4) {
-      const uint2 w = *reinterpret_cast<const uint2*>(rowp + lane * 8);
-      v[0] = bf_lo(w.x); v[1] = bf_hi(w.x); v[2] = bf_lo(w.y); v[3] = bf_hi(w.y);
-    } else {
-      const uint32_t w = *reinterpret_cast<const uint32_t*>(rowp + lane * 4);
-      v[0] = bf_lo(w); v[1] = bf_hi(w);
-    }
   } else {
-    if constexpr (VPL == 4) {
-      const float4 f = *reinterpret_cast<const float4*>(rowp + lane * 16);
-      v[0] = f.x; v[1] = f.y; v[2] = f.z; v[3] = f.w;
+    const int byte = lane * VPL * static_cast<int>(sizeof(T));
+    const char* ep = rowp + swz_chunk(byte >> 4, row, swz) * 16 + (byte & 15);
+    if constexpr (sizeof(T) == 2) {
+      if constexpr (VPL == 4) {
+        const uint2 w = *reinterpret_cast<const uint2*>(ep);
+        v[0] = bf_lo(w.x); v[1] = bf_hi(w.x); v[2] = bf_lo(w.y); v[3] = bf_hi(w.y);
+      } else {
+        const uint32_t w = *reinterpret_cast<const uint32_t*>(ep);
+        v[0] = bf_lo(w); v[1] = bf_hi(w);
+      }
     } else {
-      const float2 f = *reinterpret_cast<const float2*>(rowp + lane * 8);
-      v[0] = f.x; v[1] = f.y;
+      if constexpr (VPL == 4) {
+        const float4 f = *reinterpret_cast<const float4*>(ep);
+        v[0] = f.x; v[1] = f.y; v[2] = f.z; v[3] = f.w;
+      } else {
+        const float2 f = *reinterpret_cast<const float2*>(ep);
+        v[0] = f.x; v[1] = f.y;
+      }
     }
   }
-}
-
-__device__ __forceinline__ void store_out(float* p, float v) { *p = v; }
-__device__ __forceinline__ void store_out(__nv_bfloat16* p, float v) { *p = __float2bfloat16_rn(v); }
-
-// Resolves page-list index k of sequence b to (source, pool page id).
-__device__ __forceinline__ void page_ref(const AttnParams& p, int b, int k, int& src, int& page) {
-  int kk = k;
-  src = 0;
-  if (kk >= p.npages[0][b]) {
-    kk -= p.npages[0][b];
-    src = 1;
-    if (kk >= p.npages[1][b]) {
-      kk -= p.npages[1][b];
-      src = 2;
-    }
-  }
-  page = p.src[src].table[static_cast<int64_t>(b) * p.table_stride + kk];
 }
 
 template <typename T, int G, int D>
 __global__ void __launch_bounds__(kAttnWarps * 32)
-    attn_split_kernel(const __grid_constant__ AttnParams p) {
+    attn_split_fma_kernel(const __grid_constant__ AttnParams p) {
   using S = Shape<T, G, D>;
   using L = Smem<T, G, D>;
   extern __shared__ __align__(128) char smem[];
@@ -246,40 +702,19 @@ __global__ void __launch_bounds__(kAttnWarps * 32)
   const int tid = threadIdx.x;
   const int w = tid >> 5, lane = tid & 31;
   const int r = lane >> 3, c = lane & 7;
-  const int kvh = blockIdx.y;
-  const int chunk = blockIdx.x;
+  const Work wk = find_work(p);
+  stage_pages<L>(p, wk, smem);
 
-  int b = 0;
-  while (b + 1 < p.B && p.chunk_first[b + 1] <= chunk) ++b;
-  const int cf = p.chunk_first[b];
-  const int jc = chunk - cf;
-  const int nch = p.chunk_first[b + 1] - cf;
-  const int ntot = p.npages[0][b] + p.npages[1][b] + p.npages[2][b];
-  const int k0 = jc * p.chunk_pages;
-  const int npg = min(k0 + p.chunk_pages, ntot) - k0;
-
-  char* ring = smem;
   float* q_s = reinterpret_cast<float*>(smem + L::off_q);
   float* p_s = reinterpret_cast<float*>(smem + L::off_p) + w * L::PSW;
   float* corr_s = p_s + S::GP * kPage;
-  int* pg = reinterpret_cast<int*>(smem + L::off_pg);
-  uint32_t* pmask = reinterpret_cast<uint32_t*>(pg + kMaxChunkPages);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::off_bar);
-
-  // Stage the chunk's page references and masks, and the pre-scaled query.
-  for (int i = tid; i < npg; i += blockDim.x) {
-    int src, page;
-    page_ref(p, b, k0 + i, src, page);
-    pg[i] = (src << 28) | page;
-    pmask[i] = p.src[src].mask[page] & 0xffffu;
-  }
   {
-    const T* q = reinterpret_cast<const T*>(p.q) + static_cast<int64_t>(b) * p.q_stride_b +
-                 static_cast<int64_t>(kvh) * G * D;
+    const T* q = reinterpret_cast<const T*>(p.q) + static_cast<int64_t>(wk.b) * p.q_stride_b +
+                 static_cast<int64_t>(wk.kvh) * G * D;
     for (int i = tid; i < S::GP * D; i += blockDim.x) {
-      const int g = i / D;
+      const int gg = i / D;
       float v = 0.f;
-      if (g < G) {
+      if (gg < G) {
         if constexpr (sizeof(T) == 2)
           v = __bfloat162float(q[i]);
         else
@@ -288,45 +723,18 @@ __global__ void __launch_bounds__(kAttnWarps * 32)
       q_s[i] = v * p.qscale;
     }
   }
-  if (lane == 0) {
-    for (int s = 0; s < kAttnStages; ++s) mbar_init(smem_u32(bars + w * kAttnStages + s), 1);
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-  }
   __syncthreads();
 
+  const int* pg = reinterpret_cast<const int*>(smem + L::off_pg);
+  const uint32_t* pmask = reinterpret_cast<const uint32_t*>(pg + kMaxChunkPages);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::off_bar);
   uint64_t policy;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(policy));
-
-  char* wring = ring + w * kAttnStages * S::STAGE;
+  char* wring = smem + w * kAttnStages * S::STAGE;
   const uint32_t wbar = smem_u32(bars + w * kAttnStages);
-  const int nmine = (w < npg) ? (npg - w + kAttnWarps - 1) / kAttnWarps : 0;
-
-  auto issue = [&](int n) {
-    const int i = w + n * kAttnWarps;
-    const int ref = pg[i];
-    const int src = ref >> 28, page = ref & 0x0fffffff;
-    const PageSource& ps = p.src[src];
-    const char* gsrc = ps.base + static_cast<int64_t>(page) * ps.page_bytes +
-                       static_cast<int64_t>(kvh) * ps.head_bytes;
-    const int st = n % kAttnStages;
-    const uint32_t dst = smem_u32(wring + st * S::STAGE);
-    const uint32_t bar = wbar + st * 8;
-    const bool i8 = ps.kind == SRC_INT8;
-    const uint32_t bytes = i8 ? 2u * kPage * D : 2u * S::BLK;
-    const uint32_t sbytes = i8 ? (ps.scale_per_head ? 64u : 128u) : 0u;
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    mbar_expect_tx(bar, bytes + sbytes);
-    bulk_g2s(dst, gsrc, bytes, bar, policy);
-    if (sbytes) {
-      const char* sg = ps.scales + static_cast<int64_t>(page) * ps.scale_page_bytes +
-                       (ps.scale_per_head ? static_cast<int64_t>(kvh) * 64 : 0);
-      bulk_g2s(dst + 2 * S::BLK, sg, sbytes, bar, policy);
-    }
-  };
-
+  const int nmine = (w < wk.npg) ? (wk.npg - w + kAttnWarps - 1) / kAttnWarps : 0;
   if (lane == 0)
-    for (int n = 0; n < min(nmine, kAttnStages); ++n) issue(n);
+    for (int n = 0; n < min(nmine, kAttnStages); ++n) issue_page<S>(p, wk.kvh, pg, w, n, wring, wbar, policy);
 
   float m_run = -INFINITY, z_run = 0.f;  // for the head this lane owns
   float2 acc[G][S::VPL];
@@ -338,8 +746,9 @@ __global__ void __launch_bounds__(kAttnWarps * 32)
   // Which (head, row) logits this lane owns after the butterfly.
   const int own_g = S::NV >= 8 ? (c * S::NL) >> 2 : 0;
   const bool own_writer = S::NV >= 8 ? true : ((c & 1) == 0);
+  const bool head_lead = r == 0 && (S::NV < 8 ? c == 0 : (c & ((8 / S::GP) - 1)) == 0);
 
-  float* spill_b = p.spill + (static_cast<int64_t>(b) * p.Hkv + kvh) * p.spill_stride;
+  float* spill_b = p.spill + (static_cast<int64_t>(wk.b) * p.Hkv + wk.kvh) * p.spill_stride;
   bool aborted = false;
   int fail_n = 0;
 
@@ -353,11 +762,12 @@ __global__ void __launch_bounds__(kAttnWarps * 32)
     }
     const char* stage = wring + st * S::STAGE;
     const int i = w + n * kAttnWarps;
-    const int k = k0 + i;
+    const int k = wk.k0 + i;
     const int src = pg[i] >> 28;
     const uint32_t mask = pmask[i];
     const bool i8 = p.src[src].kind == SRC_INT8;
     const bool per_head = p.src[src].scale_per_head != 0;
+    const int swz = p.src[src].swz;
 
     // ---- QK: 4 rows per lane, QE elements each, all heads -----------------
     float part[S::NV];
@@ -365,11 +775,11 @@ __global__ void __launch_bounds__(kAttnWarps * 32)
       float2 kf[4][S::QP];
 #pragma unroll
       for (int ii = 0; ii < 4; ++ii) {
-        const char* rowp = stage + (r + 4 * ii) * (i8 ? D : S::ROWB);
+        const int row = r + 4 * ii;
         if (i8)
-          load_row_qk_i8<T, G, D>(rowp, c, kf[ii]);
+          load_row_qk_i8<T, G, D>(stage + row * D, c, kf[ii]);
         else
-          load_row_qk<T, G, D>(rowp, c, kf[ii]);
+          load_row_qk<T, G, D>(stage + row * S::ROWB, row, c, swz, kf[ii]);
       }
 #pragma unroll
       for (int g = 0; g < S::GP; ++g) {
@@ -407,11 +817,11 @@ __global__ void __launch_bounds__(kAttnWarps * 32)
         if (size >= 2) {
           const int half = size >> 1;
 #pragma unroll
-          for (int t = 0; t < S::NV / 2; ++t) {
-            if (t < half) {
-              const float send = up ? part[t] : part[t + half];
-              const float keep = up ? part[t + half] : part[t];
-              part[t] = keep + __shfl_xor_sync(kFull, send, m);
+          for (int tt = 0; tt < S::NV / 2; ++tt) {
+            if (tt < half) {
+              const float send = up ? part[tt] : part[tt + half];
+              const float keep = up ? part[tt + half] : part[tt];
+              part[tt] = keep + __shfl_xor_sync(kFull, send, m);
             }
           }
           size = half;
@@ -420,23 +830,19 @@ __global__ void __launch_bounds__(kAttnWarps * 32)
         }
       }
     }
-    // part[0 .. NL) are this lane's logits: head own_g, rows own_row(t).
+    // part[0 .. NL) are this lane's logits: head own_g, rows r + 4 * (idx & 3).
     float lg[S::NL], pv[S::NL];
     float pmax = -INFINITY;
+    const char* sc = stage + 2 * S::BLK;
 #pragma unroll
-    for (int t = 0; t < S::NL; ++t) {
-      const int idx = S::NV >= 8 ? c * S::NL + t : (c >> 1);
+    for (int tt = 0; tt < S::NL; ++tt) {
+      const int idx = S::NV >= 8 ? c * S::NL + tt : (c >> 1);
       const int row = r + 4 * (idx & 3);
-      float l = part[t];
-      if (i8) {
-        const char* sc = stage + 2 * S::BLK;
-        const float sk = per_head ? __half2float(reinterpret_cast<const __half*>(sc)[row])
-                                  : reinterpret_cast<const float*>(sc)[row];
-        l *= sk;
-      }
-      if (!((mask >> row) & 1u)) l = -INFINITY;
-      lg[t] = l;
-      pmax = fmaxf(pmax, l);
+      float x = part[tt];
+      if (i8) x *= t2_scale(sc, per_head, row);
+      if (!((mask >> row) & 1u)) x = -INFINITY;
+      lg[tt] = x;
+      pmax = fmaxf(pmax, x);
     }
 #pragma unroll
     for (int m = 1; m < 8; m <<= 1)
@@ -448,13 +854,13 @@ __global__ void __launch_bounds__(kAttnWarps * 32)
     if (m_new != -INFINITY) {
       corr = exp2f(m_run - m_new);
 #pragma unroll
-      for (int t = 0; t < S::NL; ++t) {
-        pv[t] = exp2f(lg[t] - m_new);
-        psum += pv[t];
+      for (int tt = 0; tt < S::NL; ++tt) {
+        pv[tt] = exp2f(lg[tt] - m_new);
+        psum += pv[tt];
       }
     } else {
 #pragma unroll
-      for (int t = 0; t < S::NL; ++t) pv[t] = 0.f;
+      for (int tt = 0; tt < S::NL; ++tt) pv[tt] = 0.f;
     }
     // with one head, lanes c and c ^ 1 hold the same logits: sum each row once
 #pragma unroll
@@ -468,20 +874,15 @@ __global__ void __launch_bounds__(kAttnWarps * 32)
     // spill raw logits, publish p (times the V scale for 8-bit rows) and corr
     if (own_writer && own_g < G) {
 #pragma unroll
-      for (int t = 0; t < S::NL; ++t) {
-        const int idx = S::NV >= 8 ? c * S::NL + t : (c >> 1);
+      for (int tt = 0; tt < S::NL; ++tt) {
+        const int idx = S::NV >= 8 ? c * S::NL + tt : (c >> 1);
         const int row = r + 4 * (idx & 3);
-        spill_b[(static_cast<int64_t>(k) * G + own_g) * kPage + row] = lg[t];
-        float pw = pv[t];
-        if (i8) {
-          const char* sc = stage + 2 * S::BLK;
-          const float sv = per_head ? __half2float(reinterpret_cast<const __half*>(sc)[kPage + row])
-                                    : reinterpret_cast<const float*>(sc)[kPage + row];
-          pw = ((mask >> row) & 1u) ? pw * sv : 0.f;
-        }
+        spill_b[(static_cast<int64_t>(k) * G + own_g) * kPage + row] = lg[tt];
+        float pw = pv[tt];
+        if (i8) pw = ((mask >> row) & 1u) ? pw * t2_scale(sc, per_head, kPage + row) : 0.f;
         p_s[own_g * kPage + row] = pw;
       }
-      if (r == 0 && (S::NV < 8 ? c == 0 : (c & ((8 / S::GP) - 1)) == 0)) corr_s[own_g] = corr;
+      if (head_lead) corr_s[own_g] = corr;
     }
     __syncwarp();
 
@@ -506,11 +907,11 @@ __global__ void __launch_bounds__(kAttnWarps * 32)
       for (int j = 0; j < kPage / 2; ++j) {
         float va[S::VPL], vb[S::VPL];
         if (i8) {
-          load_row_pv<T, D, true>(vblk + (2 * j) * vrow, lane, va);
-          load_row_pv<T, D, true>(vblk + (2 * j + 1) * vrow, lane, vb);
+          load_row_pv<T, D, true>(vblk + (2 * j) * vrow, 2 * j, lane, 0, va);
+          load_row_pv<T, D, true>(vblk + (2 * j + 1) * vrow, 2 * j + 1, lane, 0, vb);
         } else {
-          load_row_pv<T, D, false>(vblk + (2 * j) * vrow, lane, va);
-          load_row_pv<T, D, false>(vblk + (2 * j + 1) * vrow, lane, vb);
+          load_row_pv<T, D, false>(vblk + (2 * j) * vrow, 2 * j, lane, swz, va);
+          load_row_pv<T, D, false>(vblk + (2 * j + 1) * vrow, 2 * j + 1, lane, swz, vb);
         }
         if (partial) {  // holes may hold anything: weight 0 must not meet a NaN
           const bool oka = (mask >> (2 * j)) & 1u, okb = (mask >> (2 * j + 1)) & 1u;
@@ -529,7 +930,7 @@ __global__ void __launch_bounds__(kAttnWarps * 32)
       }
     }
     __syncwarp();
-    if (lane == 0 && n + kAttnStages < nmine) issue(n + kAttnStages);
+    if (lane == 0 && n + kAttnStages < nmine) issue_page<S>(p, wk.kvh, pg, w, n + kAttnStages, wring, wbar, policy);
   }
 
   if (aborted) {
@@ -546,136 +947,46 @@ __global__ void __launch_bounds__(kAttnWarps * 32)
       for (int e = 0; e < S::VPL; ++e) acc[g][e] = make_float2(0.f, 0.f);
   }
 
-  // ---- merge the CTA's warps ----------------------------------------------
   __syncthreads();
-  float* mo = reinterpret_cast<float*>(ring);           // [warps][G][D]
-  float* mm = mo + kAttnWarps * G * D;                  // [warps][GP]
-  float* mz = mm + kAttnWarps * S::GP;                  // [warps][GP]
+  float* mo = reinterpret_cast<float*>(smem);
+  float* mm = mo + kAttnWarps * G * D;
+  float* mz = mm + kAttnWarps * S::GP;
 #pragma unroll
   for (int g = 0; g < G; ++g)
 #pragma unroll
     for (int e = 0; e < S::VPL; ++e)
       mo[(w * G + g) * D + lane * S::VPL + e] = acc[g][e].x + acc[g][e].y;
-  if (own_writer && own_g < G && r == 0 && (S::NV < 8 ? c == 0 : (c & ((8 / S::GP) - 1)) == 0)) {
+  if (own_writer && own_g < G && head_lead) {
     mm[w * S::GP + own_g] = m_run;
     mz[w * S::GP + own_g] = z_run;
   }
   __syncthreads();
-  const int64_t pidx = static_cast<int64_t>(cf + jc) * p.Hkv + kvh;
-  for (int idx = tid; idx < G * D; idx += blockDim.x) {
-    const int g = idx / D;
-    float M = -INFINITY;
-#pragma unroll
-    for (int ww = 0; ww < kAttnWarps; ++ww) M = fmaxf(M, mm[ww * S::GP + g]);
-    float o = 0.f;
-    if (M != -INFINITY) {
-#pragma unroll
-      for (int ww = 0; ww < kAttnWarps; ++ww) {
-        const float mw = mm[ww * S::GP + g];
-        if (mw != -INFINITY) o += mo[(ww * G) * D + idx] * exp2f(mw - M);
-      }
-    }
-    p.part_o[pidx * G * D + idx] = o;
-  }
-  if (tid < G) {
-    float M = -INFINITY;
-    for (int ww = 0; ww < kAttnWarps; ++ww) M = fmaxf(M, mm[ww * S::GP + tid]);
-    float Z = 0.f;
-    if (M != -INFINITY)
-      for (int ww = 0; ww < kAttnWarps; ++ww) {
-        const float mw = mm[ww * S::GP + tid];
-        if (mw != -INFINITY) Z += mz[ww * S::GP + tid] * exp2f(mw - M);
-      }
-    p.part_m[pidx * G + tid] = M;
-    p.part_z[pidx * G + tid] = Z;
-  }
+  finish_cta<T, G, D>(p, wk, smem, &s_last);
+}
 
-  // ---- ticket: the last CTA of (b, kvh) runs the epilogue -----------------
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) {
-    const int t = atomicAdd(p.tickets + b * p.Hkv + kvh, 1);
-    s_last = (t == nch - 1);
+template <typename K>
+cudaError_t launch_kernel(K kern, int smem_bytes, const AttnParams& p, int total_chunks, cudaStream_t s,
+                          bool& configured) {
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+    if (e != cudaSuccess) return e;
+    configured = true;
   }
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-  if (tid == 0) p.tickets[b * p.Hkv + kvh] = 0;
-
-  float* cM = reinterpret_cast<float*>(ring);
-  float* cIZ = cM + S::GP;
-  if (tid < G) {
-    float M = -INFINITY;
-    for (int j = 0; j < nch; ++j)
-      M = fmaxf(M, __ldcg(p.part_m + (static_cast<int64_t>(cf + j) * p.Hkv + kvh) * G + tid));
-    float Z = 0.f;
-    if (M != -INFINITY)
-      for (int j = 0; j < nch; ++j) {
-        const int64_t pj = (static_cast<int64_t>(cf + j) * p.Hkv + kvh) * G + tid;
-        const float mj = __ldcg(p.part_m + pj);
-        if (mj != -INFINITY) Z += __ldcg(p.part_z + pj) * exp2f(mj - M);
-      }
-    cM[tid] = M;
-    cIZ[tid] = Z > 0.f ? 1.f / Z : 0.f;
-  }
-  __syncthreads();
-  {
-    T* out = reinterpret_cast<T*>(p.out) + static_cast<int64_t>(b) * p.out_stride_b +
-             static_cast<int64_t>(kvh) * G * D;
-    for (int idx = tid; idx < G * D; idx += blockDim.x) {
-      const int g = idx / D;
-      const float M = cM[g];
-      float o = 0.f;
-      if (M != -INFINITY)
-        for (int j = 0; j < nch; ++j) {
-          const int64_t pj = static_cast<int64_t>(cf + j) * p.Hkv + kvh;
-          const float mj = __ldcg(p.part_m + pj * G + g);
-          if (mj != -INFINITY) o += __ldcg(p.part_o + pj * G * D + idx) * exp2f(mj - M);
-        }
-      store_out(out + idx, o * cIZ[g]);
-    }
-  }
-  if (p.acc != nullptr) {
-    float* accb = p.acc + static_cast<int64_t>(b) * p.acc_stride_b +
-                  static_cast<int64_t>(kvh) * p.acc_stride_h;
-    float M[G], IZ[G];
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-      M[g] = cM[g];
-      IZ[g] = cIZ[g];
-    }
-    for (int item = tid; item < ntot * kPage; item += blockDim.x) {
-      const int k = item >> 4, row = item & 15;
-      int src, page;
-      page_ref(p, b, k, src, page);
-      if (!((p.src[src].mask[page] >> row) & 1u)) continue;
-      float a = 0.f;
-#pragma unroll
-      for (int g = 0; g < G; ++g) {
-        const float l = __ldcg(spill_b + (static_cast<int64_t>(k) * G + g) * kPage + row);
-        a += exp2f(l - M[g]) * IZ[g];
-      }
-      const int64_t at = p.acc_by_position
-                             ? static_cast<int64_t>(p.src[src].posmap[static_cast<int64_t>(page) * kPage + row])
-                             : static_cast<int64_t>(item);
-      if (at >= 0) accb[at] += a;
-    }
-  }
+  dim3 grid(total_chunks, p.Hkv);
+  kern<<<grid, kAttnWarps * 32, smem_bytes, s>>>(p);
+  return cudaGetLastError();
 }
 
 template <typename T, int G, int D>
 cudaError_t launch_typed(const AttnParams& p, int total_chunks, cudaStream_t s) {
   using L = Smem<T, G, D>;
-  auto kern = attn_split_kernel<T, G, D>;
-  static bool configured = false;  // per instantiation; the attribute is per function
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::TOTAL);
-    if (e != cudaSuccess) return e;
-    configured = true;
+  if constexpr (sizeof(T) == 2 && G >= 2) {
+    static bool configured = false;
+    return launch_kernel(attn_split_mma_kernel<G, D>, L::TOTAL, p, total_chunks, s, configured);
+  } else {
+    static bool configured = false;
+    return launch_kernel(attn_split_fma_kernel<T, G, D>, L::TOTAL, p, total_chunks, s, configured);
   }
-  dim3 grid(total_chunks, p.Hkv);
-  kern<<<grid, kAttnWarps * 32, L::TOTAL, s>>>(p);
-  return cudaGetLastError();
 }
 
 template <typename T>

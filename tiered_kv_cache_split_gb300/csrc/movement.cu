@@ -64,6 +64,10 @@ __device__ __forceinline__ int8_t quant_code(float x, float divisor) {
 }
 
 // ---------------------------------------------------------------- append
+// One block per (sequence, layer): the new token's K and V rows go to its T0
+// slot (full-precision rows are stored swizzled: 16-byte chunk c of row r at
+// chunk c ^ (r & 7)). Block (b, 0) also updates the page metadata, inserting a
+// new page at its sorted place in the sequence's T0 page list.
 __global__ void append_kernel(const __grid_constant__ AppendParams p) {
   const int b = blockIdx.x, l = blockIdx.y;
   const int page = p.page[b], slot = p.slot[b];
@@ -78,13 +82,27 @@ __global__ void append_kernel(const __grid_constant__ AppendParams p) {
     const char* src = (kv ? p.v : p.k) +
                       ((static_cast<int64_t>(b) * p.L + l) * p.Hkv + h) * row_bytes + v * 16;
     char* dst = dst_page + (static_cast<int64_t>(h) * 2 + kv) * kPage * row_bytes +
-                static_cast<int64_t>(slot) * row_bytes + v * 16;
+                static_cast<int64_t>(slot) * row_bytes + swz_offset(slot, v * 16, kSwizzle);
     *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(src);
   }
-  if (l == 0 && threadIdx.x == 0) {
+  if (l != 0) return;
+  if (p.new_page[b]) {
+    int32_t* row = p.table0 + static_cast<int64_t>(b) * p.table_stride;
+    const int lo = p.insert_at[b], np0 = p.np0[b];
+    // shift entries [lo, np0) one place right, highest first, a block-width at a time
+    for (int base = np0 - 1; base >= lo; base -= blockDim.x) {
+      const int i = base - static_cast<int>(threadIdx.x);
+      int32_t v = 0;
+      if (i >= lo) v = row[i];
+      __syncthreads();
+      if (i >= lo) row[i + 1] = v;
+      __syncthreads();
+    }
+    if (threadIdx.x == 0) row[lo] = page;
+  }
+  if (threadIdx.x == 0) {
     atomicOr(p.mask0 + page, 1u << slot);
     p.posmap0[static_cast<int64_t>(page) * kPage + slot] = static_cast<int32_t>(p.pos[b]);
-    if (p.new_page[b]) p.table0[static_cast<int64_t>(b) * p.table_stride + p.np0[b]] = page;
   }
 }
 
@@ -106,7 +124,7 @@ __global__ void prefill_kernel(const __grid_constant__ PrefillParams p) {
     const int h = hk >> 1, kv = hk & 1;
     const char* src = (kv ? p.v : p.k) + ((static_cast<int64_t>(l) * p.n + t) * p.Hkv + h) * row_bytes + v * 16;
     char* dst = dst_page + (static_cast<int64_t>(h) * 2 + kv) * kPage * row_bytes +
-                static_cast<int64_t>(slot) * row_bytes + v * 16;
+                static_cast<int64_t>(slot) * row_bytes + swz_offset(slot, v * 16, kSwizzle);
     *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(src);
   }
 }
@@ -136,7 +154,8 @@ __global__ void move_kernel(const __grid_constant__ MoveParams p, const Mover* _
       const char* pg = P.base[t] + l * P.layer_bytes[t] + static_cast<int64_t>(page) * P.page_bytes[t];
       for (int i = lane; i < HD; i += 32) {
         const int h = i / p.D, e = i % p.D;
-        const char* src = pg + ((static_cast<int64_t>(h) * 2 + kv) * kPage + slot) * row_bytes + e * esz;
+        const char* src = pg + ((static_cast<int64_t>(h) * 2 + kv) * kPage + slot) * row_bytes +
+                          swz_offset(slot, static_cast<int64_t>(e) * esz, kSwizzle);
         row[i] = load_elem(src, p.kv_dtype);
       }
     } else {
@@ -167,7 +186,8 @@ __global__ void move_kernel(const __grid_constant__ MoveParams p, const Mover* _
     char* pg = P.base[t] + l * P.layer_bytes[t] + static_cast<int64_t>(page) * P.page_bytes[t];
     for (int i = lane; i < HD; i += 32) {
       const int h = i / p.D, e = i % p.D;
-      char* dst = pg + ((static_cast<int64_t>(h) * 2 + kv) * kPage + slot) * row_bytes + e * esz;
+      char* dst = pg + ((static_cast<int64_t>(h) * 2 + kv) * kPage + slot) * row_bytes +
+                  swz_offset(slot, static_cast<int64_t>(e) * esz, kSwizzle);
       store_elem(dst, row[i], p.kv_dtype);
     }
     return;

@@ -12,8 +12,11 @@
 //
 // Slot rule (the page fixes none; this is the reading used throughout): a
 // token that keeps its tier keeps its slot; arrivals, in ascending position,
-// fill the sequence's holes in ascending (page, slot) order, then take the
-// pool's next never-used page; sequences are served in ascending order.
+// fill the sequence's holes in ascending (page id, slot) order, then take a new
+// page (the pool's lowest freed id, else the next never-used id); a sequence's
+// pages are kept in ascending id. After each reassignment the T0 pages of a
+// sequence are compacted into its first ceil(n / 16) pages (moves inside HBM
+// only) and the emptied pages are freed. Sequences are served in ascending order.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -156,7 +159,7 @@ Layout make_layout(const tkv_config& c) {
   y.o_tickets = take(size_t(y.maxb) * y.Hkv * 4);
   y.o_keys = take(size_t(y.maxb) * y.maxtok * 8);
   y.o_err = take(64);
-  y.o_movers = take(size_t(y.maxb) * y.maxtok * sizeof(Mover));
+  y.o_movers = take(2 * size_t(y.maxb) * y.maxtok * sizeof(Mover));
   y.o_temp = take(size_t(y.temp_rows) * y.L * 2 * y.Hkv * y.D * y.esz);
   y.o_locs = take(size_t(y.maxtok) * 4);
   const size_t q_bytes = size_t(y.maxb) * y.L * y.Hq * y.D * y.esz;
@@ -171,7 +174,7 @@ Layout make_layout(const tkv_config& c) {
   y.p_pool2c = take(size_t(y.L) * y.cap[2] * y.plb[2]);
   y.p_pool2s = take(size_t(y.L) * y.cap[2] * y.scale_rec);
   const size_t arena = align_up(size_t(y.maxb) * y.maxtok) +                       // tier read-back
-                       align_up(size_t(y.maxb) * y.maxtok * sizeof(Mover)) +       // movers
+                       align_up(2 * size_t(y.maxb) * y.maxtok * sizeof(Mover)) +   // movers
                        align_up(3 * size_t(y.maxb) * y.maxp * 4) +                 // page tables
                        align_up(size_t(y.cap[0] + y.cap[1] + y.cap[2]) * 4) +      // masks
                        align_up(size_t(y.cap[0] + y.cap[1] + y.cap[2]) * kPage * 4) +  // posmaps
@@ -201,6 +204,7 @@ struct tkv_ctx {
   int slot_rr = 0;
   int64_t steps = 0;
   int64_t next_page[3] = {0, 0, 0};
+  MinHeap free_pages[3];          // freed page ids per tier pool
   std::vector<Seq> seqs;
   std::vector<uint32_t> mask[3];
   std::vector<int32_t> posmap[3];
@@ -293,23 +297,33 @@ tkv_status sync_all(tkv_ctx* h) {
   return TKV_OK;
 }
 
-// Places `positions` (ascending) of sequence b in tier t: holes first, then new pages.
-// Returns false (leaving the pool counter untouched beyond what was used) on capacity.
+// Places `positions` (ascending) of sequence b in tier t: holes first, then new
+// pages (lowest freed id, else the next never-used id), kept in ascending id.
+// Returns false on capacity. *inserted_at receives the list index of the last
+// page added (or is left untouched).
 bool place(tkv_ctx* h, Seq& sq, int b, int t, const std::vector<int64_t>& positions,
-           std::vector<int32_t>* locs_out) {
+           std::vector<int32_t>* locs_out, int* inserted_at = nullptr) {
   for (int64_t pos : positions) {
-    int64_t code;
-    if (!sq.holes[t].empty()) {
-      code = sq.holes[t].top();
-      sq.holes[t].pop();
-    } else {
-      if (h->next_page[t] >= h->y.cap[t] || int64_t(sq.pages[t].size()) >= h->y.maxp) return false;
-      const int64_t page = h->next_page[t]++;
-      sq.pages[t].push_back(static_cast<int32_t>(page));
-      h->table[t][size_t(b) * h->y.maxp + sq.pages[t].size() - 1] = static_cast<int32_t>(page);
-      for (int s = 1; s < kPage; ++s) sq.holes[t].push(page * kPage + s);
-      code = page * kPage;
+    if (sq.holes[t].empty()) {
+      if (int64_t(sq.pages[t].size()) >= h->y.maxp) return false;
+      int64_t page;
+      if (!h->free_pages[t].empty()) {
+        page = h->free_pages[t].top();
+        h->free_pages[t].pop();
+      } else {
+        if (h->next_page[t] >= h->y.cap[t]) return false;
+        page = h->next_page[t]++;
+      }
+      std::vector<int32_t>& pl = sq.pages[t];
+      auto it = std::lower_bound(pl.begin(), pl.end(), static_cast<int32_t>(page));
+      const size_t at = size_t(it - pl.begin());
+      pl.insert(it, static_cast<int32_t>(page));
+      for (size_t i = at; i < pl.size(); ++i) h->table[t][size_t(b) * h->y.maxp + i] = pl[i];
+      if (inserted_at) *inserted_at = static_cast<int>(at);
+      for (int s = 0; s < kPage; ++s) sq.holes[t].push(page * kPage + s);
     }
+    const int64_t code = sq.holes[t].top();
+    sq.holes[t].pop();
     const int64_t page = code / kPage, slot = code % kPage;
     h->mask[t][page] |= 1u << slot;
     h->posmap[t][page * kPage + slot] = static_cast<int32_t>(pos);
@@ -318,6 +332,45 @@ bool place(tkv_ctx* h, Seq& sq, int b, int t, const std::vector<int64_t>& positi
     if (locs_out) locs_out->push_back(static_cast<int32_t>(code));
   }
   return true;
+}
+
+// Packs sequence b's T0 tokens into its first ceil(n / 16) pages; appends the
+// T0 -> T0 moves to `out` and frees the emptied pages.
+void compact_t0(tkv_ctx* h, Seq& sq, int b, std::vector<Mover>& out) {
+  std::vector<int32_t>& pl = sq.pages[0];
+  int64_t n = 0;
+  for (int32_t pg : pl) n += __builtin_popcount(h->mask[0][pg]);
+  const size_t keep = size_t(ceil_div(n, kPage));
+  if (keep >= pl.size()) return;
+  std::vector<std::pair<int64_t, int32_t>> movers;  // (position, old code)
+  for (size_t i = keep; i < pl.size(); ++i)
+    for (int s = 0; s < kPage; ++s) {
+      const int32_t pos = h->posmap[0][size_t(pl[i]) * kPage + s];
+      if (pos >= 0) movers.emplace_back(pos, pl[i] * kPage + s);
+    }
+  std::sort(movers.begin(), movers.end());
+  std::vector<int32_t> holes;
+  for (size_t i = 0; i < keep; ++i)
+    for (int s = 0; s < kPage; ++s)
+      if (!((h->mask[0][pl[i]] >> s) & 1u)) holes.push_back(pl[i] * kPage + s);
+  for (size_t k = 0; k < movers.size(); ++k) {
+    const int64_t pos = movers[k].first;
+    const int32_t from = movers[k].second, to = holes[k];
+    h->mask[0][from / kPage] &= ~(1u << (from % kPage));
+    h->posmap[0][from] = -1;
+    h->mask[0][to / kPage] |= 1u << (to % kPage);
+    h->posmap[0][to] = static_cast<int32_t>(pos);
+    sq.loc[pos] = to;
+    out.push_back(Mover{b, 0, from, 0, to, -1});
+  }
+  for (size_t i = keep; i < pl.size(); ++i) {
+    h->free_pages[0].push(pl[i]);
+    h->table[0][size_t(b) * h->y.maxp + i] = 0;
+  }
+  pl.resize(keep);
+  MinHeap fresh;
+  for (size_t k = movers.size(); k < holes.size(); ++k) fresh.push(holes[k]);
+  sq.holes[0].swap(fresh);
 }
 
 void vacate(tkv_ctx* h, Seq& sq, int t, int64_t pos) {
@@ -336,7 +389,7 @@ int64_t total_pages(const Seq& sq, bool with_t2) {
 tkv_status upload_metadata(tkv_ctx* h) {
   const Layout& y = h->y;
   char* arena = h->P(y.p_arena);
-  size_t off = align_up(size_t(y.maxb) * y.maxtok) + align_up(size_t(y.maxb) * y.maxtok * sizeof(Mover));
+  size_t off = align_up(size_t(y.maxb) * y.maxtok) + align_up(2 * size_t(y.maxb) * y.maxtok * sizeof(Mover));
   const size_t tbytes = size_t(y.maxb) * y.maxp * 4;
   for (int t = 0; t < 3; ++t) {
     std::memcpy(arena + off + t * tbytes, h->table[t].data(), tbytes);
@@ -426,13 +479,13 @@ void fill_sources(tkv_ctx* h, int layer, int slot, AttnParams& p) {
   const Layout& y = h->y;
   const int64_t head_full = int64_t(2) * kPage * y.D * y.esz;
   p.src[0] = PageSource{h->D(y.o_pool0) + size_t(layer) * y.cap[0] * y.plb[0], y.plb[0], head_full,
-                        d_table(h, 0), d_mask(h, 0), d_posmap(h, 0), nullptr, 0, 0, SRC_FULL};
+                        d_table(h, 0), d_mask(h, 0), d_posmap(h, 0), nullptr, 0, 0, SRC_FULL, kSwizzle};
   p.src[1] = PageSource{h->D(y.o_stage1) + size_t(slot) * y.cap[1] * y.plb[1], y.plb[1], head_full,
-                        d_table(h, 1), d_mask(h, 1), d_posmap(h, 1), nullptr, 0, 0, SRC_FULL};
+                        d_table(h, 1), d_mask(h, 1), d_posmap(h, 1), nullptr, 0, 0, SRC_FULL, kSwizzle};
   p.src[2] = PageSource{h->D(y.o_stage2c) + size_t(slot) * y.cap[2] * y.plb[2], y.plb[2],
                         int64_t(2) * kPage * y.D, d_table(h, 2), d_mask(h, 2), d_posmap(h, 2),
                         h->D(y.o_stage2s) + size_t(slot) * y.cap[2] * y.scale_rec, y.scale_rec,
-                        h->cfg.t2_scale_gran == TKV_SCALE_PER_TOKEN_HEAD ? 1 : 0, SRC_INT8};
+                        h->cfg.t2_scale_gran == TKV_SCALE_PER_TOKEN_HEAD ? 1 : 0, SRC_INT8, 0};
   p.nsrc = 3;
 }
 
@@ -467,7 +520,8 @@ tkv_status decode_step_device(tkv_ctx* h, const void* q, const void* k_new, cons
       if (int64_t(sq.pages[0].size()) + 1 > y.maxp) return fail(h, TKV_ERR_CAPACITY, "sequence %d: T0 page list full", b);
     }
   }
-  if (h->next_page[0] + need_pages > y.cap[0]) return fail(h, TKV_ERR_CAPACITY, "T0 pool full");
+  if (h->next_page[0] + need_pages - int64_t(h->free_pages[0].size()) > y.cap[0])
+    return fail(h, TKV_ERR_CAPACITY, "T0 pool full");
 
   // ---- append: every sequence's new token goes to T0 (recent window)
   AppendParams ap{};
@@ -484,10 +538,12 @@ tkv_status decode_step_device(tkv_ctx* h, const void* q, const void* k_new, cons
     sq.N += 1;
     const size_t np_before = sq.pages[0].size();
     std::vector<int32_t> loc;
-    place(h, sq, b, 0, {pos}, &loc);
+    int inserted_at = -1;
+    place(h, sq, b, 0, {pos}, &loc, &inserted_at);
     ap.page[b] = loc[0] / kPage;
     ap.slot[b] = loc[0] % kPage;
     ap.new_page[b] = sq.pages[0].size() != np_before;
+    ap.insert_at[b] = ap.new_page[b] ? inserted_at : -1;
     ap.np0[b] = static_cast<int32_t>(np_before);
     ap.pos[b] = pos;
   }
@@ -623,6 +679,7 @@ tkv_status do_reclassify(tkv_ctx* h) {
   // ---- allocator on a copy of the bookkeeping: a capacity failure changes nothing
   std::vector<Seq> seqs = h->seqs;
   int64_t next_page_save[3] = {h->next_page[0], h->next_page[1], h->next_page[2]};
+  MinHeap free_save[3] = {h->free_pages[0], h->free_pages[1], h->free_pages[2]};
   std::vector<uint32_t> mask_save[3];
   std::vector<int32_t> posmap_save[3], table_save[3];
   for (int t = 0; t < 3; ++t) {
@@ -633,13 +690,14 @@ tkv_status do_reclassify(tkv_ctx* h) {
   auto restore = [&]() {
     for (int t = 0; t < 3; ++t) {
       h->next_page[t] = next_page_save[t];
+      h->free_pages[t] = free_save[t];
       h->mask[t].swap(mask_save[t]);
       h->posmap[t].swap(posmap_save[t]);
       h->table[t].swap(table_save[t]);
     }
   };
 
-  std::vector<Mover> phase1, phase2;
+  std::vector<Mover> phase1, phase2, compaction;
   int64_t d2h = 0, h2d = 0;
   const int64_t row_full = int64_t(y.L) * 2 * y.Hkv * y.D * y.esz;
   const int64_t row_i8 = int64_t(y.L) * (2 * y.Hkv * y.D + (h->cfg.t2_scale_gran == TKV_SCALE_PER_TOKEN ? 8 : 4 * y.Hkv));
@@ -684,9 +742,11 @@ tkv_status do_reclassify(tkv_ctx* h) {
       }
       for (size_t a = 0; a < idx.size(); ++a) dst_loc[idx[a]] = locs[a];
     }
+    compact_t0(h, sq, b, compaction);
     for (size_t m = 0; m < moved.size(); ++m) {
       const int64_t pos = moved[m];
       const int dt = nt[pos];
+      if (dt == 0) dst_loc[m] = sq.loc[pos];  // compaction may have moved a T0 arrival
       if (dt == 3) {
         sq.tier[pos] = 3;
         sq.loc[pos] = -1;
@@ -719,7 +779,8 @@ tkv_status do_reclassify(tkv_ctx* h) {
   Mover* hm = reinterpret_cast<Mover*>(arena + moff);
   std::memcpy(hm, phase2.data(), phase2.size() * sizeof(Mover));
   std::memcpy(hm + phase2.size(), phase1.data(), phase1.size() * sizeof(Mover));
-  const size_t nmov = phase1.size() + phase2.size();
+  std::memcpy(hm + phase2.size() + phase1.size(), compaction.data(), compaction.size() * sizeof(Mover));
+  const size_t nmov = phase1.size() + phase2.size() + compaction.size();
   Mover* dm = reinterpret_cast<Mover*>(h->D(y.o_movers));
   if (nmov) CK(h, cudaMemcpyAsync(dm, hm, nmov * sizeof(Mover), cudaMemcpyHostToDevice, h->cs));
   MoveParams mp{};
@@ -743,6 +804,9 @@ tkv_status do_reclassify(tkv_ctx* h) {
   CK(h, launch_move(mp, dm + phase2.size(), int64_t(phase1.size()), h->cs));
   mp.mode = MOVE_SCATTER;
   CK(h, launch_move(mp, dm, int64_t(phase2.size()), h->cs));
+  // T0 compaction last: every slot it writes has been read by the moves above
+  mp.mode = MOVE_DIRECT;
+  CK(h, launch_move(mp, dm + phase2.size() + phase1.size(), int64_t(compaction.size()), h->cs));
   tkv_status st = upload_metadata(h);
   if (st) return st;
   std::swap(h->d_tier, h->d_tier_new);
@@ -1053,15 +1117,18 @@ tkv_status tkv_get_kv_row(tkv_handle h, int32_t seq, int64_t pos, void* k, void*
   const int t = sq.tier[pos];
   const int64_t page = sq.loc[pos] / kPage, slot = sq.loc[pos] % kPage;
   const size_t rb = size_t(y.D) * y.esz;
+  std::vector<char> raw(rb);
   for (int l = 0; l < y.L; ++l)
     for (int kv = 0; kv < 2; ++kv)
       for (int hh = 0; hh < y.Hkv; ++hh) {
         char* dst = static_cast<char*>(kv ? v : k) + (size_t(l) * y.Hkv + hh) * rb;
         const size_t off = (size_t(l) * y.cap[t] + page) * y.plb[t] + ((size_t(hh) * 2 + kv) * kPage + slot) * rb;
         if (t == 0)
-          CK(h, cudaMemcpy(dst, h->D(y.o_pool0) + off, rb, cudaMemcpyDeviceToHost));
+          CK(h, cudaMemcpy(raw.data(), h->D(y.o_pool0) + off, rb, cudaMemcpyDeviceToHost));
         else
-          std::memcpy(dst, h->P(y.p_pool1) + off, rb);
+          std::memcpy(raw.data(), h->P(y.p_pool1) + off, rb);
+        for (size_t c = 0; c < rb / 16; ++c)  // undo the chunk swizzle of the stored row
+          std::memcpy(dst + c * 16, raw.data() + swz_offset(int(slot), int64_t(c) * 16, kSwizzle), 16);
       }
   return TKV_OK;
 }
@@ -1159,7 +1226,7 @@ tkv_status tkv_paged_attention(int32_t batch, int32_t n_q_heads, int32_t n_kv_he
   for (int b = 0; b < batch; ++b) p.chunk_first[b + 1] = p.chunk_first[b] + static_cast<int32_t>(ceil_div(ntot[b], p.chunk_pages));
   const int64_t head_full = int64_t(2) * kPage * head_dim * esz;
   p.src[0] = PageSource{static_cast<const char*>(pool), head_full * n_kv_heads, head_full, page_table, slot_mask,
-                        nullptr, nullptr, 0, 0, SRC_FULL};
+                        nullptr, nullptr, 0, 0, SRC_FULL, 0};
   p.nsrc = 1;
   p.q = q; p.q_stride_b = int64_t(n_q_heads) * head_dim;
   p.out = out; p.out_stride_b = int64_t(n_q_heads) * head_dim;

@@ -19,6 +19,16 @@ enum DevError : int { DEV_OK = 0, DEV_TIMEOUT = 1, DEV_BAD_INDEX = 2 };
 
 enum SrcKind : int { SRC_FULL = 0, SRC_INT8 = 1 };
 
+// Full-precision K and V blocks of a page (16 rows of head_dim elements) are
+// stored swizzled: the 16-byte chunk c of row r sits at chunk c ^ (r & 7) of
+// that row, so that 8 consecutive rows of one column chunk fall in 8 distinct
+// shared-memory bank groups once a block is copied to shared memory verbatim.
+// 8-bit T2 blocks are stored unswizzled.
+constexpr int kSwizzle = 7;
+__host__ __device__ inline int64_t swz_offset(int row, int64_t byte_in_row, int swz) {
+  return (((byte_in_row >> 4) ^ (row & swz)) << 4) | (byte_in_row & 15);
+}
+
 // One page source of the attention kernel: a page pool (or one layer of it).
 struct PageSource {
   const char* base;          // page 0 of this source at the attended layer
@@ -31,6 +41,7 @@ struct PageSource {
   int64_t scale_page_bytes;  // bytes per page of scale records
   int32_t scale_per_head;    // 0: [2][16] float32 per page; 1: [Hkv][2][16] float16
   int32_t kind;              // SrcKind
+  int32_t swz;               // full-precision blocks: kSwizzle (library pools) or 0 (plain)
 };
 
 struct AttnParams {
@@ -89,6 +100,7 @@ struct AppendParams {
   int32_t* table0;
   int32_t table_stride;
   int32_t page[kMaxBatch], slot[kMaxBatch], np0[kMaxBatch], new_page[kMaxBatch];
+  int32_t insert_at[kMaxBatch];  // list index the new page takes (-1: none); later entries shift right
   int64_t pos[kMaxBatch];
 };
 cudaError_t launch_append(const AppendParams& p, cudaStream_t s);
