@@ -161,9 +161,12 @@ def run_gpu(args):
 
     out = None
     step = 0
+    # the untimed prefix only has to reach the tiered steady state: it cycles a
+    # few generated input sets instead of generating every step's inputs
+    pool = [inputs(i + 1) for i in range(4)]
     for _ in range(untimed):
         step += 1
-        q, k, v = inputs(step)
+        q, k, v = pool[step % len(pool)]
         out = cache.decode_step(q, k, v, out)
     timed_inputs = [inputs(step + i + 1) for i in range(K)]
     torch.cuda.synchronize()
@@ -190,8 +193,9 @@ def run_gpu(args):
     # ---- end to end through the host-buffer entry point (pinned host in and out)
     for _ in range(e2e_untimed):
         step += 1
-        q, k, v = inputs(step)
+        q, k, v = pool[step % len(pool)]
         out = cache.decode_step(q, k, v, out)
+    del pool
     host = []
     for i in range(K):
         q, k, v = inputs(step + i + 1)
@@ -242,7 +246,7 @@ def run_gpu(args):
         "steps": K, "warmup": W, "ms_per_step": ms_max / K, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": w.kv_dtype, "data": "synthetic",
         "config": _config(w, ws),
-        "roofline": {"bound": "hbm", "kernel": "attn_split_kernel", "achieved": achieved, "peak": peak,
+        "roofline": {"bound": "hbm", "kernel": "attn_split_mma_kernel + attn_combine_kernel", "achieved": achieved, "peak": peak,
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": traffic, "bytes_per_launch": bytes_per_launch,
                      "launch_ms": attn_ms},

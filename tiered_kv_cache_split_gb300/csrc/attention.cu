@@ -23,12 +23,13 @@
 //    registers and packed fp32x2 FMAs; the partial dot products of a
 //    (head, row) are reduced across 8 lanes by a transposing butterfly.
 // Per page both keep an online softmax per head in base 2 (log2(e)/sqrt(d)
-// applied to the logits) and spill the raw logits. The warps of a CTA then
-// merge (m, Z, O) in shared memory and write the CTA's partial. The last CTA
-// of each (b, KV head) to finish — found by an atomic ticket, so no CTA ever
-// waits on another — merges the partials into the output and turns every
-// spilled logit into its exact softmax weight alpha = exp2(l - M) / Z with the
-// global (M, Z), summing the G heads into the score accumulator.
+// applied to the logits) and spill the raw logits. The warps of a CTA merge
+// (m, Z, O) in shared memory and the CTA writes its partial; no CTA ever waits
+// on another. attn_combine_kernel then runs one CTA per (chunk, KV head): it
+// forms the global (M, Z) of each head from the partials, the chunk-0 CTA
+// merges the partial outputs, and every CTA turns its chunk's spilled logits
+// into exact softmax weights alpha = exp2(l - M) / Z summed over the G heads,
+// added to a slot-indexed score accumulator (the fused score epilogue).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -207,8 +208,9 @@ __device__ __forceinline__ Work find_work(const AttnParams& p) {
   wk.jc = chunk - wk.cf;
   wk.nch = p.chunk_first[b + 1] - wk.cf;
   wk.ntot = p.npages[0][b] + p.npages[1][b] + p.npages[2][b];
-  wk.k0 = wk.jc * p.chunk_pages;
-  wk.npg = min(wk.k0 + p.chunk_pages, wk.ntot) - wk.k0;
+  // balanced split of the sequence's pages over its chunks (sizes differ by <= 1)
+  wk.k0 = static_cast<int>((static_cast<int64_t>(wk.jc) * wk.ntot) / wk.nch);
+  wk.npg = static_cast<int>((static_cast<int64_t>(wk.jc + 1) * wk.ntot) / wk.nch) - wk.k0;
   return wk;
 }
 
@@ -267,9 +269,9 @@ __device__ __forceinline__ void store_out(float* p, float v) { *p = v; }
 __device__ __forceinline__ void store_out(__nv_bfloat16* p, float v) { *p = __float2bfloat16_rn(v); }
 
 // Merges the warps' (m, Z, O) — already in the MERGE area of `smem` — into the
-// CTA partial, takes the ticket, and if last runs the combine + score epilogue.
+// CTA's partial: O relative to its own max M, and (M, Z) per head.
 template <typename T, int G, int D>
-__device__ void finish_cta(const AttnParams& p, const Work& wk, char* smem, int* s_last) {
+__device__ void write_partial(const AttnParams& p, const Work& wk, char* smem) {
   using S = Shape<T, G, D>;
   const int tid = threadIdx.x;
   float* mo = reinterpret_cast<float*>(smem);           // [warps][G][D]
@@ -303,37 +305,33 @@ __device__ void finish_cta(const AttnParams& p, const Work& wk, char* smem, int*
     p.part_m[pidx * G + tid] = M;
     p.part_z[pidx * G + tid] = Z;
   }
+}
 
-  // ---- ticket: the last CTA of (b, kvh) runs the epilogue -----------------
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) {
-    const int t = atomicAdd(p.tickets + wk.b * p.Hkv + wk.kvh, 1);
-    *s_last = (t == wk.nch - 1);
-  }
-  __syncthreads();
-  if (!*s_last) return;
-  __threadfence();
-  if (tid == 0) p.tickets[wk.b * p.Hkv + wk.kvh] = 0;
-
-  float* cM = reinterpret_cast<float*>(smem);
-  float* cIZ = cM + S::GP;
+// One CTA per (chunk, KV head), after the attention kernel: global (M, Z) per
+// head from the sequence's partials; the chunk-0 CTA writes the output; every
+// CTA adds the exact softmax weights of its chunk, summed over the G heads, to
+// the score accumulator at slot 16 * k + row of the sequence's page list.
+template <typename T, int G, int D>
+__global__ void __launch_bounds__(128) attn_combine_kernel(const __grid_constant__ AttnParams p) {
+  __shared__ float cM[8], cIZ[8];
+  const int tid = threadIdx.x;
+  const Work wk = find_work(p);
   if (tid < G) {
     float M = -INFINITY;
     for (int j = 0; j < wk.nch; ++j)
-      M = fmaxf(M, __ldcg(p.part_m + (static_cast<int64_t>(wk.cf + j) * p.Hkv + wk.kvh) * G + tid));
+      M = fmaxf(M, p.part_m[(static_cast<int64_t>(wk.cf + j) * p.Hkv + wk.kvh) * G + tid]);
     float Z = 0.f;
     if (M != -INFINITY)
       for (int j = 0; j < wk.nch; ++j) {
         const int64_t pj = (static_cast<int64_t>(wk.cf + j) * p.Hkv + wk.kvh) * G + tid;
-        const float mj = __ldcg(p.part_m + pj);
-        if (mj != -INFINITY) Z += __ldcg(p.part_z + pj) * exp2f(mj - M);
+        const float mj = p.part_m[pj];
+        if (mj != -INFINITY) Z += p.part_z[pj] * exp2f(mj - M);
       }
     cM[tid] = M;
     cIZ[tid] = Z > 0.f ? 1.f / Z : 0.f;
   }
   __syncthreads();
-  {
+  if (wk.jc == 0) {
     T* out = reinterpret_cast<T*>(p.out) + static_cast<int64_t>(wk.b) * p.out_stride_b +
              static_cast<int64_t>(wk.kvh) * G * D;
     for (int idx = tid; idx < G * D; idx += blockDim.x) {
@@ -343,38 +341,34 @@ __device__ void finish_cta(const AttnParams& p, const Work& wk, char* smem, int*
       if (M != -INFINITY)
         for (int j = 0; j < wk.nch; ++j) {
           const int64_t pj = static_cast<int64_t>(wk.cf + j) * p.Hkv + wk.kvh;
-          const float mj = __ldcg(p.part_m + pj * G + g);
-          if (mj != -INFINITY) o += __ldcg(p.part_o + pj * G * D + idx) * exp2f(mj - M);
+          const float mj = p.part_m[pj * G + g];
+          if (mj != -INFINITY) o += p.part_o[pj * G * D + idx] * exp2f(mj - M);
         }
       store_out(out + idx, o * cIZ[g]);
     }
   }
-  if (p.acc != nullptr) {
-    const float* spill_b = p.spill + (static_cast<int64_t>(wk.b) * p.Hkv + wk.kvh) * p.spill_stride;
-    float* accb = p.acc + static_cast<int64_t>(wk.b) * p.acc_stride_b +
-                  static_cast<int64_t>(wk.kvh) * p.acc_stride_h;
-    float M[G], IZ[G];
+  if (p.acc == nullptr) return;
+  const float* spill_b = p.spill + (static_cast<int64_t>(wk.b) * p.Hkv + wk.kvh) * p.spill_stride;
+  float* accb = p.acc + static_cast<int64_t>(wk.b) * p.acc_stride_b +
+                static_cast<int64_t>(wk.kvh) * p.acc_stride_h;
+  float M[G], IZ[G];
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    M[g] = cM[g];
+    IZ[g] = cIZ[g];
+  }
+  for (int item = tid; item < wk.npg * kPage; item += blockDim.x) {
+    const int k = wk.k0 + (item >> 4), row = item & 15;
+    int src, page;
+    page_ref(p, wk.b, k, src, page);
+    if (!((p.src[src].mask[page] >> row) & 1u)) continue;
+    float a = 0.f;
 #pragma unroll
     for (int g = 0; g < G; ++g) {
-      M[g] = cM[g];
-      IZ[g] = cIZ[g];
+      const float l = spill_b[(static_cast<int64_t>(k) * G + g) * kPage + row];
+      a += exp2f(l - M[g]) * IZ[g];
     }
-    for (int item = tid; item < wk.ntot * kPage; item += blockDim.x) {
-      const int k = item >> 4, row = item & 15;
-      int src, page;
-      page_ref(p, wk.b, k, src, page);
-      if (!((p.src[src].mask[page] >> row) & 1u)) continue;
-      float a = 0.f;
-#pragma unroll
-      for (int g = 0; g < G; ++g) {
-        const float l = __ldcg(spill_b + (static_cast<int64_t>(k) * G + g) * kPage + row);
-        a += exp2f(l - M[g]) * IZ[g];
-      }
-      const int64_t at = p.acc_by_position
-                             ? static_cast<int64_t>(p.src[src].posmap[static_cast<int64_t>(page) * kPage + row])
-                             : static_cast<int64_t>(item);
-      if (at >= 0) accb[at] += a;
-    }
+    accb[static_cast<int64_t>(k) * kPage + row] += a;
   }
 }
 
@@ -423,7 +417,6 @@ __global__ void __launch_bounds__(kAttnWarps * 32)
   constexpr int KS = D / 16;  // k-steps of QK over d, and m-tiles of PV over d
   static_assert(G >= 2 && G <= 8, "tensor-core path serves 2..8 query heads per KV head");
   extern __shared__ __align__(128) char smem[];
-  __shared__ int s_last;
 
   const int tid = threadIdx.x;
   const int w = tid >> 5, lane = tid & 31;
@@ -609,7 +602,7 @@ __global__ void __launch_bounds__(kAttnWarps * 32)
     mz[w * S::GP + g] = z_run;
   }
   __syncthreads();
-  finish_cta<T, G, D>(p, wk, smem, &s_last);
+  write_partial<T, G, D>(p, wk, smem);
 }
 
 // ===================================================================== FP32
@@ -697,7 +690,6 @@ __global__ void __launch_bounds__(kAttnWarps * 32)
   using S = Shape<T, G, D>;
   using L = Smem<T, G, D>;
   extern __shared__ __align__(128) char smem[];
-  __shared__ int s_last;
 
   const int tid = threadIdx.x;
   const int w = tid >> 5, lane = tid & 31;
@@ -961,7 +953,7 @@ __global__ void __launch_bounds__(kAttnWarps * 32)
     mz[w * S::GP + own_g] = z_run;
   }
   __syncthreads();
-  finish_cta<T, G, D>(p, wk, smem, &s_last);
+  write_partial<T, G, D>(p, wk, smem);
 }
 
 template <typename K>
@@ -980,13 +972,17 @@ cudaError_t launch_kernel(K kern, int smem_bytes, const AttnParams& p, int total
 template <typename T, int G, int D>
 cudaError_t launch_typed(const AttnParams& p, int total_chunks, cudaStream_t s) {
   using L = Smem<T, G, D>;
+  cudaError_t e;
   if constexpr (sizeof(T) == 2 && G >= 2) {
     static bool configured = false;
-    return launch_kernel(attn_split_mma_kernel<G, D>, L::TOTAL, p, total_chunks, s, configured);
+    e = launch_kernel(attn_split_mma_kernel<G, D>, L::TOTAL, p, total_chunks, s, configured);
   } else {
     static bool configured = false;
-    return launch_kernel(attn_split_fma_kernel<T, G, D>, L::TOTAL, p, total_chunks, s, configured);
+    e = launch_kernel(attn_split_fma_kernel<T, G, D>, L::TOTAL, p, total_chunks, s, configured);
   }
+  if (e != cudaSuccess) return e;
+  attn_combine_kernel<T, G, D><<<dim3(total_chunks, p.Hkv), 128, 0, s>>>(p);
+  return cudaGetLastError();
 }
 
 template <typename T>

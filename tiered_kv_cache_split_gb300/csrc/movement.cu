@@ -228,18 +228,35 @@ __global__ void move_kernel(const __grid_constant__ MoveParams p, const Mover* _
 }
 
 // ---------------------------------------------------------------- fold
-// s[b][pos] += (sum over KV heads of acc) / (L * Hq); acc is cleared.
+// One thread per slot of a sequence's attention page list: the slot's position
+// gets (sum over KV heads of the accumulated weights) / (L * Hq) in float64;
+// the accumulator is cleared for the next step.
 __global__ void fold_kernel(const __grid_constant__ FoldParams p) {
   const int b = blockIdx.y;
-  const int64_t pos = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (pos >= p.N[b]) return;
+  const int64_t slot = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int n0 = p.npages[0][b], n1 = p.npages[1][b], n2 = p.npages[2][b];
+  if (slot >= static_cast<int64_t>(n0 + n1 + n2) * kPage) return;
+  int k = static_cast<int>(slot >> 4), src = 0;
+  const int row = static_cast<int>(slot & 15);
+  if (k >= n0) {
+    k -= n0;
+    src = 1;
+    if (k >= n1) {
+      k -= n1;
+      src = 2;
+    }
+  }
+  const int page = p.table[src][static_cast<int64_t>(b) * p.table_stride + k];
   double sum = 0.0;
   for (int h = 0; h < p.Hkv; ++h) {
-    float* a = p.acc + (static_cast<int64_t>(b) * p.Hkv + h) * p.stride + pos;
+    float* a = p.acc + (static_cast<int64_t>(b) * p.Hkv + h) * p.acc_stride + slot;
     sum += static_cast<double>(*a);
     *a = 0.f;
   }
-  p.s[static_cast<int64_t>(b) * p.stride + pos] += sum * p.inv_lh;
+  if ((p.mask[src][page] >> row) & 1u) {
+    const int pos = p.posmap[src][static_cast<int64_t>(page) * kPage + row];
+    if (pos >= 0) p.s[static_cast<int64_t>(b) * p.s_stride + pos] += sum * p.inv_lh;
+  }
 }
 
 // ---------------------------------------------------------------- quantise rows
@@ -295,10 +312,8 @@ cudaError_t launch_move(const MoveParams& p, const Mover* movers, int64_t count,
 }
 
 cudaError_t launch_fold(const FoldParams& p, cudaStream_t s) {
-  int64_t nmax = 0;
-  for (int b = 0; b < p.B; ++b) nmax = p.N[b] > nmax ? p.N[b] : nmax;
-  if (nmax == 0 || p.B == 0) return cudaSuccess;
-  fold_kernel<<<dim3(static_cast<unsigned>((nmax + 255) / 256), p.B), 256, 0, s>>>(p);
+  if (p.B == 0 || p.max_slots == 0) return cudaSuccess;
+  fold_kernel<<<dim3(static_cast<unsigned>((p.max_slots + 255) / 256), p.B), 256, 0, s>>>(p);
   return cudaGetLastError();
 }
 

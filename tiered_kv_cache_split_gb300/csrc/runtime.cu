@@ -66,7 +66,7 @@ struct Layout {
   int64_t max_chunks, spill_stride, temp_rows;
   // device offsets
   size_t o_pool0, o_stage1, o_stage2c, o_stage2s, o_table, o_mask, o_posmap, o_tier, o_tier_new,
-      o_s, o_acc, o_part_o, o_part_m, o_part_z, o_spill, o_tickets, o_keys, o_err, o_movers,
+      o_s, o_acc, o_part_o, o_part_m, o_part_z, o_spill, o_keys, o_err, o_movers,
       o_temp, o_locs, o_io, dev_bytes;
   size_t io_q, io_k, io_out;
   // pinned offsets
@@ -151,12 +151,11 @@ Layout make_layout(const tkv_config& c) {
   y.o_tier = take(size_t(y.maxb) * y.maxtok);
   y.o_tier_new = take(size_t(y.maxb) * y.maxtok);
   y.o_s = take(size_t(y.maxb) * y.maxtok * 8);
-  y.o_acc = take(size_t(y.maxb) * y.Hkv * y.maxtok * 4);
+  y.o_acc = take(size_t(y.maxb) * y.Hkv * 3 * y.maxp * kPage * 4);   // slot-indexed score increments
   y.o_part_o = take(size_t(y.max_chunks) * y.Hkv * y.G * y.D * 4);
   y.o_part_m = take(size_t(y.max_chunks) * y.Hkv * y.G * 4);
   y.o_part_z = take(size_t(y.max_chunks) * y.Hkv * y.G * 4);
   y.o_spill = take(size_t(y.maxb) * y.Hkv * y.spill_stride * 4);
-  y.o_tickets = take(size_t(y.maxb) * y.Hkv * 4);
   y.o_keys = take(size_t(y.maxb) * y.maxtok * 8);
   y.o_err = take(64);
   y.o_movers = take(2 * size_t(y.maxb) * y.maxtok * sizeof(Mover));
@@ -576,11 +575,9 @@ tkv_status decode_step_device(tkv_ctx* h, const void* q, const void* k_new, cons
   p.part_z = reinterpret_cast<float*>(h->D(y.o_part_z));
   p.spill = reinterpret_cast<float*>(h->D(y.o_spill));
   p.spill_stride = y.spill_stride;
-  p.tickets = reinterpret_cast<int32_t*>(h->D(y.o_tickets));
   p.acc = reinterpret_cast<float*>(h->D(y.o_acc));
-  p.acc_stride_b = int64_t(y.Hkv) * y.maxtok;
-  p.acc_stride_h = y.maxtok;
-  p.acc_by_position = 1;
+  p.acc_stride_h = 3 * y.maxp * kPage;
+  p.acc_stride_b = int64_t(y.Hkv) * p.acc_stride_h;
   p.err = reinterpret_cast<int32_t*>(h->D(y.o_err));
   const bool timing = h->cfg.flags & TKV_FLAG_TIMING;
   const int64_t abytes = attn_bytes_per_layer(h);
@@ -613,10 +610,21 @@ tkv_status decode_step_device(tkv_ctx* h, const void* q, const void* k_new, cons
   // ---- fold this step's score increments into s (float64)
   FoldParams fp{};
   fp.B = B; fp.Hkv = y.Hkv;
-  for (int b = 0; b < B; ++b) fp.N[b] = h->seqs[b].N;
+  fp.max_slots = 0;
+  for (int b = 0; b < B; ++b) {
+    for (int t = 0; t < 3; ++t) fp.npages[t][b] = p.npages[t][b];
+    fp.max_slots = std::max<int64_t>(fp.max_slots, ntot[b] * kPage);
+  }
+  for (int t = 0; t < 3; ++t) {
+    fp.table[t] = d_table(h, t);
+    fp.mask[t] = d_mask(h, t);
+    fp.posmap[t] = d_posmap(h, t);
+  }
+  fp.table_stride = static_cast<int32_t>(y.maxp);
   fp.s = reinterpret_cast<double*>(h->D(y.o_s));
+  fp.s_stride = y.maxtok;
   fp.acc = reinterpret_cast<float*>(h->D(y.o_acc));
-  fp.stride = y.maxtok;
+  fp.acc_stride = 3 * y.maxp * kPage;
   fp.inv_lh = 1.0 / (double(y.L) * double(y.Hq));
   CK(h, launch_fold(fp, h->cs));
 
@@ -886,7 +894,7 @@ tkv_status tkv_create(const tkv_config* cfg, void* dev_ws, size_t dev_bytes, voi
   h->d_tier = reinterpret_cast<uint8_t*>(h->D(y.o_tier));
   h->d_tier_new = reinterpret_cast<uint8_t*>(h->D(y.o_tier_new));
   // zero what must start at zero: pools (holes must hold finite values), tables,
-  // masks, tickets, accumulators, scores, the error word; posmaps start at -1
+  // masks, accumulators, scores, the error word; posmaps start at -1
   struct Z { size_t off, bytes; int val; } zs[] = {
       {y.o_pool0, size_t(y.L) * y.cap[0] * y.plb[0], 0},
       {y.o_table, 3 * size_t(y.maxb) * y.maxp * 4, 0},
@@ -894,8 +902,7 @@ tkv_status tkv_create(const tkv_config* cfg, void* dev_ws, size_t dev_bytes, voi
       {y.o_posmap, size_t(y.cap[0] + y.cap[1] + y.cap[2]) * kPage * 4, 0xff},
       {y.o_tier, size_t(y.maxb) * y.maxtok, 0},
       {y.o_s, size_t(y.maxb) * y.maxtok * 8, 0},
-      {y.o_acc, size_t(y.maxb) * y.Hkv * y.maxtok * 4, 0},
-      {y.o_tickets, size_t(y.maxb) * y.Hkv * 4, 0},
+      {y.o_acc, size_t(y.maxb) * y.Hkv * 3 * y.maxp * kPage * 4, 0},
       {y.o_err, 64, 0}};
   for (const Z& z : zs)
     if ((e = cudaMemsetAsync(h->D(z.off), z.val, z.bytes, h->cs)) != cudaSuccess)
@@ -1162,7 +1169,7 @@ const char* tkv_last_error(tkv_handle h) {
 // ------------------------------------------------------------ stateless kernels
 namespace {
 struct PagedScratch {
-  size_t o_err, o_part_o, o_part_m, o_part_z, o_spill, o_tickets, bytes;
+  size_t o_err, o_part_o, o_part_m, o_part_z, o_spill, bytes;
   int64_t max_chunks, spill_stride;
 };
 PagedScratch paged_scratch(int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int32_t max_pages) {
@@ -1177,7 +1184,6 @@ PagedScratch paged_scratch(int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int32_
   s.o_part_m = take(size_t(s.max_chunks) * Hkv * G * 4);
   s.o_part_z = take(size_t(s.max_chunks) * Hkv * G * 4);
   s.o_spill = take(size_t(B) * Hkv * s.spill_stride * 4);
-  s.o_tickets = take(size_t(B) * Hkv * 4);
   s.bytes = o;
   return s;
 }
@@ -1237,15 +1243,12 @@ tkv_status tkv_paged_attention(int32_t batch, int32_t n_q_heads, int32_t n_kv_he
   p.part_z = reinterpret_cast<float*>(sc + s.o_part_z);
   p.spill = reinterpret_cast<float*>(sc + s.o_spill);
   p.spill_stride = s.spill_stride;
-  p.tickets = reinterpret_cast<int32_t*>(sc + s.o_tickets);
   p.acc = alpha_sum;
   p.acc_stride_b = int64_t(n_kv_heads) * max_pages * kPage;
   p.acc_stride_h = int64_t(max_pages) * kPage;
-  p.acc_by_position = 0;
   p.err = reinterpret_cast<int32_t*>(sc + s.o_err);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  cudaError_t e = cudaMemsetAsync(sc + s.o_tickets, 0, size_t(batch) * n_kv_heads * 4, st);
-  if (e == cudaSuccess) e = cudaMemsetAsync(sc + s.o_err, 0, 64, st);
+  cudaError_t e = cudaMemsetAsync(sc + s.o_err, 0, 64, st);
   if (e != cudaSuccess) return fail_cuda(nullptr, "cudaMemsetAsync", e);
   e = launch_attention(p, kv_dtype, p.chunk_first[batch], st);
   if (e != cudaSuccess) return fail_cuda(nullptr, "attention launch", e);

@@ -51,7 +51,7 @@ struct AttnParams {
   int32_t table_stride;
   int32_t npages[3][kMaxBatch];
   int32_t chunk_first[kMaxBatch + 1];   // prefix sums of chunks per sequence
-  int32_t chunk_pages;
+  int32_t chunk_pages;                  // upper bound of pages per chunk (chunks are balanced)
   const void* q;          // element (b, h, e) at q[b * q_stride_b + h * D + e]
   int64_t q_stride_b;
   void* out;
@@ -62,10 +62,8 @@ struct AttnParams {
   float* part_z;          // [chunk * Hkv + kvh][G]
   float* spill;           // per (b, kvh) region of spill_stride floats: [page k][G][16]
   int64_t spill_stride;
-  int32_t* tickets;       // [B * Hkv], zero between launches
-  float* acc;             // score accumulator (may be null)
+  float* acc;             // score accumulator at [b * acc_stride_b + kvh * acc_stride_h + 16 k + row] (may be null)
   int64_t acc_stride_b, acc_stride_h;
-  int32_t acc_by_position;  // 1: index = position from posmap; 0: index = 16 * k + slot
   int32_t* err;
 };
 
@@ -140,12 +138,20 @@ struct MoveParams {
 };
 cudaError_t launch_move(const MoveParams& p, const Mover* movers, int64_t count, cudaStream_t s);
 
+// s[b][pos] += (sum over KV heads of acc at the slot holding pos) / (L * Hq);
+// slots follow the attention page order (T0, T1, then T2 page lists).
 struct FoldParams {
   int32_t B, Hkv;
-  int64_t N[kMaxBatch];
-  double* s;               // [B][stride]
-  float* acc;              // [B][Hkv][stride]
-  int64_t stride;
+  int32_t npages[3][kMaxBatch];
+  const int32_t* table[3];
+  int32_t table_stride;
+  const uint32_t* mask[3];
+  const int32_t* posmap[3];
+  int64_t max_slots;       // largest 16 * (pages of a sequence)
+  double* s;               // [B][s_stride]
+  int64_t s_stride;
+  float* acc;              // [B][Hkv][acc_stride]
+  int64_t acc_stride;
   double inv_lh;           // 1 / (L * Hq)
 };
 cudaError_t launch_fold(const FoldParams& p, cudaStream_t s);
