@@ -308,22 +308,24 @@ __device__ void write_partial(const AttnParams& p, const Work& wk, char* smem) {
 }
 
 // One CTA per (chunk, KV head), after the attention kernel: global (M, Z) per
-// head from the sequence's partials; the chunk-0 CTA writes the output; every
-// CTA adds the exact softmax weights of its chunk, summed over the G heads, to
-// the score accumulator at slot 16 * k + row of the sequence's page list.
+// head from the sequence's partials; each CTA merges a slice of the partial
+// outputs into the output, and adds the exact softmax weights of its own chunk,
+// summed over the G heads, to the score accumulator at slot 16 * k + row of the
+// sequence's page list. Masked slots hold -inf logits, so they add exactly 0
+// and no page metadata is read here.
 template <typename T, int G, int D>
 __global__ void __launch_bounds__(128) attn_combine_kernel(const __grid_constant__ AttnParams p) {
   __shared__ float cM[8], cIZ[8];
   const int tid = threadIdx.x;
   const Work wk = find_work(p);
+  const int64_t base = static_cast<int64_t>(wk.cf) * p.Hkv + wk.kvh;  // partial of chunk j: base + j * Hkv
   if (tid < G) {
     float M = -INFINITY;
-    for (int j = 0; j < wk.nch; ++j)
-      M = fmaxf(M, p.part_m[(static_cast<int64_t>(wk.cf + j) * p.Hkv + wk.kvh) * G + tid]);
+    for (int j = 0; j < wk.nch; ++j) M = fmaxf(M, p.part_m[(base + static_cast<int64_t>(j) * p.Hkv) * G + tid]);
     float Z = 0.f;
     if (M != -INFINITY)
       for (int j = 0; j < wk.nch; ++j) {
-        const int64_t pj = (static_cast<int64_t>(wk.cf + j) * p.Hkv + wk.kvh) * G + tid;
+        const int64_t pj = (base + static_cast<int64_t>(j) * p.Hkv) * G + tid;
         const float mj = p.part_m[pj];
         if (mj != -INFINITY) Z += p.part_z[pj] * exp2f(mj - M);
       }
@@ -331,16 +333,19 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(const __grid_constant
     cIZ[tid] = Z > 0.f ? 1.f / Z : 0.f;
   }
   __syncthreads();
-  if (wk.jc == 0) {
+  {
+    // this chunk's slice of the G * D outputs
+    const int lo = static_cast<int>((static_cast<int64_t>(wk.jc) * G * D) / wk.nch);
+    const int hi = static_cast<int>((static_cast<int64_t>(wk.jc + 1) * G * D) / wk.nch);
     T* out = reinterpret_cast<T*>(p.out) + static_cast<int64_t>(wk.b) * p.out_stride_b +
              static_cast<int64_t>(wk.kvh) * G * D;
-    for (int idx = tid; idx < G * D; idx += blockDim.x) {
+    for (int idx = lo + tid; idx < hi; idx += blockDim.x) {
       const int g = idx / D;
       const float M = cM[g];
       float o = 0.f;
       if (M != -INFINITY)
         for (int j = 0; j < wk.nch; ++j) {
-          const int64_t pj = static_cast<int64_t>(wk.cf + j) * p.Hkv + wk.kvh;
+          const int64_t pj = base + static_cast<int64_t>(j) * p.Hkv;
           const float mj = p.part_m[pj * G + g];
           if (mj != -INFINITY) o += p.part_o[pj * G * D + idx] * exp2f(mj - M);
         }
@@ -359,9 +364,6 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(const __grid_constant
   }
   for (int item = tid; item < wk.npg * kPage; item += blockDim.x) {
     const int k = wk.k0 + (item >> 4), row = item & 15;
-    int src, page;
-    page_ref(p, wk.b, k, src, page);
-    if (!((p.src[src].mask[page] >> row) & 1u)) continue;
     float a = 0.f;
 #pragma unroll
     for (int g = 0; g < G; ++g) {
@@ -483,16 +485,21 @@ __global__ void __launch_bounds__(kAttnWarps * 32)
     const uint32_t kbase = smem_u32(stage), vbase = kbase + S::BLK;
 
     // ---- S^T = Q K^T: two n-tiles of 8 keys -----------------------------------
+    // even and odd k-steps accumulate separately: four independent MMA chains
     float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+    float s2[4] = {0.f, 0.f, 0.f, 0.f}, s3[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int ks = 0; ks < KS; ++ks) {
-      uint32_t b0, b1, b2, b3;
+    for (int ks = 0; ks < KS; ks += 2) {
+      uint32_t b0, b1, b2, b3, c0, c1, c2, c3;
       ldsm_x4(kbase + lrow * S::ROWB + swz_chunk(2 * ks + lchunk, lrow, swz) * 16, b0, b1, b2, b3);
+      ldsm_x4(kbase + lrow * S::ROWB + swz_chunk(2 * ks + 2 + lchunk, lrow, swz) * 16, c0, c1, c2, c3);
       mma_bf16(s0, qa[ks][0], 0u, qa[ks][1], 0u, b0, b1);
       mma_bf16(s1, qa[ks][0], 0u, qa[ks][1], 0u, b2, b3);
+      mma_bf16(s2, qa[ks + 1][0], 0u, qa[ks + 1][1], 0u, c0, c1);
+      mma_bf16(s3, qa[ks + 1][0], 0u, qa[ks + 1][1], 0u, c2, c3);
     }
     // this lane's logits: head g, keys 2t, 2t+1, 8+2t, 9+2t
-    float l[4] = {s0[0], s0[1], s1[0], s1[1]};
+    float l[4] = {s0[0] + s2[0], s0[1] + s2[1], s1[0] + s3[0], s1[1] + s3[1]};
     const int rows[4] = {2 * t, 2 * t + 1, 8 + 2 * t, 9 + 2 * t};
     const char* sc = stage + 2 * S::BLK;
     const bool per_head = ps.scale_per_head != 0;
@@ -985,6 +992,38 @@ cudaError_t launch_typed(const AttnParams& p, int total_chunks, cudaStream_t s) 
   return cudaGetLastError();
 }
 
+template <typename T, int G, int D>
+int resident_typed() {
+  using L = Smem<T, G, D>;
+  int dev = 0, sms = 0, per_sm = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 304;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 304;
+  cudaError_t e;
+  if constexpr (sizeof(T) == 2 && G >= 2) {
+    cudaFuncSetAttribute(attn_split_mma_kernel<G, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::TOTAL);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, attn_split_mma_kernel<G, D>, kAttnWarps * 32, L::TOTAL);
+  } else {
+    cudaFuncSetAttribute(attn_split_fma_kernel<T, G, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::TOTAL);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, attn_split_fma_kernel<T, G, D>, kAttnWarps * 32, L::TOTAL);
+  }
+  (void)cudaGetLastError();
+  if (e != cudaSuccess || per_sm < 1) return 2 * sms;
+  return sms * per_sm;
+}
+
+template <typename T>
+int resident_g(int G, int D) {
+#define TKV_CASE(GG, DD) \
+  if (G == GG && D == DD) return resident_typed<T, GG, DD>();
+  TKV_CASE(1, 64) TKV_CASE(1, 128)
+  TKV_CASE(2, 64) TKV_CASE(2, 128)
+  TKV_CASE(4, 64) TKV_CASE(4, 128)
+  TKV_CASE(7, 64) TKV_CASE(7, 128)
+  TKV_CASE(8, 64) TKV_CASE(8, 128)
+#undef TKV_CASE
+  return 304;
+}
+
 template <typename T>
 cudaError_t dispatch_g(const AttnParams& p, int total_chunks, cudaStream_t s) {
   const int G = p.G, D = p.D;
@@ -1000,6 +1039,11 @@ cudaError_t dispatch_g(const AttnParams& p, int total_chunks, cudaStream_t s) {
 }
 
 }  // namespace
+
+int resident_attention_ctas(int kv_dtype, int G, int D) {
+  if (kv_dtype == 1) return resident_g<__nv_bfloat16>(G, D);
+  return resident_g<float>(G, D);
+}
 
 int attention_supported(int kv_dtype, int G, int D) {
   (void)kv_dtype;

@@ -214,6 +214,7 @@ struct tkv_ctx {
   std::vector<TimedPair> pending, spare;
   uint8_t* d_tier = nullptr;
   uint8_t* d_tier_new = nullptr;
+  int resident_ctas = 304;  // attention CTAs resident on the whole GPU at once
 
   char* D(size_t off) const { return dev + off; }
   char* P(size_t off) const { return pin + off; }
@@ -427,16 +428,47 @@ int32_t* d_table(tkv_ctx* h, int t) {
   return reinterpret_cast<int32_t*>(h->D(h->y.o_table)) + size_t(t) * h->y.maxb * h->y.maxp;
 }
 
-int choose_chunk_pages(const tkv_ctx* h, const std::vector<int64_t>& ntot) {
-  if (h->cfg.split_pages > 0) return h->cfg.split_pages;
+// Splits every sequence's page list into chunks, one attention CTA per
+// (chunk, KV head): the chunk counts are apportioned to the page counts so
+// that the grid fills whole waves of resident CTAs (the last wave would
+// otherwise run nearly empty) and chunks of all sequences hold about the same
+// number of pages. Writes chunk_first[0..B] and returns the page bound.
+int plan_chunks(const std::vector<int64_t>& ntot, int Hkv, int split_pages, int resident_ctas,
+                int32_t* chunk_first) {
+  const int B = static_cast<int>(ntot.size());
+  std::vector<int64_t> nch(B, 1);
   int64_t sum = 0;
   for (int64_t n : ntot) sum += n;
-  sum *= h->y.Hkv;
-  // about four waves of two resident CTAs per SM on 152 SMs
-  const int64_t target = 4 * 2 * 152;
-  int64_t cp = ceil_div(std::max<int64_t>(sum, 1), target);
-  cp = std::max<int64_t>(16, std::min<int64_t>(cp, kMaxChunkPages));
-  return static_cast<int>(ceil_div(cp, kAttnWarps) * kAttnWarps);
+  if (split_pages > 0) {
+    for (int b = 0; b < B; ++b) nch[b] = std::max<int64_t>(1, ceil_div(ntot[b], split_pages));
+  } else {
+    // waves of resident CTAs, about 16 pages or more per chunk
+    int64_t waves = std::max<int64_t>(1, (sum * Hkv) / (int64_t(resident_ctas) * 48));
+    waves = std::min<int64_t>(waves, 8);
+    const int64_t target = std::max<int64_t>(B, waves * resident_ctas / Hkv);
+    // largest-remainder apportionment of `target` chunks to the page counts
+    int64_t given = 0;
+    std::vector<std::pair<double, int>> rem(B);
+    for (int b = 0; b < B; ++b) {
+      const double share = double(ntot[b]) * double(target) / double(std::max<int64_t>(sum, 1));
+      nch[b] = std::max<int64_t>(1, int64_t(share));
+      given += nch[b];
+      rem[b] = {share - std::floor(share), b};
+    }
+    std::sort(rem.begin(), rem.end(), [](const auto& x, const auto& y) { return x.first > y.first; });
+    for (int i = 0; given < target && i < B; ++i, ++given) nch[rem[i].second] += 1;
+    for (int b = 0; b < B; ++b) {
+      nch[b] = std::min<int64_t>(nch[b], std::max<int64_t>(ceil_div(ntot[b], 8), 1));  // >= ~8 pages each
+      nch[b] = std::max<int64_t>(nch[b], ceil_div(ntot[b], kMaxChunkPages));
+    }
+  }
+  int bound = 1;
+  chunk_first[0] = 0;
+  for (int b = 0; b < B; ++b) {
+    chunk_first[b + 1] = chunk_first[b] + static_cast<int32_t>(nch[b]);
+    bound = std::max<int>(bound, static_cast<int>(ceil_div(ntot[b], nch[b])));
+  }
+  return bound;
 }
 
 tkv_status enqueue_prefetch(tkv_ctx* h, int layer, int slot) {
@@ -561,10 +593,7 @@ tkv_status decode_step_device(tkv_ctx* h, const void* q, const void* k_new, cons
     p.npages[2][b] = t2_read ? static_cast<int32_t>(sq.pages[2].size()) : 0;
     ntot[b] = p.npages[0][b] + p.npages[1][b] + p.npages[2][b];
   }
-  p.chunk_pages = choose_chunk_pages(h, ntot);
-  p.chunk_first[0] = 0;
-  for (int b = 0; b < B; ++b)
-    p.chunk_first[b + 1] = p.chunk_first[b] + static_cast<int32_t>(ceil_div(ntot[b], p.chunk_pages));
+  p.chunk_pages = plan_chunks(ntot, y.Hkv, h->cfg.split_pages, h->resident_ctas, p.chunk_first);
   const int total_chunks = p.chunk_first[B];
   if (total_chunks > y.max_chunks) return fail(h, TKV_ERR_INTERNAL, "chunk table overflow");
   p.q_stride_b = int64_t(y.L) * y.Hq * y.D;
@@ -893,6 +922,7 @@ tkv_status tkv_create(const tkv_config* cfg, void* dev_ws, size_t dev_bytes, voi
   }
   h->d_tier = reinterpret_cast<uint8_t*>(h->D(y.o_tier));
   h->d_tier_new = reinterpret_cast<uint8_t*>(h->D(y.o_tier_new));
+  h->resident_ctas = resident_attention_ctas(cfg->kv_dtype, y.G, y.D);
   // zero what must start at zero: pools (holes must hold finite values), tables,
   // masks, accumulators, scores, the error word; posmaps start at -1
   struct Z { size_t off, bytes; int val; } zs[] = {
@@ -1223,13 +1253,8 @@ tkv_status tkv_paged_attention(int32_t batch, int32_t n_q_heads, int32_t n_kv_he
     p.npages[0][b] = page_counts[b];
     ntot[b] = page_counts[b];
   }
-  int64_t sum = 0;
-  for (int64_t n : ntot) sum += n;
-  int64_t cp = ceil_div(sum * n_kv_heads, 4 * 2 * 152);
-  cp = std::max<int64_t>(16, std::min<int64_t>(cp, kMaxChunkPages));
-  p.chunk_pages = static_cast<int32_t>(ceil_div(cp, kAttnWarps) * kAttnWarps);
-  p.chunk_first[0] = 0;
-  for (int b = 0; b < batch; ++b) p.chunk_first[b + 1] = p.chunk_first[b] + static_cast<int32_t>(ceil_div(ntot[b], p.chunk_pages));
+  p.chunk_pages = plan_chunks(ntot, n_kv_heads, 0, resident_attention_ctas(kv_dtype, G, head_dim), p.chunk_first);
+  if (p.chunk_first[batch] > s.max_chunks) return fail(nullptr, TKV_ERR_INTERNAL, "chunk plan exceeds the scratch");
   const int64_t head_full = int64_t(2) * kPage * head_dim * esz;
   p.src[0] = PageSource{static_cast<const char*>(pool), head_full * n_kv_heads, head_full, page_table, slot_mask,
                         nullptr, nullptr, 0, 0, SRC_FULL, 0};

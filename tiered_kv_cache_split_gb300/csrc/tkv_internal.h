@@ -10,8 +10,14 @@ namespace tkv {
 
 constexpr int kPage = 16;          // tokens per page
 constexpr int kMaxBatch = 64;      // sequences per handle (kernel parameters carry per-sequence arrays)
-constexpr int kAttnWarps = 4;      // consumer warps per attention CTA
-constexpr int kAttnStages = 3;     // smem pages in flight per warp
+#ifndef TKV_ATTN_WARPS
+#define TKV_ATTN_WARPS 4
+#endif
+#ifndef TKV_ATTN_STAGES
+#define TKV_ATTN_STAGES 3
+#endif
+constexpr int kAttnWarps = TKV_ATTN_WARPS;    // consumer warps per attention CTA
+constexpr int kAttnStages = TKV_ATTN_STAGES;  // smem pages in flight per warp
 constexpr int kMaxChunkPages = 128;
 
 // Device-side error codes written into the handle's error word.
@@ -70,6 +76,8 @@ struct AttnParams {
 // attention.cu
 cudaError_t launch_attention(const AttnParams& p, int kv_dtype, int total_chunks, cudaStream_t s);
 int attention_supported(int kv_dtype, int G, int D);
+// attention CTAs that fit on the current device at once (SMs x CTAs per SM)
+int resident_attention_ctas(int kv_dtype, int G, int D);
 
 // classify.cu
 struct ClassifyParams {
