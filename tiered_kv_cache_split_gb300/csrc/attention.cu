@@ -6,10 +6,11 @@
 // heads that share that KV head, so every K/V byte is read from HBM once.
 // Pages come from up to three sources in page order: the T0 pool in HBM, the
 // T1 staging copy prefetched from pinned host DDR, and the T2 staging copy of
-// 8-bit codes (Methodology 1, 3, 4). Each consumer warp owns a private ring of
-// shared-memory stages filled by 1-D bulk TMA copies (cp.async.bulk with an
-// mbarrier transaction count, L2 evict-first); lane 0 of the warp issues them,
-// so no warp ever waits on another while streaming.
+// 8-bit codes (Methodology 1, 3, 4). A producer warp streams the chunk's pages
+// into a shared-memory ring with 1-D bulk TMA copies (cp.async.bulk, mbarrier
+// transaction counts, L2 evict-first) as far ahead as the ring allows; the
+// consumer warps take pages round-robin, each waiting on the page's "full"
+// barrier and releasing the stage through its "empty" barrier.
 //
 // Two page processors share that pipeline and the epilogue:
 //  * attn_split_mma_kernel (bf16 KV, G >= 2): the G query heads of a KV head
@@ -162,12 +163,12 @@ struct Shape {
 template <typename T, int G, int D>
 struct Smem {
   using S = Shape<T, G, D>;
-  static constexpr int RING = kAttnWarps * kAttnStages * S::STAGE;
+  static constexpr int RING = kAttnStages * S::STAGE;
   static constexpr int QS = S::GP * D * 4;
   static constexpr int PSW = S::GP * kPage + 8;   // floats per warp: p[GP][16], corr[GP]
   static constexpr int PS = kAttnWarps * PSW * 4;
   static constexpr int PG = kMaxChunkPages * 8;
-  static constexpr int BARS = kAttnWarps * kAttnStages * 8;
+  static constexpr int BARS = 2 * kAttnStages * 8;  // full[stages], empty[stages]
   static constexpr int MERGE = kAttnWarps * (G * D + 2 * S::GP) * 4;
   static constexpr int BODY = ((RING > MERGE ? RING : MERGE) + 127) / 128 * 128;
   static constexpr int off_q = BODY;
@@ -226,27 +227,25 @@ __device__ __forceinline__ void stage_pages(const AttnParams& p, const Work& wk,
     pg[i] = (src << 28) | page;
     pmask[i] = p.src[src].mask[page] & 0xffffu;
   }
-  if ((threadIdx.x & 31) == 0) {
-    const int w = threadIdx.x >> 5;
-    for (int s = 0; s < kAttnStages; ++s) mbar_init(smem_u32(bars + w * kAttnStages + s), 1);
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < 2 * kAttnStages; ++s) mbar_init(smem_u32(bars + s), 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
 }
 
-// Lane 0 of warp w: bulk-copy the n-th page of the warp into its ring stage.
+// Producer lane: bulk-copy page i of the chunk into ring stage st, completing
+// the stage's "full" barrier with the page's byte count.
 template <typename S>
-__device__ __forceinline__ void issue_page(const AttnParams& p, int kvh, const int* pg, int w, int n,
-                                           char* wring, uint32_t wbar, uint64_t policy) {
-  const int i = w + n * kAttnWarps;
+__device__ __forceinline__ void issue_page(const AttnParams& p, int kvh, const int* pg, int i, int st,
+                                           char* ring, uint32_t full0, uint64_t policy) {
   const int ref = pg[i];
   const int src = ref >> 28, page = ref & 0x0fffffff;
   const PageSource& ps = p.src[src];
   const char* gsrc = ps.base + static_cast<int64_t>(page) * ps.page_bytes +
                      static_cast<int64_t>(kvh) * ps.head_bytes;
-  const int st = n % kAttnStages;
-  const uint32_t dst = smem_u32(wring + st * S::STAGE);
-  const uint32_t bar = wbar + st * 8;
+  const uint32_t dst = smem_u32(ring + st * S::STAGE);
+  const uint32_t bar = full0 + st * 8;
   const bool i8 = ps.kind == SRC_INT8;
   const uint32_t bytes = i8 ? 2u * kPage * (S::ROWB / S::ESZ) : 2u * S::BLK;
   const uint32_t sbytes = i8 ? (ps.scale_per_head ? 64u : 128u) : 0u;
@@ -258,6 +257,36 @@ __device__ __forceinline__ void issue_page(const AttnParams& p, int kvh, const i
                      (ps.scale_per_head ? static_cast<int64_t>(kvh) * 64 : 0);
     bulk_g2s(dst + 2 * S::BLK, sg, sbytes, bar, policy);
   }
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+// The producer warp's job (lane 0): keep the ring full; returns pages issued.
+template <typename S>
+__device__ int produce(const AttnParams& p, const Work& wk, const int* pg, char* ring, uint32_t full0,
+                       uint32_t empty0, volatile int* abort_flag) {
+  uint64_t policy;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(policy));
+  int issued = 0;
+  for (int i = 0; i < wk.npg; ++i) {
+    const int st = i % kAttnStages;
+    if (i >= kAttnStages && !mbar_wait(empty0 + st * 8, ((i / kAttnStages) - 1) & 1)) {
+      *abort_flag = 1;
+      break;
+    }
+    if (*abort_flag) break;
+    issue_page<S>(p, wk.kvh, pg, i, st, ring, full0, policy);
+    ++issued;
+  }
+  return issued;
+}
+
+// After an abort: wait (bounded) for the copies still in flight to land.
+__device__ void drain(int issued, uint32_t full0) {
+  const int lo = issued > kAttnStages ? issued - kAttnStages : 0;
+  for (int i = lo; i < issued; ++i) (void)mbar_wait(full0 + (i % kAttnStages) * 8, (i / kAttnStages) & 1);
 }
 
 __device__ __forceinline__ float t2_scale(const char* stage_scales, bool per_head, int idx) {
@@ -411,7 +440,7 @@ __device__ __forceinline__ void widen_i8_page(char* stage, int lane) {
 }
 
 template <int G, int D>
-__global__ void __launch_bounds__(kAttnWarps * 32)
+__global__ void __launch_bounds__((kAttnWarps + 1) * 32)
     attn_split_mma_kernel(const __grid_constant__ AttnParams p) {
   using T = __nv_bfloat16;
   using S = Shape<T, G, D>;
@@ -419,11 +448,13 @@ __global__ void __launch_bounds__(kAttnWarps * 32)
   constexpr int KS = D / 16;  // k-steps of QK over d, and m-tiles of PV over d
   static_assert(G >= 2 && G <= 8, "tensor-core path serves 2..8 query heads per KV head");
   extern __shared__ __align__(128) char smem[];
+  __shared__ volatile int s_abort;
 
   const int tid = threadIdx.x;
   const int w = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, t = lane & 3;  // fragment row group and column pair
   const Work wk = find_work(p);
+  if (tid == 0) s_abort = 0;
   stage_pages<L>(p, wk, smem);
 
   // Q fragments (A operand, heads as rows; rows 8..15 of the tile are zero)
@@ -446,13 +477,11 @@ __global__ void __launch_bounds__(kAttnWarps * 32)
   const int* pg = reinterpret_cast<const int*>(smem + L::off_pg);
   const uint32_t* pmask = reinterpret_cast<const uint32_t*>(pg + kMaxChunkPages);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::off_bar);
-  uint64_t policy;
-  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(policy));
-  char* wring = smem + w * kAttnStages * S::STAGE;
-  const uint32_t wbar = smem_u32(bars + w * kAttnStages);
-  const int nmine = (w < wk.npg) ? (wk.npg - w + kAttnWarps - 1) / kAttnWarps : 0;
-  if (lane == 0)
-    for (int n = 0; n < min(nmine, kAttnStages); ++n) issue_page<S>(p, wk.kvh, pg, w, n, wring, wbar, policy);
+  char* ring = smem;
+  const uint32_t full0 = smem_u32(bars), empty0 = full0 + kAttnStages * 8;
+  const bool consumer = w < kAttnWarps;
+  int issued = 0;
+  if (!consumer && lane == 0) issued = produce<S>(p, wk, pg, ring, full0, empty0, &s_abort);
 
   float m_run = -INFINITY, z_run = 0.f;  // softmax state of head g
   float o[KS][4];                        // O^T tiles: d rows, head columns
@@ -462,19 +491,15 @@ __global__ void __launch_bounds__(kAttnWarps * 32)
   // per-lane ldmatrix row / chunk selectors (matrix = lane / 8)
   const int lrow = ((lane >> 4) << 3) | (lane & 7);
   const int lchunk = (lane >> 3) & 1;
-  bool aborted = false;
-  int fail_n = 0;
 
-  for (int n = 0; n < nmine; ++n) {
-    const int st = n % kAttnStages;
-    const bool ok = __all_sync(kFull, mbar_wait(wbar + st * 8, (n / kAttnStages) & 1));
+  for (int i = w; consumer && i < wk.npg; i += kAttnWarps) {
+    const int st = i % kAttnStages;
+    const bool ok = __all_sync(kFull, mbar_wait(full0 + st * 8, (i / kAttnStages) & 1));
     if (!ok) {
-      aborted = true;
-      fail_n = n;
+      if (lane == 0) s_abort = 1;
       break;
     }
-    char* stage = wring + st * S::STAGE;
-    const int i = w + n * kAttnWarps;
+    char* stage = ring + st * S::STAGE;
     const int k = wk.k0 + i;
     const int src = pg[i] >> 28;
     const uint32_t mask = pmask[i];
@@ -574,26 +599,28 @@ __global__ void __launch_bounds__(kAttnWarps * 32)
       mma_bf16(o[mt], a0, a1, a2, a3, pb0, pb1);
     }
     __syncwarp();
-    if (lane == 0 && n + kAttnStages < nmine) issue_page<S>(p, wk.kvh, pg, w, n + kAttnStages, wring, wbar, policy);
+    if (lane == 0) mbar_arrive(empty0 + st * 8);
   }
 
-  if (aborted) {
-    atomicExch(p.err, DEV_TIMEOUT);
-    const int hi = min(fail_n + kAttnStages, nmine);
-    for (int n = fail_n; n < hi; ++n) (void)mbar_wait(wbar + (n % kAttnStages) * 8, (n / kAttnStages) & 1);
+  __syncthreads();
+  if (s_abort) {  // a bounded wait gave up: land the copies in flight, publish an empty partial
+    if (!consumer && lane == 0) {
+      drain(issued, full0);
+      atomicExch(p.err, DEV_TIMEOUT);
+    }
     m_run = -INFINITY;
     z_run = 0.f;
 #pragma unroll
     for (int mt = 0; mt < KS; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
   }
-
-  // ---- hand the warp's (m, Z, O) to the CTA merge ------------------------------
   __syncthreads();
+
+  // ---- hand the consumer warps' (m, Z, O) to the CTA merge ----------------------
   float* mo = reinterpret_cast<float*>(smem);
   float* mm = mo + kAttnWarps * G * D;
   float* mz = mm + kAttnWarps * S::GP;
 #pragma unroll
-  for (int mt = 0; mt < KS; ++mt) {
+  for (int mt = 0; consumer && mt < KS; ++mt) {
     const int d0 = 16 * mt + g;
     if (2 * t < G) {
       mo[(w * G + 2 * t) * D + d0] = o[mt][0];
@@ -604,7 +631,7 @@ __global__ void __launch_bounds__(kAttnWarps * 32)
       mo[(w * G + 2 * t + 1) * D + d0 + 8] = o[mt][3];
     }
   }
-  if (t == 0 && g < G) {
+  if (consumer && t == 0 && g < G) {
     mm[w * S::GP + g] = m_run;
     mz[w * S::GP + g] = z_run;
   }
@@ -692,16 +719,18 @@ __device__ __forceinline__ void load_row_pv(const char* rowp, int row, int lane,
 }
 
 template <typename T, int G, int D>
-__global__ void __launch_bounds__(kAttnWarps * 32)
+__global__ void __launch_bounds__((kAttnWarps + 1) * 32)
     attn_split_fma_kernel(const __grid_constant__ AttnParams p) {
   using S = Shape<T, G, D>;
   using L = Smem<T, G, D>;
   extern __shared__ __align__(128) char smem[];
+  __shared__ volatile int s_abort;
 
   const int tid = threadIdx.x;
   const int w = tid >> 5, lane = tid & 31;
   const int r = lane >> 3, c = lane & 7;
   const Work wk = find_work(p);
+  if (tid == 0) s_abort = 0;
   stage_pages<L>(p, wk, smem);
 
   float* q_s = reinterpret_cast<float*>(smem + L::off_q);
@@ -727,13 +756,11 @@ __global__ void __launch_bounds__(kAttnWarps * 32)
   const int* pg = reinterpret_cast<const int*>(smem + L::off_pg);
   const uint32_t* pmask = reinterpret_cast<const uint32_t*>(pg + kMaxChunkPages);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::off_bar);
-  uint64_t policy;
-  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(policy));
-  char* wring = smem + w * kAttnStages * S::STAGE;
-  const uint32_t wbar = smem_u32(bars + w * kAttnStages);
-  const int nmine = (w < wk.npg) ? (wk.npg - w + kAttnWarps - 1) / kAttnWarps : 0;
-  if (lane == 0)
-    for (int n = 0; n < min(nmine, kAttnStages); ++n) issue_page<S>(p, wk.kvh, pg, w, n, wring, wbar, policy);
+  char* ring = smem;
+  const uint32_t full0 = smem_u32(bars), empty0 = full0 + kAttnStages * 8;
+  const bool consumer = w < kAttnWarps;
+  int issued = 0;
+  if (!consumer && lane == 0) issued = produce<S>(p, wk, pg, ring, full0, empty0, &s_abort);
 
   float m_run = -INFINITY, z_run = 0.f;  // for the head this lane owns
   float2 acc[G][S::VPL];
@@ -748,19 +775,15 @@ __global__ void __launch_bounds__(kAttnWarps * 32)
   const bool head_lead = r == 0 && (S::NV < 8 ? c == 0 : (c & ((8 / S::GP) - 1)) == 0);
 
   float* spill_b = p.spill + (static_cast<int64_t>(wk.b) * p.Hkv + wk.kvh) * p.spill_stride;
-  bool aborted = false;
-  int fail_n = 0;
 
-  for (int n = 0; n < nmine; ++n) {
-    const int st = n % kAttnStages;
-    const bool ok = __all_sync(kFull, mbar_wait(wbar + st * 8, (n / kAttnStages) & 1));
+  for (int i = w; consumer && i < wk.npg; i += kAttnWarps) {
+    const int st = i % kAttnStages;
+    const bool ok = __all_sync(kFull, mbar_wait(full0 + st * 8, (i / kAttnStages) & 1));
     if (!ok) {
-      aborted = true;
-      fail_n = n;
+      if (lane == 0) s_abort = 1;
       break;
     }
-    const char* stage = wring + st * S::STAGE;
-    const int i = w + n * kAttnWarps;
+    const char* stage = ring + st * S::STAGE;
     const int k = wk.k0 + i;
     const int src = pg[i] >> 28;
     const uint32_t mask = pmask[i];
@@ -929,15 +952,15 @@ __global__ void __launch_bounds__(kAttnWarps * 32)
       }
     }
     __syncwarp();
-    if (lane == 0 && n + kAttnStages < nmine) issue_page<S>(p, wk.kvh, pg, w, n + kAttnStages, wring, wbar, policy);
+    if (lane == 0) mbar_arrive(empty0 + st * 8);
   }
 
-  if (aborted) {
-    atomicExch(p.err, DEV_TIMEOUT);
-    // let the copies this warp issued but did not consume land before the CTA exits
-    const int hi = min(fail_n + kAttnStages, nmine);
-    for (int n = fail_n; n < hi; ++n)
-      (void)mbar_wait(wbar + (n % kAttnStages) * 8, (n / kAttnStages) & 1);
+  __syncthreads();
+  if (s_abort) {  // a bounded wait gave up: land the copies in flight, publish an empty partial
+    if (!consumer && lane == 0) {
+      drain(issued, full0);
+      atomicExch(p.err, DEV_TIMEOUT);
+    }
     m_run = -INFINITY;
     z_run = 0.f;
 #pragma unroll
@@ -945,17 +968,16 @@ __global__ void __launch_bounds__(kAttnWarps * 32)
 #pragma unroll
       for (int e = 0; e < S::VPL; ++e) acc[g][e] = make_float2(0.f, 0.f);
   }
-
   __syncthreads();
   float* mo = reinterpret_cast<float*>(smem);
   float* mm = mo + kAttnWarps * G * D;
   float* mz = mm + kAttnWarps * S::GP;
 #pragma unroll
-  for (int g = 0; g < G; ++g)
+  for (int g = 0; consumer && g < G; ++g)
 #pragma unroll
     for (int e = 0; e < S::VPL; ++e)
       mo[(w * G + g) * D + lane * S::VPL + e] = acc[g][e].x + acc[g][e].y;
-  if (own_writer && own_g < G && head_lead) {
+  if (consumer && own_writer && own_g < G && head_lead) {
     mm[w * S::GP + own_g] = m_run;
     mz[w * S::GP + own_g] = z_run;
   }
@@ -972,7 +994,7 @@ cudaError_t launch_kernel(K kern, int smem_bytes, const AttnParams& p, int total
     configured = true;
   }
   dim3 grid(total_chunks, p.Hkv);
-  kern<<<grid, kAttnWarps * 32, smem_bytes, s>>>(p);
+  kern<<<grid, (kAttnWarps + 1) * 32, smem_bytes, s>>>(p);
   return cudaGetLastError();
 }
 
@@ -1001,10 +1023,10 @@ int resident_typed() {
   cudaError_t e;
   if constexpr (sizeof(T) == 2 && G >= 2) {
     cudaFuncSetAttribute(attn_split_mma_kernel<G, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::TOTAL);
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, attn_split_mma_kernel<G, D>, kAttnWarps * 32, L::TOTAL);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, attn_split_mma_kernel<G, D>, (kAttnWarps + 1) * 32, L::TOTAL);
   } else {
     cudaFuncSetAttribute(attn_split_fma_kernel<T, G, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::TOTAL);
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, attn_split_fma_kernel<T, G, D>, kAttnWarps * 32, L::TOTAL);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, attn_split_fma_kernel<T, G, D>, (kAttnWarps + 1) * 32, L::TOTAL);
   }
   (void)cudaGetLastError();
   if (e != cudaSuccess || per_sm < 1) return 2 * sms;

@@ -14,10 +14,10 @@ constexpr int kMaxBatch = 64;      // sequences per handle (kernel parameters ca
 #define TKV_ATTN_WARPS 4
 #endif
 #ifndef TKV_ATTN_STAGES
-#define TKV_ATTN_STAGES 3
+#define TKV_ATTN_STAGES 10
 #endif
-constexpr int kAttnWarps = TKV_ATTN_WARPS;    // consumer warps per attention CTA
-constexpr int kAttnStages = TKV_ATTN_STAGES;  // smem pages in flight per warp
+constexpr int kAttnWarps = TKV_ATTN_WARPS;    // consumer warps per attention CTA (+ 1 producer warp)
+constexpr int kAttnStages = TKV_ATTN_STAGES;  // shared-memory ring of page stages per CTA
 constexpr int kMaxChunkPages = 128;
 
 // Device-side error codes written into the handle's error word.
