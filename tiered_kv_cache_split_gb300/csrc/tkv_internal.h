@@ -14,10 +14,15 @@ constexpr int kMaxBatch = 64;      // sequences per handle (kernel parameters ca
 #define TKV_ATTN_WARPS 4
 #endif
 #ifndef TKV_ATTN_STAGES
-#define TKV_ATTN_STAGES 10
+#define TKV_ATTN_STAGES 12
 #endif
 constexpr int kAttnWarps = TKV_ATTN_WARPS;    // consumer warps per attention CTA (+ 1 producer warp)
 constexpr int kAttnStages = TKV_ATTN_STAGES;  // shared-memory ring of page stages per CTA
+// Page i goes to ring stage i % stages and to consumer warp i % warps. With the
+// stage count a multiple of the warp count every stage has a single consumer,
+// so each warp waits on a stage's mbarrier phases one after another; otherwise
+// a warp would skip phases and a parity wait could match a stale phase.
+static_assert(kAttnStages % kAttnWarps == 0, "ring stages must be a multiple of consumer warps");
 constexpr int kMaxChunkPages = 128;
 
 // Device-side error codes written into the handle's error word.
