@@ -146,7 +146,7 @@ def run_gpu(args):
     total_steps = untimed + K + e2e_untimed + K
     w = w.replace(n_steps=total_steps + 1)
 
-    cache = TieredKVCache.from_workload(w, timing=True)
+    cache = TieredKVCache.from_workload(w, timing=True, split_pages=args.split_pages)
     t0 = time.time()
     for b in range(w.batch):
         n, P = w.context_lens()[b], w.prompt_lens()[b]
@@ -346,6 +346,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--layers", type=int, default=0, help="override the layer count (profiling a small case)")
+    ap.add_argument("--split-pages", type=int, default=0, help="pages per attention CTA (0: planned)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

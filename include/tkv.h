@@ -83,7 +83,7 @@ typedef struct {
   int32_t n_layers, n_q_heads, n_kv_heads, head_dim; /* Hq % Hkv == 0; d in {64, 128} */
   int32_t kv_dtype;                                   /* TKV_DTYPE_* */
   int32_t max_batch;                                  /* 1 .. 64 sequences */
-  int64_t max_tokens;                                 /* positions per sequence */
+  int64_t max_tokens;                                 /* positions per sequence, <= 262080 */
   int32_t page_size;                                  /* must be 16 */
   int32_t n_sink, recent_window;
   int32_t budget_mode;                                /* TKV_BUDGET_* */
@@ -185,7 +185,7 @@ TKV_API const char* tkv_last_error(tkv_handle h);
  *   pool     device [n_pages][Hkv][2][16][d]  page p, head h: K rows then V rows
  *   page_table device int32 [B][max_pages]  pool ids of each sequence's pages
  *   slot_mask  device uint32 [n_pages]      bit j set = slot j holds a token
- *   page_counts HOST int32 [B]              pages used by each sequence
+ *   page_counts HOST int32 [B]              pages used by each sequence (max_pages <= 16384)
  *   out      device [B][Hq][d]           (KV dtype)
  *   alpha_sum device float [B][Hkv][max_pages * 16] or NULL: adds, for each slot,
  *            the softmax weight summed over the G query heads of KV head h (slot order = page

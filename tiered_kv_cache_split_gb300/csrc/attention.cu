@@ -341,25 +341,42 @@ __device__ void write_partial(const AttnParams& p, const Work& wk, char* smem) {
 // outputs into the output, and adds the exact softmax weights of its own chunk,
 // summed over the G heads, to the score accumulator at slot 16 * k + row of the
 // sequence's page list. Masked slots hold -inf logits, so they add exactly 0
-// and no page metadata is read here.
+// and no page metadata is read here. Loads are batched so that each phase
+// costs about one memory round trip.
+constexpr int kCombineThreads = 128;
+constexpr int kMaxCombineChunks = kMaxChunksPerSeq;
+
 template <typename T, int G, int D>
-__global__ void __launch_bounds__(128) attn_combine_kernel(const __grid_constant__ AttnParams p) {
+__global__ void __launch_bounds__(kCombineThreads) attn_combine_kernel(const __grid_constant__ AttnParams p) {
+  __shared__ float sm_m[kMaxCombineChunks][8], sm_z[kMaxCombineChunks][8];
+  __shared__ float sm_w[kMaxCombineChunks][8];  // exp2(m_j - M) / Z per chunk and head
   __shared__ float cM[8], cIZ[8];
   const int tid = threadIdx.x;
   const Work wk = find_work(p);
   const int64_t base = static_cast<int64_t>(wk.cf) * p.Hkv + wk.kvh;  // partial of chunk j: base + j * Hkv
+  const int nch = min(wk.nch, kMaxCombineChunks);
+  for (int e = tid; e < nch * G; e += kCombineThreads) {
+    const int j = e / G, g = e % G;
+    const int64_t pj = (base + static_cast<int64_t>(j) * p.Hkv) * G + g;
+    sm_m[j][g] = __ldg(p.part_m + pj);
+    sm_z[j][g] = __ldg(p.part_z + pj);
+  }
+  __syncthreads();
   if (tid < G) {
     float M = -INFINITY;
-    for (int j = 0; j < wk.nch; ++j) M = fmaxf(M, p.part_m[(base + static_cast<int64_t>(j) * p.Hkv) * G + tid]);
+    for (int j = 0; j < nch; ++j) M = fmaxf(M, sm_m[j][tid]);
     float Z = 0.f;
     if (M != -INFINITY)
-      for (int j = 0; j < wk.nch; ++j) {
-        const int64_t pj = (base + static_cast<int64_t>(j) * p.Hkv) * G + tid;
-        const float mj = p.part_m[pj];
-        if (mj != -INFINITY) Z += p.part_z[pj] * exp2f(mj - M);
-      }
+      for (int j = 0; j < nch; ++j)
+        if (sm_m[j][tid] != -INFINITY) Z += sm_z[j][tid] * exp2f(sm_m[j][tid] - M);
     cM[tid] = M;
     cIZ[tid] = Z > 0.f ? 1.f / Z : 0.f;
+  }
+  __syncthreads();
+  for (int e = tid; e < nch * G; e += kCombineThreads) {
+    const int j = e / G, g = e % G;
+    const float mj = sm_m[j][g];
+    sm_w[j][g] = (mj == -INFINITY || cM[g] == -INFINITY) ? 0.f : exp2f(mj - cM[g]) * cIZ[g];
   }
   __syncthreads();
   {
@@ -368,38 +385,50 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(const __grid_constant
     const int hi = static_cast<int>((static_cast<int64_t>(wk.jc + 1) * G * D) / wk.nch);
     T* out = reinterpret_cast<T*>(p.out) + static_cast<int64_t>(wk.b) * p.out_stride_b +
              static_cast<int64_t>(wk.kvh) * G * D;
-    for (int idx = lo + tid; idx < hi; idx += blockDim.x) {
+    for (int idx = lo + tid; idx < hi; idx += kCombineThreads) {
       const int g = idx / D;
-      const float M = cM[g];
       float o = 0.f;
-      if (M != -INFINITY)
-        for (int j = 0; j < wk.nch; ++j) {
-          const int64_t pj = base + static_cast<int64_t>(j) * p.Hkv;
-          const float mj = p.part_m[pj * G + g];
-          if (mj != -INFINITY) o += p.part_o[pj * G * D + idx] * exp2f(mj - M);
-        }
-      store_out(out + idx, o * cIZ[g]);
+#pragma unroll 8
+      for (int j = 0; j < nch; ++j)
+        o += __ldg(p.part_o + (base + static_cast<int64_t>(j) * p.Hkv) * G * D + idx) * sm_w[j][g];
+      store_out(out + idx, o);
     }
   }
   if (p.acc == nullptr) return;
-  const float* spill_b = p.spill + (static_cast<int64_t>(wk.b) * p.Hkv + wk.kvh) * p.spill_stride;
-  float* accb = p.acc + static_cast<int64_t>(wk.b) * p.acc_stride_b +
-                static_cast<int64_t>(wk.kvh) * p.acc_stride_h;
+  const float* __restrict__ spill_b = p.spill + (static_cast<int64_t>(wk.b) * p.Hkv + wk.kvh) * p.spill_stride;
+  float* __restrict__ accb = p.acc + static_cast<int64_t>(wk.b) * p.acc_stride_b +
+                             static_cast<int64_t>(wk.kvh) * p.acc_stride_h;
   float M[G], IZ[G];
 #pragma unroll
   for (int g = 0; g < G; ++g) {
     M[g] = cM[g];
     IZ[g] = cIZ[g];
   }
-  for (int item = tid; item < wk.npg * kPage; item += blockDim.x) {
-    const int k = wk.k0 + (item >> 4), row = item & 15;
-    float a = 0.f;
+  constexpr int U = 4;
+  const int items = wk.npg * kPage;
+  for (int first = tid; first < items; first += kCombineThreads * U) {
+    float l[U][G], old[U];
 #pragma unroll
-    for (int g = 0; g < G; ++g) {
-      const float l = spill_b[(static_cast<int64_t>(k) * G + g) * kPage + row];
-      a += exp2f(l - M[g]) * IZ[g];
+    for (int u = 0; u < U; ++u) {
+      const int item = first + u * kCombineThreads;
+      if (item < items) {
+        const int k = wk.k0 + (item >> 4), row = item & 15;
+#pragma unroll
+        for (int g = 0; g < G; ++g) l[u][g] = __ldg(spill_b + (static_cast<int64_t>(k) * G + g) * kPage + row);
+        old[u] = accb[static_cast<int64_t>(k) * kPage + row];
+      }
     }
-    accb[static_cast<int64_t>(k) * kPage + row] += a;
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int item = first + u * kCombineThreads;
+      if (item < items) {
+        const int k = wk.k0 + (item >> 4), row = item & 15;
+        float a = 0.f;
+#pragma unroll
+        for (int g = 0; g < G; ++g) a += exp2f(l[u][g] - M[g]) * IZ[g];
+        accb[static_cast<int64_t>(k) * kPage + row] = old[u] + a;
+      }
+    }
   }
 }
 
@@ -1010,7 +1039,7 @@ cudaError_t launch_typed(const AttnParams& p, int total_chunks, cudaStream_t s) 
     e = launch_kernel(attn_split_fma_kernel<T, G, D>, L::TOTAL, p, total_chunks, s, configured);
   }
   if (e != cudaSuccess) return e;
-  attn_combine_kernel<T, G, D><<<dim3(total_chunks, p.Hkv), 128, 0, s>>>(p);
+  attn_combine_kernel<T, G, D><<<dim3(total_chunks, p.Hkv), kCombineThreads, 0, s>>>(p);
   return cudaGetLastError();
 }
 

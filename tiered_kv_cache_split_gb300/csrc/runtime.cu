@@ -32,7 +32,7 @@
 #include <string>
 #include <vector>
 
-#include "../../include/tkv.h"
+#include "tkv.h"
 #include "tkv_internal.h"
 
 using namespace tkv;
@@ -93,7 +93,8 @@ std::string validate(const tkv_config& c) {
     return bad("unsupported (Hq/Hkv, head_dim): group size must be 1, 2, 4, 7 or 8 and head_dim 64 or 128");
   if (c.kv_dtype != TKV_DTYPE_F32 && c.kv_dtype != TKV_DTYPE_BF16) return bad("kv_dtype");
   if (c.max_batch < 1 || c.max_batch > kMaxBatch) return bad("max_batch must be 1..64");
-  if (c.max_tokens < 1 || c.max_tokens > (int64_t(1) << 27)) return bad("max_tokens out of range");
+  if (c.max_tokens < 1 || c.max_tokens > int64_t(kMaxChunksPerSeq) * kMaxChunkPages * kPage - 4 * kPage)
+    return bad("max_tokens out of range (1 .. 262080)");
   if (c.page_size != kPage) return bad("page_size must be 16");
   if (c.n_sink < 0 || c.recent_window < 0) return bad("n_sink / recent_window negative");
   if (c.budget_mode == TKV_BUDGET_PERCENT) {
@@ -462,6 +463,8 @@ int plan_chunks(const std::vector<int64_t>& ntot, int Hkv, int split_pages, int 
       nch[b] = std::max<int64_t>(nch[b], ceil_div(ntot[b], kMaxChunkPages));
     }
   }
+  for (int b = 0; b < B; ++b)  // the combine kernel merges at most kMaxChunksPerSeq chunks
+    nch[b] = std::max<int64_t>(std::min<int64_t>(nch[b], kMaxChunksPerSeq), ceil_div(ntot[b], kMaxChunkPages));
   int bound = 1;
   chunk_first[0] = 0;
   for (int b = 0; b < B; ++b) {
@@ -1248,6 +1251,7 @@ tkv_status tkv_paged_attention(int32_t batch, int32_t n_q_heads, int32_t n_kv_he
   p.B = batch; p.Hq = n_q_heads; p.Hkv = n_kv_heads; p.D = head_dim; p.G = G;
   p.table_stride = max_pages;
   std::vector<int64_t> ntot(batch);
+  if (max_pages > kMaxChunksPerSeq * kMaxChunkPages) return fail(nullptr, TKV_ERR_INVALID_ARG, "max_pages above 16384");
   for (int b = 0; b < batch; ++b) {
     if (page_counts[b] < 1 || page_counts[b] > max_pages) return fail(nullptr, TKV_ERR_INVALID_ARG, "page_counts[%d] out of 1..max_pages", b);
     p.npages[0][b] = page_counts[b];

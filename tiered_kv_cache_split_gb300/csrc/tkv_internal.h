@@ -23,7 +23,8 @@ constexpr int kAttnStages = TKV_ATTN_STAGES;  // shared-memory ring of page stag
 // so each warp waits on a stage's mbarrier phases one after another; otherwise
 // a warp would skip phases and a parity wait could match a stale phase.
 static_assert(kAttnStages % kAttnWarps == 0, "ring stages must be a multiple of consumer warps");
-constexpr int kMaxChunkPages = 128;
+constexpr int kMaxChunkPages = 256;   // pages one attention CTA may take
+constexpr int kMaxChunksPerSeq = 64;  // chunks of one sequence the combine kernel merges
 
 // Device-side error codes written into the handle's error word.
 enum DevError : int { DEV_OK = 0, DEV_TIMEOUT = 1, DEV_BAD_INDEX = 2 };
