@@ -38,6 +38,7 @@ class Stats(ctypes.Structure):
         ("steps", c_i64), ("reclassifies", c_i64), ("movers", c_i64), ("attn_launches", c_i64),
         ("attn_bytes", c_i64), ("prefetch_bytes", c_i64), ("h2d_move_bytes", c_i64),
         ("d2h_move_bytes", c_i64), ("tier_counts", c_i64 * 4), ("attn_ms", ctypes.c_double),
+        ("combine_ms", ctypes.c_double),
         ("prefetch_ms", ctypes.c_double), ("reclassify_ms", ctypes.c_double),
     ]
 

@@ -215,23 +215,21 @@ __device__ __forceinline__ Work find_work(const AttnParams& p) {
   return wk;
 }
 
-// Stages the chunk's page references and masks, and initialises each warp's barriers.
+// Initialises the ring's full and empty barriers (thread 0); a CTA barrier
+// must follow before any thread uses them.
 template <typename L>
-__device__ __forceinline__ void stage_pages(const AttnParams& p, const Work& wk, char* smem) {
-  int* pg = reinterpret_cast<int*>(smem + L::off_pg);
-  uint32_t* pmask = reinterpret_cast<uint32_t*>(pg + kMaxChunkPages);
+__device__ __forceinline__ void init_barriers(char* smem) {
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::off_bar);
-  for (int i = threadIdx.x; i < wk.npg; i += blockDim.x) {
-    int src, page;
-    page_ref(p, wk.b, wk.k0 + i, src, page);
-    pg[i] = (src << 28) | page;
-    pmask[i] = p.src[src].mask[page] & 0xffffu;
-  }
   if (threadIdx.x == 0) {
     for (int s = 0; s < 2 * kAttnStages; ++s) mbar_init(smem_u32(bars + s), 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
+}
+
+// Barrier among the consumer warps only (the producer warp runs ahead).
+__device__ __forceinline__ void consumer_sync() {
+  asm volatile("bar.sync 1, %0;" ::"r"(kAttnWarps * 32) : "memory");
 }
 
 // Producer lane: bulk-copy page i of the chunk into ring stage st, completing
@@ -263,22 +261,40 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
-// The producer warp's job (lane 0): keep the ring full; returns pages issued.
+// The producer warp's job: resolve the chunk's pages 32 at a time (one per
+// lane: source, pool page, valid mask, published in shared memory for the
+// consumers) and let lane 0 keep the ring full. Returns the pages issued (lane 0).
 template <typename S>
-__device__ int produce(const AttnParams& p, const Work& wk, const int* pg, char* ring, uint32_t full0,
-                       uint32_t empty0, volatile int* abort_flag) {
+__device__ int produce(const AttnParams& p, const Work& wk, int* pg, uint32_t* pmask, char* ring,
+                       uint32_t full0, uint32_t empty0, volatile int* abort_flag) {
+  const int lane = threadIdx.x & 31;
   uint64_t policy;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(policy));
   int issued = 0;
-  for (int i = 0; i < wk.npg; ++i) {
-    const int st = i % kAttnStages;
-    if (i >= kAttnStages && !mbar_wait(empty0 + st * 8, ((i / kAttnStages) - 1) & 1)) {
-      *abort_flag = 1;
-      break;
+  for (int base = 0; base < wk.npg; base += 32) {
+    const int mine = base + lane;
+    if (mine < wk.npg) {
+      int src, page;
+      page_ref(p, wk.b, wk.k0 + mine, src, page);
+      pg[mine] = (src << 28) | page;
+      pmask[mine] = p.src[src].mask[page] & 0xffffu;
     }
+    __syncwarp();
+    if (lane == 0) {
+      const int end = min(base + 32, wk.npg);
+      for (int i = base; i < end; ++i) {
+        const int st = i % kAttnStages;
+        if (i >= kAttnStages && !mbar_wait(empty0 + st * 8, ((i / kAttnStages) - 1) & 1)) {
+          *abort_flag = 1;
+          break;
+        }
+        if (*abort_flag) break;
+        issue_page<S>(p, wk.kvh, pg, i, st, ring, full0, policy);
+        ++issued;
+      }
+    }
+    __syncwarp();
     if (*abort_flag) break;
-    issue_page<S>(p, wk.kvh, pg, i, st, ring, full0, policy);
-    ++issued;
   }
   return issued;
 }
@@ -484,11 +500,21 @@ __global__ void __launch_bounds__((kAttnWarps + 1) * 32)
   const int g = lane >> 2, t = lane & 3;  // fragment row group and column pair
   const Work wk = find_work(p);
   if (tid == 0) s_abort = 0;
-  stage_pages<L>(p, wk, smem);
+  init_barriers<L>(smem);
+  __syncthreads();
+
+  int* pg = reinterpret_cast<int*>(smem + L::off_pg);
+  uint32_t* pmask = reinterpret_cast<uint32_t*>(pg + kMaxChunkPages);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::off_bar);
+  char* ring = smem;
+  const uint32_t full0 = smem_u32(bars), empty0 = full0 + kAttnStages * 8;
+  const bool consumer = w < kAttnWarps;
+  int issued = 0;
+  if (!consumer) issued = produce<S>(p, wk, pg, pmask, ring, full0, empty0, &s_abort);
 
   // Q fragments (A operand, heads as rows; rows 8..15 of the tile are zero)
   uint32_t qa[KS][2];
-  {
+  if (consumer) {
     const T* q = reinterpret_cast<const T*>(p.q) + static_cast<int64_t>(wk.b) * p.q_stride_b +
                  static_cast<int64_t>(wk.kvh) * G * D;
 #pragma unroll
@@ -501,16 +527,6 @@ __global__ void __launch_bounds__((kAttnWarps + 1) * 32)
       }
     }
   }
-  __syncthreads();
-
-  const int* pg = reinterpret_cast<const int*>(smem + L::off_pg);
-  const uint32_t* pmask = reinterpret_cast<const uint32_t*>(pg + kMaxChunkPages);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::off_bar);
-  char* ring = smem;
-  const uint32_t full0 = smem_u32(bars), empty0 = full0 + kAttnStages * 8;
-  const bool consumer = w < kAttnWarps;
-  int issued = 0;
-  if (!consumer && lane == 0) issued = produce<S>(p, wk, pg, ring, full0, empty0, &s_abort);
 
   float m_run = -INFINITY, z_run = 0.f;  // softmax state of head g
   float o[KS][4];                        // O^T tiles: d rows, head columns
@@ -760,7 +776,17 @@ __global__ void __launch_bounds__((kAttnWarps + 1) * 32)
   const int r = lane >> 3, c = lane & 7;
   const Work wk = find_work(p);
   if (tid == 0) s_abort = 0;
-  stage_pages<L>(p, wk, smem);
+  init_barriers<L>(smem);
+  __syncthreads();
+
+  int* pg = reinterpret_cast<int*>(smem + L::off_pg);
+  uint32_t* pmask = reinterpret_cast<uint32_t*>(pg + kMaxChunkPages);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::off_bar);
+  char* ring = smem;
+  const uint32_t full0 = smem_u32(bars), empty0 = full0 + kAttnStages * 8;
+  const bool consumer = w < kAttnWarps;
+  int issued = 0;
+  if (!consumer) issued = produce<S>(p, wk, pg, pmask, ring, full0, empty0, &s_abort);
 
   float* q_s = reinterpret_cast<float*>(smem + L::off_q);
   float* p_s = reinterpret_cast<float*>(smem + L::off_p) + w * L::PSW;
@@ -768,7 +794,7 @@ __global__ void __launch_bounds__((kAttnWarps + 1) * 32)
   {
     const T* q = reinterpret_cast<const T*>(p.q) + static_cast<int64_t>(wk.b) * p.q_stride_b +
                  static_cast<int64_t>(wk.kvh) * G * D;
-    for (int i = tid; i < S::GP * D; i += blockDim.x) {
+    for (int i = tid; consumer && i < S::GP * D; i += kAttnWarps * 32) {
       const int gg = i / D;
       float v = 0.f;
       if (gg < G) {
@@ -780,16 +806,7 @@ __global__ void __launch_bounds__((kAttnWarps + 1) * 32)
       q_s[i] = v * p.qscale;
     }
   }
-  __syncthreads();
-
-  const int* pg = reinterpret_cast<const int*>(smem + L::off_pg);
-  const uint32_t* pmask = reinterpret_cast<const uint32_t*>(pg + kMaxChunkPages);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::off_bar);
-  char* ring = smem;
-  const uint32_t full0 = smem_u32(bars), empty0 = full0 + kAttnStages * 8;
-  const bool consumer = w < kAttnWarps;
-  int issued = 0;
-  if (!consumer && lane == 0) issued = produce<S>(p, wk, pg, ring, full0, empty0, &s_abort);
+  if (consumer) consumer_sync();
 
   float m_run = -INFINITY, z_run = 0.f;  // for the head this lane owns
   float2 acc[G][S::VPL];
@@ -1027,20 +1044,21 @@ cudaError_t launch_kernel(K kern, int smem_bytes, const AttnParams& p, int total
   return cudaGetLastError();
 }
 
+// part 0: the page-streaming kernel; part 1: the combine / score kernel
 template <typename T, int G, int D>
-cudaError_t launch_typed(const AttnParams& p, int total_chunks, cudaStream_t s) {
+cudaError_t launch_typed(const AttnParams& p, int total_chunks, cudaStream_t s, int part) {
   using L = Smem<T, G, D>;
-  cudaError_t e;
+  if (part == 1) {
+    attn_combine_kernel<T, G, D><<<dim3(total_chunks, p.Hkv), kCombineThreads, 0, s>>>(p);
+    return cudaGetLastError();
+  }
   if constexpr (sizeof(T) == 2 && G >= 2) {
     static bool configured = false;
-    e = launch_kernel(attn_split_mma_kernel<G, D>, L::TOTAL, p, total_chunks, s, configured);
+    return launch_kernel(attn_split_mma_kernel<G, D>, L::TOTAL, p, total_chunks, s, configured);
   } else {
     static bool configured = false;
-    e = launch_kernel(attn_split_fma_kernel<T, G, D>, L::TOTAL, p, total_chunks, s, configured);
+    return launch_kernel(attn_split_fma_kernel<T, G, D>, L::TOTAL, p, total_chunks, s, configured);
   }
-  if (e != cudaSuccess) return e;
-  attn_combine_kernel<T, G, D><<<dim3(total_chunks, p.Hkv), kCombineThreads, 0, s>>>(p);
-  return cudaGetLastError();
 }
 
 template <typename T, int G, int D>
@@ -1076,10 +1094,10 @@ int resident_g(int G, int D) {
 }
 
 template <typename T>
-cudaError_t dispatch_g(const AttnParams& p, int total_chunks, cudaStream_t s) {
+cudaError_t dispatch_g(const AttnParams& p, int total_chunks, cudaStream_t s, int part) {
   const int G = p.G, D = p.D;
 #define TKV_CASE(GG, DD) \
-  if (G == GG && D == DD) return launch_typed<T, GG, DD>(p, total_chunks, s);
+  if (G == GG && D == DD) return launch_typed<T, GG, DD>(p, total_chunks, s, part);
   TKV_CASE(1, 64) TKV_CASE(1, 128)
   TKV_CASE(2, 64) TKV_CASE(2, 128)
   TKV_CASE(4, 64) TKV_CASE(4, 128)
@@ -1102,10 +1120,16 @@ int attention_supported(int kv_dtype, int G, int D) {
   return g_ok && (D == 64 || D == 128);
 }
 
-cudaError_t launch_attention(const AttnParams& p, int kv_dtype, int total_chunks, cudaStream_t s) {
+cudaError_t launch_attention_part(const AttnParams& p, int kv_dtype, int total_chunks, cudaStream_t s, int part) {
   if (total_chunks <= 0) return cudaSuccess;
-  if (kv_dtype == 1) return dispatch_g<__nv_bfloat16>(p, total_chunks, s);
-  return dispatch_g<float>(p, total_chunks, s);
+  if (kv_dtype == 1) return dispatch_g<__nv_bfloat16>(p, total_chunks, s, part);
+  return dispatch_g<float>(p, total_chunks, s, part);
+}
+
+cudaError_t launch_attention(const AttnParams& p, int kv_dtype, int total_chunks, cudaStream_t s) {
+  cudaError_t e = launch_attention_part(p, kv_dtype, total_chunks, s, 0);
+  if (e != cudaSuccess) return e;
+  return launch_attention_part(p, kv_dtype, total_chunks, s, 1);
 }
 
 }  // namespace tkv

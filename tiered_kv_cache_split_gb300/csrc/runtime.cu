@@ -187,7 +187,7 @@ Layout make_layout(const tkv_config& c) {
 
 struct TimedPair {
   cudaEvent_t a, b;
-  int kind;  // 0 attention, 1 prefetch
+  int kind;  // 0 attention stream kernel, 1 prefetch, 2 combine / score kernel
 };
 
 }  // namespace
@@ -259,8 +259,10 @@ void harvest(tkv_ctx* h) {
     if (cudaEventElapsedTime(&ms, tp.a, tp.b) == cudaSuccess) {
       if (tp.kind == 0)
         h->stats.attn_ms += ms;
-      else
+      else if (tp.kind == 1)
         h->stats.prefetch_ms += ms;
+      else
+        h->stats.combine_ms += ms;
     }
     h->spare.push_back(tp);
   }
@@ -623,16 +625,23 @@ tkv_status decode_step_device(tkv_ctx* h, const void* q, const void* k_new, cons
     fill_sources(h, l, slot, p);
     p.q = static_cast<const char*>(q) + size_t(l) * y.Hq * y.D * y.esz;
     p.out = static_cast<char*>(out) + size_t(l) * y.Hq * y.D * y.esz;
-    TimedPair tp{};
+    TimedPair tp{}, tc{};
     if (timing) {
       st = timed_pair(h, 0, &tp);
+      if (!st) st = timed_pair(h, 2, &tc);
       if (st) return st;
       CK(h, cudaEventRecord(tp.a, h->cs));
     }
-    CK(h, launch_attention(p, h->cfg.kv_dtype, total_chunks, h->cs));
+    CK(h, launch_attention_part(p, h->cfg.kv_dtype, total_chunks, h->cs, 0));
     if (timing) {
       CK(h, cudaEventRecord(tp.b, h->cs));
+      CK(h, cudaEventRecord(tc.a, h->cs));
+    }
+    CK(h, launch_attention_part(p, h->cfg.kv_dtype, total_chunks, h->cs, 1));
+    if (timing) {
+      CK(h, cudaEventRecord(tc.b, h->cs));
       h->pending.push_back(tp);
+      h->pending.push_back(tc);
     }
     CK(h, cudaEventRecord(h->ev_free[slot], h->cs));
     h->stats.attn_launches += 1;

@@ -14,7 +14,7 @@ constexpr int kMaxBatch = 64;      // sequences per handle (kernel parameters ca
 #define TKV_ATTN_WARPS 4
 #endif
 #ifndef TKV_ATTN_STAGES
-#define TKV_ATTN_STAGES 12
+#define TKV_ATTN_STAGES 8
 #endif
 constexpr int kAttnWarps = TKV_ATTN_WARPS;    // consumer warps per attention CTA (+ 1 producer warp)
 constexpr int kAttnStages = TKV_ATTN_STAGES;  // shared-memory ring of page stages per CTA
@@ -81,6 +81,8 @@ struct AttnParams {
 
 // attention.cu
 cudaError_t launch_attention(const AttnParams& p, int kv_dtype, int total_chunks, cudaStream_t s);
+// part 0: the page-streaming attention kernel; part 1: the combine / score kernel
+cudaError_t launch_attention_part(const AttnParams& p, int kv_dtype, int total_chunks, cudaStream_t s, int part);
 int attention_supported(int kv_dtype, int G, int D);
 // attention CTAs that fit on the current device at once (SMs x CTAs per SM)
 int resident_attention_ctas(int kv_dtype, int G, int D);
