@@ -159,22 +159,25 @@ struct Shape {
   static_assert(D % 32 == 0, "head_dim must be a multiple of 32");
 };
 
-// Shared-memory layout of the attention CTA.
-template <typename T, int G, int D>
+// Shared-memory layout of the attention CTA. The fp32 kernel also keeps the
+// scaled query and per-warp probabilities in shared memory.
+template <typename T, int G, int D, bool FMA>
 struct Smem {
   using S = Shape<T, G, D>;
   static constexpr int RING = kAttnStages * S::STAGE;
-  static constexpr int QS = S::GP * D * 4;
+  static constexpr int QS = FMA ? S::GP * D * 4 : 0;
   static constexpr int PSW = S::GP * kPage + 8;   // floats per warp: p[GP][16], corr[GP]
-  static constexpr int PS = kAttnWarps * PSW * 4;
-  static constexpr int PG = kMaxChunkPages * 8;
+  static constexpr int PS = FMA ? kAttnWarps * PSW * 4 : 0;
+  static constexpr int PG = kMaxChunkPages * 8;   // page reference + valid mask per page
+  static constexpr int DESC = kMaxChunkPages * 16; // producer's copy descriptors per page
   static constexpr int BARS = 2 * kAttnStages * 8;  // full[stages], empty[stages]
   static constexpr int MERGE = kAttnWarps * (G * D + 2 * S::GP) * 4;
   static constexpr int BODY = ((RING > MERGE ? RING : MERGE) + 127) / 128 * 128;
   static constexpr int off_q = BODY;
   static constexpr int off_p = off_q + QS;
   static constexpr int off_pg = off_p + PS;
-  static constexpr int off_bar = (off_pg + PG + 15) / 16 * 16;
+  static constexpr int off_desc = (off_pg + PG + 15) / 16 * 16;
+  static constexpr int off_bar = off_desc + DESC;
   static constexpr int TOTAL = off_bar + BARS;
 };
 
@@ -232,70 +235,73 @@ __device__ __forceinline__ void consumer_sync() {
   asm volatile("bar.sync 1, %0;" ::"r"(kAttnWarps * 32) : "memory");
 }
 
+// A page's copy, resolved once: the source address of its (KV head) record
+// with flags in the low bits (bit 0: 8-bit page, bit 1: per-head scales), and
+// for 8-bit pages the address of its scale record.
+struct PageCopy {
+  unsigned long long src;
+  unsigned long long scales;
+};
+
 // Producer lane: bulk-copy page i of the chunk into ring stage st, completing
 // the stage's "full" barrier with the page's byte count.
 template <typename S>
-__device__ __forceinline__ void issue_page(const AttnParams& p, int kvh, const int* pg, int i, int st,
-                                           char* ring, uint32_t full0, uint64_t policy) {
-  const int ref = pg[i];
-  const int src = ref >> 28, page = ref & 0x0fffffff;
-  const PageSource& ps = p.src[src];
-  const char* gsrc = ps.base + static_cast<int64_t>(page) * ps.page_bytes +
-                     static_cast<int64_t>(kvh) * ps.head_bytes;
+__device__ __forceinline__ void issue_page(const PageCopy& c, int st, char* ring, uint32_t full0,
+                                           uint64_t policy) {
+  const bool i8 = c.src & 1ull;
+  const char* gsrc = reinterpret_cast<const char*>(c.src & ~15ull);
   const uint32_t dst = smem_u32(ring + st * S::STAGE);
   const uint32_t bar = full0 + st * 8;
-  const bool i8 = ps.kind == SRC_INT8;
   const uint32_t bytes = i8 ? 2u * kPage * (S::ROWB / S::ESZ) : 2u * S::BLK;
-  const uint32_t sbytes = i8 ? (ps.scale_per_head ? 64u : 128u) : 0u;
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  const uint32_t sbytes = i8 ? ((c.src & 2ull) ? 64u : 128u) : 0u;
   mbar_expect_tx(bar, bytes + sbytes);
   bulk_g2s(dst, gsrc, bytes, bar, policy);
-  if (sbytes) {
-    const char* sg = ps.scales + static_cast<int64_t>(page) * ps.scale_page_bytes +
-                     (ps.scale_per_head ? static_cast<int64_t>(kvh) * 64 : 0);
-    bulk_g2s(dst + 2 * S::BLK, sg, sbytes, bar, policy);
-  }
+  if (sbytes) bulk_g2s(dst + 2 * S::BLK, reinterpret_cast<const char*>(c.scales), sbytes, bar, policy);
 }
 
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
-// The producer warp's job: resolve the chunk's pages 32 at a time (one per
-// lane: source, pool page, valid mask, published in shared memory for the
-// consumers) and let lane 0 keep the ring full. Returns the pages issued (lane 0).
+// The producer warp's job: resolve every page of the chunk (one lane per page:
+// source, pool page, valid mask and copy descriptor, published in shared
+// memory), then let lane 0 keep the ring full. Returns the pages issued (lane 0).
 template <typename S>
-__device__ int produce(const AttnParams& p, const Work& wk, int* pg, uint32_t* pmask, char* ring,
-                       uint32_t full0, uint32_t empty0, volatile int* abort_flag) {
+__device__ int produce(const AttnParams& p, const Work& wk, int* pg, uint32_t* pmask, PageCopy* desc,
+                       char* ring, uint32_t full0, uint32_t empty0, volatile int* abort_flag) {
   const int lane = threadIdx.x & 31;
-  uint64_t policy;
-  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(policy));
-  int issued = 0;
-  for (int base = 0; base < wk.npg; base += 32) {
-    const int mine = base + lane;
-    if (mine < wk.npg) {
-      int src, page;
-      page_ref(p, wk.b, wk.k0 + mine, src, page);
-      pg[mine] = (src << 28) | page;
-      pmask[mine] = p.src[src].mask[page] & 0xffffu;
-    }
-    __syncwarp();
-    if (lane == 0) {
-      const int end = min(base + 32, wk.npg);
-      for (int i = base; i < end; ++i) {
-        const int st = i % kAttnStages;
-        if (i >= kAttnStages && !mbar_wait(empty0 + st * 8, ((i / kAttnStages) - 1) & 1)) {
-          *abort_flag = 1;
-          break;
-        }
-        if (*abort_flag) break;
-        issue_page<S>(p, wk.kvh, pg, i, st, ring, full0, policy);
-        ++issued;
-      }
-    }
-    __syncwarp();
-    if (*abort_flag) break;
+  for (int i = lane; i < wk.npg; i += 32) {
+    int src, page;
+    page_ref(p, wk.b, wk.k0 + i, src, page);
+    const PageSource& ps = p.src[src];
+    pg[i] = (src << 28) | page;
+    pmask[i] = ps.mask[page] & 0xffffu;
+    const bool i8 = ps.kind == SRC_INT8;
+    PageCopy c;
+    c.src = reinterpret_cast<unsigned long long>(ps.base + static_cast<int64_t>(page) * ps.page_bytes +
+                                                 static_cast<int64_t>(wk.kvh) * ps.head_bytes) |
+            (i8 ? 1ull : 0ull) | ((i8 && ps.scale_per_head) ? 2ull : 0ull);
+    c.scales = i8 ? reinterpret_cast<unsigned long long>(ps.scales + static_cast<int64_t>(page) * ps.scale_page_bytes +
+                                                         (ps.scale_per_head ? static_cast<int64_t>(wk.kvh) * 64 : 0))
+                  : 0ull;
+    desc[i] = c;
   }
+  __syncwarp();
+  int issued = 0;
+  if (lane == 0) {
+    uint64_t policy;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(policy));
+    for (int i = 0; i < wk.npg; ++i) {
+      const int st = i % kAttnStages;
+      if (i >= kAttnStages && !mbar_wait(empty0 + st * 8, ((i / kAttnStages) - 1) & 1)) {
+        *abort_flag = 1;
+        break;
+      }
+      issue_page<S>(desc[i], st, ring, full0, policy);
+      ++issued;
+    }
+  }
+  __syncwarp();
   return issued;
 }
 
@@ -359,7 +365,7 @@ __device__ void write_partial(const AttnParams& p, const Work& wk, char* smem) {
 // sequence's page list. Masked slots hold -inf logits, so they add exactly 0
 // and no page metadata is read here. Loads are batched so that each phase
 // costs about one memory round trip.
-constexpr int kCombineThreads = 128;
+constexpr int kCombineThreads = 256;
 constexpr int kMaxCombineChunks = kMaxChunksPerSeq;
 
 template <typename T, int G, int D>
@@ -369,6 +375,9 @@ __global__ void __launch_bounds__(kCombineThreads) attn_combine_kernel(const __g
   __shared__ float cM[8], cIZ[8];
   const int tid = threadIdx.x;
   const Work wk = find_work(p);
+  // launched as a programmatic dependent of the attention kernel: wait here
+  // until its partials and spilled logits are complete and visible
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int64_t base = static_cast<int64_t>(wk.cf) * p.Hkv + wk.kvh;  // partial of chunk j: base + j * Hkv
   const int nch = min(wk.nch, kMaxCombineChunks);
   for (int e = tid; e < nch * G; e += kCombineThreads) {
@@ -420,7 +429,7 @@ __global__ void __launch_bounds__(kCombineThreads) attn_combine_kernel(const __g
     M[g] = cM[g];
     IZ[g] = cIZ[g];
   }
-  constexpr int U = 4;
+  constexpr int U = 2;
   const int items = wk.npg * kPage;
   for (int first = tid; first < items; first += kCombineThreads * U) {
     float l[U][G], old[U];
@@ -485,11 +494,11 @@ __device__ __forceinline__ void widen_i8_page(char* stage, int lane) {
 }
 
 template <int G, int D>
-__global__ void __launch_bounds__((kAttnWarps + 1) * 32)
+__global__ void __launch_bounds__((kAttnWarps + 1) * 32, 3)
     attn_split_mma_kernel(const __grid_constant__ AttnParams p) {
   using T = __nv_bfloat16;
   using S = Shape<T, G, D>;
-  using L = Smem<T, G, D>;
+  using L = Smem<T, G, D, false>;
   constexpr int KS = D / 16;  // k-steps of QK over d, and m-tiles of PV over d
   static_assert(G >= 2 && G <= 8, "tensor-core path serves 2..8 query heads per KV head");
   extern __shared__ __align__(128) char smem[];
@@ -510,7 +519,8 @@ __global__ void __launch_bounds__((kAttnWarps + 1) * 32)
   const uint32_t full0 = smem_u32(bars), empty0 = full0 + kAttnStages * 8;
   const bool consumer = w < kAttnWarps;
   int issued = 0;
-  if (!consumer) issued = produce<S>(p, wk, pg, pmask, ring, full0, empty0, &s_abort);
+  if (!consumer)
+    issued = produce<S>(p, wk, pg, pmask, reinterpret_cast<PageCopy*>(smem + L::off_desc), ring, full0, empty0, &s_abort);
 
   // Q fragments (A operand, heads as rows; rows 8..15 of the tile are zero)
   uint32_t qa[KS][2];
@@ -644,7 +654,12 @@ __global__ void __launch_bounds__((kAttnWarps + 1) * 32)
       mma_bf16(o[mt], a0, a1, a2, a3, pb0, pb1);
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(empty0 + st * 8);
+    if (lane == 0) {
+      // the stage was written through the generic proxy (widened codes, zeroed
+      // rows): order those writes before the next bulk copy into it
+      if (i8 || mask != 0xffffu) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      mbar_arrive(empty0 + st * 8);
+    }
   }
 
   __syncthreads();
@@ -767,7 +782,7 @@ template <typename T, int G, int D>
 __global__ void __launch_bounds__((kAttnWarps + 1) * 32)
     attn_split_fma_kernel(const __grid_constant__ AttnParams p) {
   using S = Shape<T, G, D>;
-  using L = Smem<T, G, D>;
+  using L = Smem<T, G, D, true>;
   extern __shared__ __align__(128) char smem[];
   __shared__ volatile int s_abort;
 
@@ -786,7 +801,8 @@ __global__ void __launch_bounds__((kAttnWarps + 1) * 32)
   const uint32_t full0 = smem_u32(bars), empty0 = full0 + kAttnStages * 8;
   const bool consumer = w < kAttnWarps;
   int issued = 0;
-  if (!consumer) issued = produce<S>(p, wk, pg, pmask, ring, full0, empty0, &s_abort);
+  if (!consumer)
+    issued = produce<S>(p, wk, pg, pmask, reinterpret_cast<PageCopy*>(smem + L::off_desc), ring, full0, empty0, &s_abort);
 
   float* q_s = reinterpret_cast<float*>(smem + L::off_q);
   float* p_s = reinterpret_cast<float*>(smem + L::off_p) + w * L::PSW;
@@ -1047,10 +1063,20 @@ cudaError_t launch_kernel(K kern, int smem_bytes, const AttnParams& p, int total
 // part 0: the page-streaming kernel; part 1: the combine / score kernel
 template <typename T, int G, int D>
 cudaError_t launch_typed(const AttnParams& p, int total_chunks, cudaStream_t s, int part) {
-  using L = Smem<T, G, D>;
+  constexpr bool kMma = sizeof(T) == 2 && G >= 2;
+  using L = Smem<T, G, D, !kMma>;
   if (part == 1) {
-    attn_combine_kernel<T, G, D><<<dim3(total_chunks, p.Hkv), kCombineThreads, 0, s>>>(p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(total_chunks, p.Hkv);
+    cfg.blockDim = dim3(kCombineThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, attn_combine_kernel<T, G, D>, p);
   }
   if constexpr (sizeof(T) == 2 && G >= 2) {
     static bool configured = false;
@@ -1063,7 +1089,8 @@ cudaError_t launch_typed(const AttnParams& p, int total_chunks, cudaStream_t s, 
 
 template <typename T, int G, int D>
 int resident_typed() {
-  using L = Smem<T, G, D>;
+  constexpr bool kMma = sizeof(T) == 2 && G >= 2;
+  using L = Smem<T, G, D, !kMma>;
   int dev = 0, sms = 0, per_sm = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 304;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 304;
