@@ -36,6 +36,23 @@ def _peaks():
     return 6800.0, "fallback"
 
 
+def _traffic(workload):
+    """DRAM read + write bytes per attention launch from the committed ncu
+    capture, or None when there is none for this workload or the kernel source
+    changed since it was taken."""
+    import hashlib
+    tp = os.path.join(ROOT, "profiles", "attention_traffic.json")
+    if not os.path.exists(tp):
+        return None
+    rec = json.load(open(tp)).get(workload)
+    if not rec:
+        return None
+    src = os.path.join(ROOT, "tiered_kv_cache_split_gb300", "csrc", "attention.cu")
+    if hashlib.sha256(open(src, "rb").read()).hexdigest() != rec.get("attention_cu_sha256"):
+        return None
+    return rec["traffic_bytes_per_launch"]
+
+
 def _workload(name):
     from synth import WORKLOADS
     return WORKLOADS[name]
@@ -237,12 +254,9 @@ def run_gpu(args):
     achieved = bytes_per_launch / (attn_ms * 1e6) if attn_ms > 0 else 0.0
     pair = bytes_per_launch / ((attn_ms + combine_ms) * 1e6) if attn_ms > 0 else 0.0
     prefetch_gbs = st["prefetch_bytes"] / (st["prefetch_ms"] * 1e6) if st["prefetch_ms"] > 0 else None
-    launches = K * (w.n_layers + 2) + st["reclassifies"] * 4
+    launches = st["kernel_launches"]   # counted by the library over the timed region
     clocks = clk.summary()
-    traffic = None
-    tp = os.path.join(ROOT, "profiles", "attention_traffic.json")
-    if os.path.exists(tp):
-        traffic = json.load(open(tp)).get(w.name)
+    traffic = _traffic(w.name)
     line = {
         "metric": METRIC, "value": ws * K / (ms_max / 1000.0), "unit": "steps/s", "n_gpus": ws,
         "steps": K, "warmup": W, "ms_per_step": ms_max / K, "higher_is_better": True,

@@ -110,6 +110,7 @@ typedef struct {
   double combine_ms;           /* summed combine / score kernel time  (TKV_FLAG_TIMING) */
   double prefetch_ms;          /* summed prefetch copy time      (TKV_FLAG_TIMING) */
   double reclassify_ms;        /* summed reclassify wall time    (TKV_FLAG_TIMING) */
+  int64_t kernel_launches;     /* kernels this handle launched (steps, reclassify, prefill) */
 } tkv_stats;
 
 /* Device and pinned-host bytes tkv_create needs for this configuration. */

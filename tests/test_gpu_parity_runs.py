@@ -13,7 +13,7 @@ from helpers import (OUT_ATOL, assert_page_tables_equal, assert_scores_close, pr
                      prefill_oracle)
 from oracle import OracleCache
 from oracle.classify import T2
-from synth import CHAIN7B, TINY
+from synth import CHAIN7B, MHA16K, TINY, long128k
 
 pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda:0")
@@ -78,3 +78,26 @@ def test_chain7b_shape_until_all_four_tiers_exist():
     worst, oc = _run(CHAIN7B, 448, check_rows=False)
     counts = np.bincount(oc.seqs[0].tier, minlength=4)
     assert np.all(counts > 0), counts
+
+
+def test_mha_shape_with_delayed_spikes_and_per_head_fp16_scales():
+    # the MHA configuration (32 query = 32 KV heads, d = 128, bf16; T2 codes with
+    # one float16 scale per token and KV head; keys with delayed spikes) at 2
+    # layers, 2 requests of 700 tokens and Delta = 16, so that 64 steps make four
+    # reassignments over every tier.
+    w = MHA16K.replace(n_layers=2, batch=2, context=("fixed", 700), prompt_len=64,
+                       key_scale=("delayed_spikes", 0.02, 6.0, 40, 4), reclassify_interval=16, n_steps=64)
+    worst, oc = _run(w, 64)
+    for b in range(w.batch):
+        assert np.all(np.bincount(oc.seqs[b].tier, minlength=4) > 0)
+
+
+@pytest.mark.parametrize("t0", [25, 75])
+def test_long_context_shape_without_t2(t0):
+    # the long-context sweep (32 query / 8 KV heads, d = 128, bf16, lognormal(0, 1)
+    # key scale, T2 = 0, T3 = 5%) at 2 layers, 2 requests of 3000 tokens, Delta = 16.
+    w = long128k(t0).replace(n_layers=2, batch=2, context=("fixed", 3000), reclassify_interval=16, n_steps=48)
+    worst, oc = _run(w, 48)
+    for b in range(w.batch):
+        counts = np.bincount(oc.seqs[b].tier, minlength=4)
+        assert counts[2] == 0 and counts[0] > 0 and counts[1] > 0 and counts[3] > 0, counts

@@ -116,7 +116,7 @@ std::string validate(const tkv_config& c) {
   if (!combo_ok) return bad("T2 scales: per-token scales are float32, per-token-head scales float16");
   if (c.t2_mode != TKV_T2_ATTEND && c.t2_mode != TKV_T2_MASK) return bad("t2_mode");
   if (c.t0_pages < 0 || c.t1_pages < 0 || c.t2_pages < 0 || c.max_staged_movers < 0) return bad("negative capacity");
-  if (c.split_pages < 0 || c.split_pages > kMaxChunkPages) return bad("split_pages must be 0..128");
+  if (c.split_pages < 0 || c.split_pages > kMaxChunkPages) return bad("split_pages must be 0..256");
   return std::string();
 }
 
@@ -244,6 +244,14 @@ tkv_status fail_cuda(tkv_ctx* h, const char* what, cudaError_t e) {
   do {                                                         \
     cudaError_t e_ = (call);                                   \
     if (e_ != cudaSuccess) return fail_cuda((h), #call, e_);   \
+  } while (0)
+
+// A kernel launch that took place when `launched` holds (launchers return
+// early without a launch on empty work); counted in the handle's statistics.
+#define LK(h, call, launched)                                  \
+  do {                                                         \
+    CK(h, call);                                               \
+    if (launched) (h)->stats.kernel_launches += 1;             \
   } while (0)
 
 tkv_status check_usable(tkv_ctx* h) {
@@ -583,7 +591,7 @@ tkv_status decode_step_device(tkv_ctx* h, const void* q, const void* k_new, cons
     ap.np0[b] = static_cast<int32_t>(np_before);
     ap.pos[b] = pos;
   }
-  CK(h, launch_append(ap, h->cs));
+  LK(h, launch_append(ap, h->cs), B > 0);
 
   // ---- per layer: prefetch T1/T2 (copy stream), attention + fused scores (compute stream)
   AttnParams p{};
@@ -632,12 +640,12 @@ tkv_status decode_step_device(tkv_ctx* h, const void* q, const void* k_new, cons
       if (st) return st;
       CK(h, cudaEventRecord(tp.a, h->cs));
     }
-    CK(h, launch_attention_part(p, h->cfg.kv_dtype, total_chunks, h->cs, 0));
+    LK(h, launch_attention_part(p, h->cfg.kv_dtype, total_chunks, h->cs, 0), total_chunks > 0);
     if (timing) {
       CK(h, cudaEventRecord(tp.b, h->cs));
       CK(h, cudaEventRecord(tc.a, h->cs));
     }
-    CK(h, launch_attention_part(p, h->cfg.kv_dtype, total_chunks, h->cs, 1));
+    LK(h, launch_attention_part(p, h->cfg.kv_dtype, total_chunks, h->cs, 1), total_chunks > 0);
     if (timing) {
       CK(h, cudaEventRecord(tc.b, h->cs));
       h->pending.push_back(tp);
@@ -667,7 +675,7 @@ tkv_status decode_step_device(tkv_ctx* h, const void* q, const void* k_new, cons
   fp.acc = reinterpret_cast<float*>(h->D(y.o_acc));
   fp.acc_stride = 3 * y.maxp * kPage;
   fp.inv_lh = 1.0 / (double(y.L) * double(y.Hq));
-  CK(h, launch_fold(fp, h->cs));
+  LK(h, launch_fold(fp, h->cs), fp.B > 0 && fp.max_slots > 0);
 
   h->steps += 1;
   h->stats.steps += 1;
@@ -718,7 +726,7 @@ tkv_status do_reclassify(tkv_ctx* h) {
     int64_t nmax = 0;
     for (const Seq& sq : h->seqs) nmax = std::max(nmax, sq.N);
     CK(h, cudaMemcpy2DAsync(h->d_tier, y.maxtok, arena, y.maxtok, nmax, B, cudaMemcpyHostToDevice, h->cs));
-    CK(h, launch_classify(cp, h->cs));
+    LK(h, launch_classify(cp, h->cs), cp.B > 0);
     CK(h, cudaMemcpy2DAsync(arena, y.maxtok, h->d_tier_new, y.maxtok, nmax, B, cudaMemcpyDeviceToHost, h->cs));
     tkv_status st = sync_all(h);
     if (st) return st;
@@ -848,14 +856,14 @@ tkv_status do_reclassify(tkv_ctx* h) {
   mp.pools.scale_f16 = h->cfg.t2_scale_dtype == TKV_SCALE_F16;
   mp.temp = h->D(y.o_temp);
   mp.mode = MOVE_GATHER;
-  CK(h, launch_move(mp, dm, int64_t(phase2.size()), h->cs));
+  LK(h, launch_move(mp, dm, int64_t(phase2.size()), h->cs), !phase2.empty());
   mp.mode = MOVE_DIRECT;
-  CK(h, launch_move(mp, dm + phase2.size(), int64_t(phase1.size()), h->cs));
+  LK(h, launch_move(mp, dm + phase2.size(), int64_t(phase1.size()), h->cs), !phase1.empty());
   mp.mode = MOVE_SCATTER;
-  CK(h, launch_move(mp, dm, int64_t(phase2.size()), h->cs));
+  LK(h, launch_move(mp, dm, int64_t(phase2.size()), h->cs), !phase2.empty());
   // T0 compaction last: every slot it writes has been read by the moves above
   mp.mode = MOVE_DIRECT;
-  CK(h, launch_move(mp, dm + phase2.size() + phase1.size(), int64_t(compaction.size()), h->cs));
+  LK(h, launch_move(mp, dm + phase2.size() + phase1.size(), int64_t(compaction.size()), h->cs), !compaction.empty());
   tkv_status st = upload_metadata(h);
   if (st) return st;
   std::swap(h->d_tier, h->d_tier_new);
@@ -1014,7 +1022,7 @@ tkv_status tkv_append(tkv_handle h, int32_t seq, const void* k, const void* v, i
   pp.L = y.L; pp.Hkv = y.Hkv; pp.D = y.D; pp.esz = y.esz; pp.n = n_tokens;
   pp.k = static_cast<const char*>(k); pp.v = static_cast<const char*>(v); pp.loc = dl;
   pp.pool0 = h->D(y.o_pool0); pp.layer_bytes = y.cap[0] * y.plb[0]; pp.page_bytes = y.plb[0];
-  CK(h, launch_prefill(pp, h->cs));
+  LK(h, launch_prefill(pp, h->cs), n_tokens > 0);
   if (tkv_status st = upload_metadata(h)) return st;
   return sync_all(h);
 }
