@@ -265,7 +265,7 @@ def run_gpu(args):
         "roofline": {"bound": "hbm", "kernel": "attn_split_mma_kernel", "achieved": achieved, "peak": peak,
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": traffic, "bytes_per_launch": bytes_per_launch,
-                     "launch_ms": attn_ms, "combine_ms": combine_ms,
+                     "launch_ms": attn_ms, "combine_ms_per_layer": combine_ms,
                      "with_combine": {"achieved": pair, "frac": pair / peak}},
         "kv_read_gbs": achieved,
         "link": {"prefetch_gbs": prefetch_gbs, "probe_h2d_gbs": link_gbs,
@@ -273,6 +273,9 @@ def run_gpu(args):
                  "prefetch_bytes_per_step": st["prefetch_bytes"] / K},
         "reclassify_ms": st["reclassify_ms"] / max(st["reclassifies"], 1) if st["reclassifies"] else None,
         "reclassifies_in_timed_region": st["reclassifies"],
+        "movers_per_reclassify": st["movers"] / max(st["reclassifies"], 1),
+        "move_bytes_per_reclassify": {"h2d": st["h2d_move_bytes"] / max(st["reclassifies"], 1),
+                                      "d2h": st["d2h_move_bytes"] / max(st["reclassifies"], 1)},
         "tier_counts": st["tier_counts"],
         "e2e": {"value": ws * K / e2e_s, "unit": "steps/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},

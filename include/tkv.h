@@ -106,8 +106,10 @@ typedef struct {
   int64_t h2d_move_bytes;      /* bytes moved host -> device at reclassify */
   int64_t d2h_move_bytes;      /* bytes moved device -> host at reclassify */
   int64_t tier_counts[4];      /* current tokens per tier over all sequences */
-  double attn_ms;              /* summed attention stream-kernel time (TKV_FLAG_TIMING) */
-  double combine_ms;           /* summed combine / score kernel time  (TKV_FLAG_TIMING) */
+  double attn_ms;              /* summed attention kernel time; each launch also finishes the
+                                  previous layer's output merge and score epilogue (TKV_FLAG_TIMING) */
+  double combine_ms;           /* summed time of the last layer's epilogue kernel, one launch per
+                                  step (TKV_FLAG_TIMING) */
   double prefetch_ms;          /* summed prefetch copy time      (TKV_FLAG_TIMING) */
   double reclassify_ms;        /* summed reclassify wall time    (TKV_FLAG_TIMING) */
   int64_t kernel_launches;     /* kernels this handle launched (steps, reclassify, prefill) */

@@ -26,11 +26,13 @@
 // Per page both keep an online softmax per head in base 2 (log2(e)/sqrt(d)
 // applied to the logits) and spill the raw logits. The warps of a CTA merge
 // (m, Z, O) in shared memory and the CTA writes its partial; no CTA ever waits
-// on another. attn_combine_kernel then runs one CTA per (chunk, KV head): it
-// forms the global (M, Z) of each head from the partials, the chunk-0 CTA
-// merges the partial outputs, and every CTA turns its chunk's spilled logits
-// into exact softmax weights alpha = exp2(l - M) / Z summed over the G heads,
-// added to a slot-indexed score accumulator (the fused score epilogue).
+// on another. A layer's epilogue — the global (M, Z) of each head from the
+// partials, the merged output (each chunk's CTA merges a slice), and the exact
+// softmax weights alpha = exp2(l - M) / Z of the chunk's slots summed over the
+// G heads, added to a slot-indexed score accumulator (the fused score
+// epilogue) — runs in the consumer warps of the NEXT layer's attention launch,
+// before their first page, while the producer warp already fills the ring.
+// The last layer's epilogue (or a lone layer's) is attn_combine_kernel.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -263,6 +265,16 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
+// Per-page word the producer publishes for the consumers: valid-slot bits in
+// the low 16 bits, then the page's source traits, so that the consumers never
+// index the source table.
+constexpr uint32_t kFlagI8 = 1u << 16, kFlagPerHead = 1u << 17;
+constexpr int kFlagSwzShift = 18;
+__device__ __forceinline__ uint32_t page_flags(uint32_t valid, bool i8, bool per_head, int swz) {
+  return (valid & 0xffffu) | (i8 ? kFlagI8 : 0u) | (per_head ? kFlagPerHead : 0u) |
+         (static_cast<uint32_t>(swz & 7) << kFlagSwzShift);
+}
+
 // The producer warp's job: resolve every page of the chunk (one lane per page:
 // source, pool page, valid mask and copy descriptor, published in shared
 // memory), then let lane 0 keep the ring full. Returns the pages issued (lane 0).
@@ -275,8 +287,8 @@ __device__ int produce(const AttnParams& p, const Work& wk, int* pg, uint32_t* p
     page_ref(p, wk.b, wk.k0 + i, src, page);
     const PageSource& ps = p.src[src];
     pg[i] = (src << 28) | page;
-    pmask[i] = ps.mask[page] & 0xffffu;
     const bool i8 = ps.kind == SRC_INT8;
+    pmask[i] = page_flags(ps.mask[page], i8, ps.scale_per_head != 0, ps.swz);
     PageCopy c;
     c.src = reinterpret_cast<unsigned long long>(ps.base + static_cast<int64_t>(page) * ps.page_bytes +
                                                  static_cast<int64_t>(wk.kvh) * ps.head_bytes) |
@@ -358,84 +370,86 @@ __device__ void write_partial(const AttnParams& p, const Work& wk, char* smem) {
   }
 }
 
-// One CTA per (chunk, KV head), after the attention kernel: global (M, Z) per
-// head from the sequence's partials; each CTA merges a slice of the partial
-// outputs into the output, and adds the exact softmax weights of its own chunk,
-// summed over the G heads, to the score accumulator at slot 16 * k + row of the
-// sequence's page list. Masked slots hold -inf logits, so they add exactly 0
-// and no page metadata is read here. Loads are batched so that each phase
-// costs about one memory round trip.
-constexpr int kCombineThreads = 256;
-constexpr int kMaxCombineChunks = kMaxChunksPerSeq;
+// The epilogue of one (chunk, KV head) of a finished layer, run by NT threads
+// (tid < NT, NT a multiple of 32): global (M, Z) of each head from the
+// sequence's chunk partials (one warp per head), this chunk's slice of the
+// merged output, and the exact softmax weights alpha = exp2(l - M) / Z of this
+// chunk's slots, summed over the G heads and added to the score accumulator at
+// slot 16 * k + row of the sequence's page list (the fused score epilogue of
+// Methodology 2). Masked slots hold -inf logits, so they add exactly 0 and no
+// page metadata is read. `sync` synchronises the NT threads.
+struct LayerBufs {
+  const float* part_o;
+  const float* part_m;
+  const float* part_z;
+  const float* spill;
+  void* out;
+};
 
-template <typename T, int G, int D>
-__global__ void __launch_bounds__(kCombineThreads) attn_combine_kernel(const __grid_constant__ AttnParams p) {
-  __shared__ float sm_m[kMaxCombineChunks][8], sm_z[kMaxCombineChunks][8];
-  __shared__ float sm_w[kMaxCombineChunks][8];  // exp2(m_j - M) / Z per chunk and head
-  __shared__ float cM[8], cIZ[8];
-  const int tid = threadIdx.x;
-  const Work wk = find_work(p);
-  // launched as a programmatic dependent of the attention kernel: wait here
-  // until its partials and spilled logits are complete and visible
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+template <typename T, int G, int D, int NT, typename Sync>
+__device__ void layer_epilogue(const AttnParams& p, const LayerBufs& lb, const Work& wk, int tid,
+                               float* sM, float* sIZ, Sync sync) {
+  const int warp = tid >> 5, lane = tid & 31;
   const int64_t base = static_cast<int64_t>(wk.cf) * p.Hkv + wk.kvh;  // partial of chunk j: base + j * Hkv
-  const int nch = min(wk.nch, kMaxCombineChunks);
-  for (int e = tid; e < nch * G; e += kCombineThreads) {
-    const int j = e / G, g = e % G;
-    const int64_t pj = (base + static_cast<int64_t>(j) * p.Hkv) * G + g;
-    sm_m[j][g] = __ldg(p.part_m + pj);
-    sm_z[j][g] = __ldg(p.part_z + pj);
-  }
-  __syncthreads();
-  if (tid < G) {
+  const int nch = wk.nch;
+  for (int g = warp; g < G; g += NT / 32) {
     float M = -INFINITY;
-    for (int j = 0; j < nch; ++j) M = fmaxf(M, sm_m[j][tid]);
+    for (int j = lane; j < nch; j += 32) M = fmaxf(M, __ldg(lb.part_m + (base + static_cast<int64_t>(j) * p.Hkv) * G + g));
+#pragma unroll
+    for (int m = 16; m >= 1; m >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, m));
     float Z = 0.f;
     if (M != -INFINITY)
-      for (int j = 0; j < nch; ++j)
-        if (sm_m[j][tid] != -INFINITY) Z += sm_z[j][tid] * exp2f(sm_m[j][tid] - M);
-    cM[tid] = M;
-    cIZ[tid] = Z > 0.f ? 1.f / Z : 0.f;
+      for (int j = lane; j < nch; j += 32) {
+        const int64_t pj = (base + static_cast<int64_t>(j) * p.Hkv) * G + g;
+        const float mj = __ldg(lb.part_m + pj);
+        if (mj != -INFINITY) Z += __ldg(lb.part_z + pj) * exp2f(mj - M);
+      }
+#pragma unroll
+    for (int m = 16; m >= 1; m >>= 1) Z += __shfl_xor_sync(kFull, Z, m);
+    if (lane == 0) {
+      sM[g] = M;
+      sIZ[g] = Z > 0.f ? 1.f / Z : 0.f;
+    }
   }
-  __syncthreads();
-  for (int e = tid; e < nch * G; e += kCombineThreads) {
-    const int j = e / G, g = e % G;
-    const float mj = sm_m[j][g];
-    sm_w[j][g] = (mj == -INFINITY || cM[g] == -INFINITY) ? 0.f : exp2f(mj - cM[g]) * cIZ[g];
-  }
-  __syncthreads();
+  sync();
   {
     // this chunk's slice of the G * D outputs
-    const int lo = static_cast<int>((static_cast<int64_t>(wk.jc) * G * D) / wk.nch);
-    const int hi = static_cast<int>((static_cast<int64_t>(wk.jc + 1) * G * D) / wk.nch);
-    T* out = reinterpret_cast<T*>(p.out) + static_cast<int64_t>(wk.b) * p.out_stride_b +
+    const int lo = static_cast<int>((static_cast<int64_t>(wk.jc) * G * D) / nch);
+    const int hi = static_cast<int>((static_cast<int64_t>(wk.jc + 1) * G * D) / nch);
+    T* out = reinterpret_cast<T*>(lb.out) + static_cast<int64_t>(wk.b) * p.out_stride_b +
              static_cast<int64_t>(wk.kvh) * G * D;
-    for (int idx = lo + tid; idx < hi; idx += kCombineThreads) {
+    for (int idx = lo + tid; idx < hi; idx += NT) {
       const int g = idx / D;
+      const float Mg = sM[g], IZg = sIZ[g];
       float o = 0.f;
-#pragma unroll 8
-      for (int j = 0; j < nch; ++j)
-        o += __ldg(p.part_o + (base + static_cast<int64_t>(j) * p.Hkv) * G * D + idx) * sm_w[j][g];
+      if (Mg != -INFINITY) {
+#pragma unroll 4
+        for (int j = 0; j < nch; ++j) {
+          const int64_t pj = base + static_cast<int64_t>(j) * p.Hkv;
+          const float mj = __ldg(lb.part_m + pj * G + g);
+          if (mj != -INFINITY) o += __ldg(lb.part_o + pj * G * D + idx) * (exp2f(mj - Mg) * IZg);
+        }
+      }
       store_out(out + idx, o);
     }
   }
   if (p.acc == nullptr) return;
-  const float* __restrict__ spill_b = p.spill + (static_cast<int64_t>(wk.b) * p.Hkv + wk.kvh) * p.spill_stride;
+  const float* __restrict__ spill_b = lb.spill + (static_cast<int64_t>(wk.b) * p.Hkv + wk.kvh) * p.spill_stride;
   float* __restrict__ accb = p.acc + static_cast<int64_t>(wk.b) * p.acc_stride_b +
                              static_cast<int64_t>(wk.kvh) * p.acc_stride_h;
   float M[G], IZ[G];
 #pragma unroll
   for (int g = 0; g < G; ++g) {
-    M[g] = cM[g];
-    IZ[g] = cIZ[g];
+    M[g] = sM[g];
+    IZ[g] = sIZ[g];
   }
-  constexpr int U = 2;
+  constexpr int U = 4;
   const int items = wk.npg * kPage;
-  for (int first = tid; first < items; first += kCombineThreads * U) {
+  for (int first = tid; first < items; first += NT * U) {
     float l[U][G], old[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      const int item = first + u * kCombineThreads;
+      const int item = first + u * NT;
       if (item < items) {
         const int k = wk.k0 + (item >> 4), row = item & 15;
 #pragma unroll
@@ -445,7 +459,7 @@ __global__ void __launch_bounds__(kCombineThreads) attn_combine_kernel(const __g
     }
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      const int item = first + u * kCombineThreads;
+      const int item = first + u * NT;
       if (item < items) {
         const int k = wk.k0 + (item >> 4), row = item & 15;
         float a = 0.f;
@@ -457,25 +471,51 @@ __global__ void __launch_bounds__(kCombineThreads) attn_combine_kernel(const __g
   }
 }
 
+// The epilogue of a layer as a kernel of its own: one CTA per (chunk, KV head),
+// launched as a programmatic dependent of that layer's attention kernel (used
+// for a single layer, and for the last layer of a decode step).
+constexpr int kCombineThreads = 256;
+
+template <typename T, int G, int D>
+__global__ void __launch_bounds__(kCombineThreads) attn_combine_kernel(const __grid_constant__ AttnParams p) {
+  __shared__ float sM[8], sIZ[8];
+  const Work wk = find_work(p);
+  // wait here until the attention kernel's partials and spilled logits are complete and visible
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const LayerBufs lb{p.part_o, p.part_m, p.part_z, p.spill, p.out};
+  layer_epilogue<T, G, D, kCombineThreads>(p, lb, wk, threadIdx.x, sM, sIZ, [] { __syncthreads(); });
+}
+
+// The previous layer's epilogue, run by an attention CTA's consumer warps
+// before they take their first page (the producer warp meanwhile fills the
+// ring): the same (chunk, KV head) split, since every layer of a step has the
+// same chunk plan.
+template <typename T, int G, int D>
+__device__ __forceinline__ void prev_layer_epilogue(const AttnParams& p, const Work& wk, int tid, float* sM,
+                                                    float* sIZ) {
+  if (!p.has_prev) return;
+  const LayerBufs lb{p.prev_part_o, p.prev_part_m, p.prev_part_z, p.prev_spill, p.prev_out};
+  layer_epilogue<T, G, D, kAttnWarps * 32>(p, lb, wk, tid, sM, sIZ, [] { consumer_sync(); });
+}
+
 // ===================================================================== MMA
 // Widens an 8-bit page (codes at stage + 0: K block then V block, unswizzled)
-// into bf16 K and V blocks in the swizzled layout, in place.
+// into bf16 K and V blocks in the swizzled layout, in place. The V codes are
+// widened first (their bf16 block lies past the codes), then the K codes, each
+// block read whole into registers before it is written.
 template <int D>
-__device__ __forceinline__ void widen_i8_page(char* stage, int lane) {
+__device__ __forceinline__ void widen_i8_block(char* stage, int kv, int lane) {
   constexpr int ROWB = D * 2;
-  constexpr int CODE_VECS = 2 * kPage * D / 16;  // uint4 of codes in the page-head record
-  constexpr int PER_LANE = CODE_VECS / 32;
+  constexpr int PER_BLOCK = kPage * D / 16;  // uint4 of codes in one block
+  constexpr int PER_LANE = PER_BLOCK / 32;
   uint4 v[PER_LANE];
 #pragma unroll
-  for (int i = 0; i < PER_LANE; ++i) v[i] = reinterpret_cast<const uint4*>(stage)[lane + 32 * i];
+  for (int i = 0; i < PER_LANE; ++i) v[i] = reinterpret_cast<const uint4*>(stage + kv * kPage * D)[lane + 32 * i];
   __syncwarp();
 #pragma unroll
   for (int i = 0; i < PER_LANE; ++i) {
-    const int vec = lane + 32 * i;                 // 16 codes: block kv, row r, columns [16c, 16c + 16)
-    const int per_block = kPage * D / 16;
-    const int kv = vec / per_block;
-    const int rem = vec % per_block;
-    const int r = rem / (D / 16), c = rem % (D / 16);
+    const int vec = lane + 32 * i;                 // 16 codes: row r, columns [16c, 16c + 16)
+    const int r = vec / (D / 16), c = vec % (D / 16);
     const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
     uint4 lo, hi;
     lo.x = pack_bf16(i8f(w[0], 0), i8f(w[0], 1));
@@ -493,6 +533,12 @@ __device__ __forceinline__ void widen_i8_page(char* stage, int lane) {
   __syncwarp();
 }
 
+template <int D>
+__device__ __forceinline__ void widen_i8_page(char* stage, int lane) {
+  widen_i8_block<D>(stage, 1, lane);  // V codes [16 D, 32 D) -> bf16 V block [32 D, 64 D)
+  widen_i8_block<D>(stage, 0, lane);  // K codes [0, 16 D)     -> bf16 K block [0, 32 D)
+}
+
 template <int G, int D>
 __global__ void __launch_bounds__((kAttnWarps + 1) * 32, 3)
     attn_split_mma_kernel(const __grid_constant__ AttnParams p) {
@@ -503,6 +549,7 @@ __global__ void __launch_bounds__((kAttnWarps + 1) * 32, 3)
   static_assert(G >= 2 && G <= 8, "tensor-core path serves 2..8 query heads per KV head");
   extern __shared__ __align__(128) char smem[];
   __shared__ volatile int s_abort;
+  __shared__ float s_epM[8], s_epIZ[8];  // previous layer's (M, 1 / Z) per head
 
   const int tid = threadIdx.x;
   const int w = tid >> 5, lane = tid & 31;
@@ -521,6 +568,8 @@ __global__ void __launch_bounds__((kAttnWarps + 1) * 32, 3)
   int issued = 0;
   if (!consumer)
     issued = produce<S>(p, wk, pg, pmask, reinterpret_cast<PageCopy*>(smem + L::off_desc), ring, full0, empty0, &s_abort);
+
+  if (consumer) prev_layer_epilogue<T, G, D>(p, wk, tid, s_epM, s_epIZ);
 
   // Q fragments (A operand, heads as rows; rows 8..15 of the tile are zero)
   uint32_t qa[KS][2];
@@ -556,11 +605,10 @@ __global__ void __launch_bounds__((kAttnWarps + 1) * 32, 3)
     }
     char* stage = ring + st * S::STAGE;
     const int k = wk.k0 + i;
-    const int src = pg[i] >> 28;
-    const uint32_t mask = pmask[i];
-    const PageSource& ps = p.src[src];
-    const bool i8 = ps.kind == SRC_INT8;
-    const int swz = i8 ? kSwizzle : ps.swz;
+    const uint32_t flags = pmask[i];
+    const uint32_t mask = flags & 0xffffu;
+    const bool i8 = (flags & kFlagI8) != 0;
+    const int swz = i8 ? kSwizzle : static_cast<int>((flags >> kFlagSwzShift) & 7u);
     if (i8) widen_i8_page<D>(stage, lane);
     const uint32_t kbase = smem_u32(stage), vbase = kbase + S::BLK;
 
@@ -582,7 +630,7 @@ __global__ void __launch_bounds__((kAttnWarps + 1) * 32, 3)
     float l[4] = {s0[0] + s2[0], s0[1] + s2[1], s1[0] + s3[0], s1[1] + s3[1]};
     const int rows[4] = {2 * t, 2 * t + 1, 8 + 2 * t, 9 + 2 * t};
     const char* sc = stage + 2 * S::BLK;
-    const bool per_head = ps.scale_per_head != 0;
+    const bool per_head = (flags & kFlagPerHead) != 0;
     float pmax = -INFINITY;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
@@ -785,6 +833,7 @@ __global__ void __launch_bounds__((kAttnWarps + 1) * 32)
   using L = Smem<T, G, D, true>;
   extern __shared__ __align__(128) char smem[];
   __shared__ volatile int s_abort;
+  __shared__ float s_epM[8], s_epIZ[8];  // previous layer's (M, 1 / Z) per head
 
   const int tid = threadIdx.x;
   const int w = tid >> 5, lane = tid & 31;
@@ -823,6 +872,7 @@ __global__ void __launch_bounds__((kAttnWarps + 1) * 32)
     }
   }
   if (consumer) consumer_sync();
+  if (consumer) prev_layer_epilogue<T, G, D>(p, wk, tid, s_epM, s_epIZ);
 
   float m_run = -INFINITY, z_run = 0.f;  // for the head this lane owns
   float2 acc[G][S::VPL];
@@ -847,11 +897,11 @@ __global__ void __launch_bounds__((kAttnWarps + 1) * 32)
     }
     const char* stage = ring + st * S::STAGE;
     const int k = wk.k0 + i;
-    const int src = pg[i] >> 28;
-    const uint32_t mask = pmask[i];
-    const bool i8 = p.src[src].kind == SRC_INT8;
-    const bool per_head = p.src[src].scale_per_head != 0;
-    const int swz = p.src[src].swz;
+    const uint32_t flags = pmask[i];
+    const uint32_t mask = flags & 0xffffu;
+    const bool i8 = (flags & kFlagI8) != 0;
+    const bool per_head = (flags & kFlagPerHead) != 0;
+    const int swz = static_cast<int>((flags >> kFlagSwzShift) & 7u);
 
     // ---- QK: 4 rows per lane, QE elements each, all heads -----------------
     float part[S::NV];

@@ -130,98 +130,157 @@ __global__ void prefill_kernel(const __grid_constant__ PrefillParams p) {
 }
 
 // ---------------------------------------------------------------- movers
-// One block per (mover, layer); warp 0 moves the K row, warp 1 the V row.
-// The row (all KV heads) is staged in shared memory as float32.
-__global__ void move_kernel(const __grid_constant__ MoveParams p, const Mover* __restrict__ movers) {
-  extern __shared__ float row_s[];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+// One block per (mover, layer) moves the token's K and V rows of every KV head.
+// Full-precision rows move as 16-byte chunks: the swizzle only permutes the
+// chunks of a row, so a chunk keeps its place in the row's logical order and
+// is read and written whole (T1 and T2 pools are host memory reached over the
+// host link, where wide accesses matter most). Rows that leave T2 are
+// dequantised chunk by chunk; rows that enter T2 pass through shared memory as
+// float32 for the absmax of their scale group.
+constexpr int kMoveThreads = 128;
+
+// Full-precision chunk c of row hk (= head * 2 + kv) of a location: a pool slot
+// (tier 0 or 1), or a staging row of `temp` (plain layout [rows][L][2][Hkv][D]).
+__device__ __forceinline__ char* full_chunk(const MoveParams& p, int tier, int loc, int temp_row, int l,
+                                           int hk, int c, int64_t row_bytes) {
+  if (tier < 0) {
+    const int h = hk >> 1, kv = hk & 1;
+    return p.temp + (((static_cast<int64_t>(temp_row) * p.L + l) * 2 + kv) * p.Hkv + h) * row_bytes + c * 16;
+  }
+  const int page = loc >> 4, slot = loc & 15;
+  const TierPools& P = p.pools;
+  char* pg = P.base[tier] + l * P.layer_bytes[tier] + static_cast<int64_t>(page) * P.page_bytes[tier];
+  return pg + (static_cast<int64_t>(hk) * kPage + slot) * row_bytes + ((c ^ (slot & kSwizzle)) << 4);
+}
+
+__device__ __forceinline__ float t2_scale_of(const TierPools& P, const char* sc, int hk, int slot) {
+  const int kv = hk & 1;
+  if (P.scale_per_head) {
+    if (P.scale_f16) return __half2float(reinterpret_cast<const __half*>(sc)[hk * kPage + slot]);
+    return reinterpret_cast<const float*>(sc)[hk * kPage + slot];
+  }
+  return reinterpret_cast<const float*>(sc)[kv * kPage + slot];
+}
+
+__global__ void __launch_bounds__(kMoveThreads) move_kernel(const __grid_constant__ MoveParams p,
+                                                            const Mover* __restrict__ movers) {
+  extern __shared__ float row_s[];  // [2][Hkv][D] float32 (rows entering T2)
   const Mover mv = movers[blockIdx.x];
   const int l = blockIdx.y;
-  const int kv = warp;
-  const int HD = p.Hkv * p.D;
-  float* row = row_s + kv * HD;
+  const int tid = threadIdx.x;
   const int esz = p.kv_dtype == 1 ? 2 : 4;
-  const TierPools& P = p.pools;
   const int64_t row_bytes = static_cast<int64_t>(p.D) * esz;
+  const int cpr = static_cast<int>(row_bytes / 16);  // 16-byte chunks per full-precision row
+  const int epc = 16 / esz;                          // elements per chunk
+  const int nchunk = 2 * p.Hkv * cpr;
+  const TierPools& P = p.pools;
+  const int st = p.mode == MOVE_SCATTER ? -1 : mv.src_tier;  // -1: the staging rows
+  const int dt = p.mode == MOVE_GATHER ? -1 : mv.dst_tier;
 
-  // ---- read
-  if (p.mode == MOVE_SCATTER) {
-    const char* src = p.temp + ((static_cast<int64_t>(mv.temp_row) * p.L + l) * 2 + kv) * HD * esz;
-    for (int i = lane; i < HD; i += 32) row[i] = load_elem(src + static_cast<int64_t>(i) * esz, p.kv_dtype);
-  } else {
-    const int t = mv.src_tier, page = mv.src_loc >> 4, slot = mv.src_loc & 15;
-    if (t == 0 || t == 1) {
-      const char* pg = P.base[t] + l * P.layer_bytes[t] + static_cast<int64_t>(page) * P.page_bytes[t];
-      for (int i = lane; i < HD; i += 32) {
-        const int h = i / p.D, e = i % p.D;
-        const char* src = pg + ((static_cast<int64_t>(h) * 2 + kv) * kPage + slot) * row_bytes +
-                          swz_offset(slot, static_cast<int64_t>(e) * esz, kSwizzle);
-        row[i] = load_elem(src, p.kv_dtype);
+  if (st != 2 && dt != 2) {  // full precision -> full precision
+    for (int j = tid; j < nchunk; j += kMoveThreads) {
+      const int hk = j / cpr, c = j % cpr;
+      const uint4 v = *reinterpret_cast<const uint4*>(full_chunk(p, st, mv.src_loc, mv.temp_row, l, hk, c, row_bytes));
+      *reinterpret_cast<uint4*>(full_chunk(p, dt, mv.dst_loc, mv.temp_row, l, hk, c, row_bytes)) = v;
+    }
+    return;
+  }
+
+  if (st == 2) {  // leaving T2: dequantise to the destination's storage, chunk by chunk
+    const int page = mv.src_loc >> 4, slot = mv.src_loc & 15;
+    const char* pg = P.base[2] + l * P.layer_bytes[2] + static_cast<int64_t>(page) * P.page_bytes[2];
+    const char* sc = P.t2_scales + l * P.t2_scale_layer_bytes + static_cast<int64_t>(page) * P.t2_scale_page_bytes;
+    for (int j = tid; j < nchunk; j += kMoveThreads) {
+      const int hk = j / cpr, c = j % cpr;
+      const float scale = t2_scale_of(P, sc, hk, slot);
+      const int8_t* codes = reinterpret_cast<const int8_t*>(pg + (static_cast<int64_t>(hk) * kPage + slot) * p.D + c * epc);
+      uint4 out;
+      if (esz == 2) {
+        const uint2 w = *reinterpret_cast<const uint2*>(codes);
+        uint32_t r[4];
+        const uint32_t words[2] = {w.x, w.y};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint32_t word = words[q >> 1];
+          const int b0 = 2 * (q & 1);
+          const float x0 = __fmul_rn(static_cast<float>(static_cast<int8_t>((word >> (8 * b0)) & 0xffu)), scale);
+          const float x1 = __fmul_rn(static_cast<float>(static_cast<int8_t>((word >> (8 * b0 + 8)) & 0xffu)), scale);
+          const __nv_bfloat162 v2 = __floats2bfloat162_rn(x0, x1);
+          r[q] = *reinterpret_cast<const uint32_t*>(&v2);
+        }
+        out = make_uint4(r[0], r[1], r[2], r[3]);
+      } else {
+        const uint32_t word = *reinterpret_cast<const uint32_t*>(codes);
+        float f[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          f[q] = __fmul_rn(static_cast<float>(static_cast<int8_t>((word >> (8 * q)) & 0xffu)), scale);
+        out = make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]), __float_as_uint(f[3]));
+      }
+      *reinterpret_cast<uint4*>(full_chunk(p, dt, mv.dst_loc, mv.temp_row, l, hk, c, row_bytes)) = out;
+    }
+    return;
+  }
+
+  // entering T2: stage the rows as float32, one scale per group, 16 codes per store
+  const int HD = p.Hkv * p.D;
+  for (int j = tid; j < nchunk; j += kMoveThreads) {
+    const int hk = j / cpr, c = j % cpr;
+    const int h = hk >> 1, kv = hk & 1;
+    const uint4 v = *reinterpret_cast<const uint4*>(full_chunk(p, st, mv.src_loc, mv.temp_row, l, hk, c, row_bytes));
+    float* dst = row_s + kv * HD + h * p.D + c * epc;
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    if (esz == 2) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        dst[2 * q] = __uint_as_float(w[q] << 16);
+        dst[2 * q + 1] = __uint_as_float(w[q] & 0xffff0000u);
       }
     } else {
-      const char* pg = P.base[2] + l * P.layer_bytes[2] + static_cast<int64_t>(page) * P.page_bytes[2];
-      const char* sc = P.t2_scales + l * P.t2_scale_layer_bytes + static_cast<int64_t>(page) * P.t2_scale_page_bytes;
-      for (int i = lane; i < HD; i += 32) {
-        const int h = i / p.D, e = i % p.D;
-        const int8_t code = *reinterpret_cast<const int8_t*>(pg + ((static_cast<int64_t>(h) * 2 + kv) * kPage + slot) * p.D + e);
-        float scale;
-        if (P.scale_per_head)
-          scale = __half2float(reinterpret_cast<const __half*>(sc)[(h * 2 + kv) * kPage + slot]);
-        else
-          scale = reinterpret_cast<const float*>(sc)[kv * kPage + slot];
-        row[i] = storage_round(__fmul_rn(static_cast<float>(code), scale), p.kv_dtype);
-      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) dst[q] = __uint_as_float(w[q]);
     }
   }
-  __syncwarp();
-
-  // ---- write
-  if (p.mode == MOVE_GATHER) {
-    char* dst = p.temp + ((static_cast<int64_t>(mv.temp_row) * p.L + l) * 2 + kv) * HD * esz;
-    for (int i = lane; i < HD; i += 32) store_elem(dst + static_cast<int64_t>(i) * esz, row[i], p.kv_dtype);
-    return;
-  }
-  const int t = mv.dst_tier, page = mv.dst_loc >> 4, slot = mv.dst_loc & 15;
-  if (t == 0 || t == 1) {
-    char* pg = P.base[t] + l * P.layer_bytes[t] + static_cast<int64_t>(page) * P.page_bytes[t];
-    for (int i = lane; i < HD; i += 32) {
-      const int h = i / p.D, e = i % p.D;
-      char* dst = pg + ((static_cast<int64_t>(h) * 2 + kv) * kPage + slot) * row_bytes +
-                  swz_offset(slot, static_cast<int64_t>(e) * esz, kSwizzle);
-      store_elem(dst, row[i], p.kv_dtype);
-    }
-    return;
-  }
-  // into T2: 8-bit codes and scales
+  __syncthreads();
+  const int warp = tid >> 5, lane = tid & 31;
+  const int page = mv.dst_loc >> 4, slot = mv.dst_loc & 15;
   char* pg = P.base[2] + l * P.layer_bytes[2] + static_cast<int64_t>(page) * P.page_bytes[2];
   char* sc = P.t2_scales + l * P.t2_scale_layer_bytes + static_cast<int64_t>(page) * P.t2_scale_page_bytes;
-  if (!P.scale_per_head) {
+  // scale groups: per token, one per K / V over all heads; per token and head, one per (head, K / V)
+  const int ngroups = P.scale_per_head ? 2 * p.Hkv : 2;
+  const int glen = P.scale_per_head ? p.D : HD;
+  for (int gi = warp; gi < ngroups; gi += kMoveThreads / 32) {
+    const int kv = P.scale_per_head ? (gi & 1) : gi;
+    const int h0 = P.scale_per_head ? (gi >> 1) : 0;
+    const float* x = row_s + kv * HD + h0 * p.D;
     float amax = 0.f;
-    for (int i = lane; i < HD; i += 32) amax = fmaxf(amax, fabsf(row[i]));
+    for (int i = lane; i < glen; i += 32) amax = fmaxf(amax, fabsf(x[i]));
     amax = warp_max(amax);
     __half h16;
-    const float div = quant_scale(amax, 0, &h16);
-    for (int i = lane; i < HD; i += 32) {
-      const int h = i / p.D, e = i % p.D;
-      *reinterpret_cast<int8_t*>(pg + ((static_cast<int64_t>(h) * 2 + kv) * kPage + slot) * p.D + e) =
-          quant_code(row[i], div);
+    const float div = quant_scale(amax, P.scale_f16, &h16);
+    for (int v = lane; v < glen / 16; v += 32) {  // 16 consecutive codes of one head row
+      const int i0 = v * 16;
+      const int h = h0 + i0 / p.D, e0 = i0 % p.D;
+      uint32_t w[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        uint32_t word = 0;
+#pragma unroll
+        for (int bb = 0; bb < 4; ++bb)
+          word |= (static_cast<uint32_t>(static_cast<uint8_t>(quant_code(x[i0 + 4 * q + bb], div)))) << (8 * bb);
+        w[q] = word;
+      }
+      *reinterpret_cast<uint4*>(pg + ((static_cast<int64_t>(h) * 2 + kv) * kPage + slot) * p.D + e0) =
+          make_uint4(w[0], w[1], w[2], w[3]);
     }
-    if (lane == 0) reinterpret_cast<float*>(sc)[kv * kPage + slot] = div;
-  } else {
-    for (int h = 0; h < p.Hkv; ++h) {
-      float amax = 0.f;
-      for (int e = lane; e < p.D; e += 32) amax = fmaxf(amax, fabsf(row[h * p.D + e]));
-      amax = warp_max(amax);
-      __half h16;
-      const float div = quant_scale(amax, P.scale_f16, &h16);
-      for (int e = lane; e < p.D; e += 32)
-        *reinterpret_cast<int8_t*>(pg + ((static_cast<int64_t>(h) * 2 + kv) * kPage + slot) * p.D + e) =
-            quant_code(row[h * p.D + e], div);
-      if (lane == 0) {
+    if (lane == 0) {
+      if (P.scale_per_head) {
         if (P.scale_f16)
-          reinterpret_cast<__half*>(sc)[(h * 2 + kv) * kPage + slot] = h16;
+          reinterpret_cast<__half*>(sc)[(h0 * 2 + kv) * kPage + slot] = h16;
         else
-          reinterpret_cast<float*>(sc)[(h * 2 + kv) * kPage + slot] = div;
+          reinterpret_cast<float*>(sc)[(h0 * 2 + kv) * kPage + slot] = div;
+      } else {
+        reinterpret_cast<float*>(sc)[kv * kPage + slot] = div;
       }
     }
   }
@@ -307,7 +366,7 @@ cudaError_t launch_move(const MoveParams& p, const Mover* movers, int64_t count,
     configured = true;
   }
   if (smem > 96 * 1024) return cudaErrorInvalidValue;
-  move_kernel<<<dim3(static_cast<unsigned>(count), p.L), 64, smem, s>>>(p, movers);
+  move_kernel<<<dim3(static_cast<unsigned>(count), p.L), kMoveThreads, smem, s>>>(p, movers);
   return cudaGetLastError();
 }
 

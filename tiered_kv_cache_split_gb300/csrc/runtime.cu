@@ -153,10 +153,12 @@ Layout make_layout(const tkv_config& c) {
   y.o_tier_new = take(size_t(y.maxb) * y.maxtok);
   y.o_s = take(size_t(y.maxb) * y.maxtok * 8);
   y.o_acc = take(size_t(y.maxb) * y.Hkv * 3 * y.maxp * kPage * 4);   // slot-indexed score increments
-  y.o_part_o = take(size_t(y.max_chunks) * y.Hkv * y.G * y.D * 4);
-  y.o_part_m = take(size_t(y.max_chunks) * y.Hkv * y.G * 4);
-  y.o_part_z = take(size_t(y.max_chunks) * y.Hkv * y.G * 4);
-  y.o_spill = take(size_t(y.maxb) * y.Hkv * y.spill_stride * 4);
+  // partials and spilled logits: two layers' worth, since each layer's epilogue
+  // runs inside the next layer's attention launch
+  y.o_part_o = take(2 * size_t(y.max_chunks) * y.Hkv * y.G * y.D * 4);
+  y.o_part_m = take(2 * size_t(y.max_chunks) * y.Hkv * y.G * 4);
+  y.o_part_z = take(2 * size_t(y.max_chunks) * y.Hkv * y.G * 4);
+  y.o_spill = take(2 * size_t(y.maxb) * y.Hkv * y.spill_stride * 4);
   y.o_keys = take(size_t(y.maxb) * y.maxtok * 8);
   y.o_err = take(64);
   y.o_movers = take(2 * size_t(y.maxb) * y.maxtok * sizeof(Mover));
@@ -612,10 +614,14 @@ tkv_status decode_step_device(tkv_ctx* h, const void* q, const void* k_new, cons
   p.q_stride_b = int64_t(y.L) * y.Hq * y.D;
   p.out_stride_b = int64_t(y.L) * y.Hq * y.D;
   p.qscale = static_cast<float>(1.4426950408889634 / std::sqrt(double(y.D)));
-  p.part_o = reinterpret_cast<float*>(h->D(y.o_part_o));
-  p.part_m = reinterpret_cast<float*>(h->D(y.o_part_m));
-  p.part_z = reinterpret_cast<float*>(h->D(y.o_part_z));
-  p.spill = reinterpret_cast<float*>(h->D(y.o_spill));
+  // two buffers of partials and spilled logits, by layer parity
+  const size_t part_o_n = size_t(y.max_chunks) * y.Hkv * y.G * y.D;
+  const size_t part_mz_n = size_t(y.max_chunks) * y.Hkv * y.G;
+  const size_t spill_n = size_t(y.maxb) * y.Hkv * y.spill_stride;
+  float* part_o = reinterpret_cast<float*>(h->D(y.o_part_o));
+  float* part_m = reinterpret_cast<float*>(h->D(y.o_part_m));
+  float* part_z = reinterpret_cast<float*>(h->D(y.o_part_z));
+  float* spill = reinterpret_cast<float*>(h->D(y.o_spill));
   p.spill_stride = y.spill_stride;
   p.acc = reinterpret_cast<float*>(h->D(y.o_acc));
   p.acc_stride_h = 3 * y.maxp * kPage;
@@ -624,6 +630,9 @@ tkv_status decode_step_device(tkv_ctx* h, const void* q, const void* k_new, cons
   const bool timing = h->cfg.flags & TKV_FLAG_TIMING;
   const int64_t abytes = attn_bytes_per_layer(h);
 
+  // Layer l's attention launch first finishes layer l - 1 (its output merge and
+  // score epilogue) in its consumer warps; the last layer's epilogue is a
+  // launch of its own after the loop.
   for (int l = 0; l < y.L; ++l) {
     const int slot = h->slot_rr;
     h->slot_rr ^= 1;
@@ -631,29 +640,45 @@ tkv_status decode_step_device(tkv_ctx* h, const void* q, const void* k_new, cons
     if (st) return st;
     if (h->xs != h->cs) CK(h, cudaStreamWaitEvent(h->cs, h->ev_ready[slot], 0));
     fill_sources(h, l, slot, p);
+    const int par = l & 1;
+    p.has_prev = l > 0;
+    p.prev_part_o = p.part_o;
+    p.prev_part_m = p.part_m;
+    p.prev_part_z = p.part_z;
+    p.prev_spill = p.spill;
+    p.prev_out = p.out;
+    p.part_o = part_o + par * part_o_n;
+    p.part_m = part_m + par * part_mz_n;
+    p.part_z = part_z + par * part_mz_n;
+    p.spill = spill + par * spill_n;
     p.q = static_cast<const char*>(q) + size_t(l) * y.Hq * y.D * y.esz;
     p.out = static_cast<char*>(out) + size_t(l) * y.Hq * y.D * y.esz;
-    TimedPair tp{}, tc{};
+    TimedPair tp{};
     if (timing) {
       st = timed_pair(h, 0, &tp);
-      if (!st) st = timed_pair(h, 2, &tc);
       if (st) return st;
       CK(h, cudaEventRecord(tp.a, h->cs));
     }
     LK(h, launch_attention_part(p, h->cfg.kv_dtype, total_chunks, h->cs, 0), total_chunks > 0);
     if (timing) {
       CK(h, cudaEventRecord(tp.b, h->cs));
+      h->pending.push_back(tp);
+    }
+    CK(h, cudaEventRecord(h->ev_free[slot], h->cs));
+    h->stats.attn_launches += 1;
+    h->stats.attn_bytes += abytes;
+  }
+  {
+    TimedPair tc{};
+    if (timing) {
+      if (tkv_status st = timed_pair(h, 2, &tc)) return st;
       CK(h, cudaEventRecord(tc.a, h->cs));
     }
     LK(h, launch_attention_part(p, h->cfg.kv_dtype, total_chunks, h->cs, 1), total_chunks > 0);
     if (timing) {
       CK(h, cudaEventRecord(tc.b, h->cs));
-      h->pending.push_back(tp);
       h->pending.push_back(tc);
     }
-    CK(h, cudaEventRecord(h->ev_free[slot], h->cs));
-    h->stats.attn_launches += 1;
-    h->stats.attn_bytes += abytes;
   }
 
   // ---- fold this step's score increments into s (float64)
@@ -692,6 +717,9 @@ tkv_status do_reclassify(tkv_ctx* h) {
   const Layout& y = h->y;
   const int B = static_cast<int>(h->seqs.size());
   if (B == 0) return fail(h, TKV_ERR_STATE, "no sequence to reclassify");
+  // the reassignment reads the scores of every step enqueued so far: drain them
+  // first (this also keeps queued decode work out of the reassignment's time)
+  if (tkv_status st0 = sync_all(h)) return st0;
   const auto t_start = std::chrono::steady_clock::now();
 
   // ---- classifier kernel: new tiers on the device

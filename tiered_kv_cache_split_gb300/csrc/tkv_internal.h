@@ -77,6 +77,14 @@ struct AttnParams {
   float* acc;             // score accumulator at [b * acc_stride_b + kvh * acc_stride_h + 16 k + row] (may be null)
   int64_t acc_stride_b, acc_stride_h;
   int32_t* err;
+  // The previous layer of the same step (same chunk plan), whose output merge
+  // and score epilogue this launch's consumer warps run first (has_prev != 0).
+  int32_t has_prev;
+  const float* prev_part_o;
+  const float* prev_part_m;
+  const float* prev_part_z;
+  const float* prev_spill;
+  void* prev_out;
 };
 
 // attention.cu
