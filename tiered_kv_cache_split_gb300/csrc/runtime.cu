@@ -93,7 +93,7 @@ std::string validate(const tkv_config& c) {
     return bad("unsupported (Hq/Hkv, head_dim): group size must be 1, 2, 4, 7 or 8 and head_dim 64 or 128");
   if (c.kv_dtype != TKV_DTYPE_F32 && c.kv_dtype != TKV_DTYPE_BF16) return bad("kv_dtype");
   if (c.max_batch < 1 || c.max_batch > kMaxBatch) return bad("max_batch must be 1..64");
-  if (c.max_tokens < 1 || c.max_tokens > int64_t(kMaxChunksPerSeq) * kMaxChunkPages * kPage - 4 * kPage)
+  if (c.max_tokens < 1 || c.max_tokens > int64_t(kMaxSeqPages) * kPage - 4 * kPage)
     return bad("max_tokens out of range (1 .. 262080)");
   if (c.page_size != kPage) return bad("page_size must be 16");
   if (c.n_sink < 0 || c.recent_window < 0) return bad("n_sink / recent_window negative");
@@ -160,7 +160,7 @@ Layout make_layout(const tkv_config& c) {
   y.o_part_z = take(2 * size_t(y.max_chunks) * y.Hkv * y.G * 4);
   y.o_spill = take(2 * size_t(y.maxb) * y.Hkv * y.spill_stride * 4);
   y.o_keys = take(size_t(y.maxb) * y.maxtok * 8);
-  y.o_err = take(64);
+  y.o_err = take(64);   // int32 [0]: device error word; [4], [5]: epilogue work counters by layer parity
   y.o_movers = take(2 * size_t(y.maxb) * y.maxtok * sizeof(Mover));
   y.o_temp = take(size_t(y.temp_rows) * y.L * 2 * y.Hkv * y.D * y.esz);
   y.o_locs = take(size_t(y.maxtok) * 4);
@@ -442,46 +442,51 @@ int32_t* d_table(tkv_ctx* h, int t) {
 }
 
 // Splits every sequence's page list into chunks, one attention CTA per
-// (chunk, KV head): the chunk counts are apportioned to the page counts so
-// that the grid fills whole waves of resident CTAs (the last wave would
-// otherwise run nearly empty) and chunks of all sequences hold about the same
-// number of pages. Writes chunk_first[0..B] and returns the page bound.
-int plan_chunks(const std::vector<int64_t>& ntot, int Hkv, int split_pages, int resident_ctas,
-                int32_t* chunk_first) {
+// (chunk, KV head). Chunks are balanced by cost (page_at_cost): the kernel
+// splits each sequence into equal-cost chunks, and the number of chunks per
+// sequence is chosen greedily to minimise the costliest chunk, so that the
+// grid's last CTAs finish close to the typical one; the total fills whole
+// waves of resident CTAs. Writes chunk_first[0..B] and returns the page bound.
+int plan_chunks(const std::vector<int64_t>& ntot, const std::vector<int64_t>& cost, int Hkv, int split_pages,
+                int resident_ctas, int32_t* chunk_first) {
   const int B = static_cast<int>(ntot.size());
-  std::vector<int64_t> nch(B, 1);
+  std::vector<int64_t> nch(B, 1), cap(B, 1);
   int64_t sum = 0;
   for (int64_t n : ntot) sum += n;
+  for (int b = 0; b < B; ++b) {
+    // at most kMaxChunkPages pages per chunk, at least ~8 pages per chunk
+    const int64_t floor_b = std::max<int64_t>(1, ceil_div(cost[b], kMaxChunkCost));
+    nch[b] = floor_b;
+    cap[b] = std::max<int64_t>(floor_b, std::min<int64_t>(kMaxChunksPerSeq, std::max<int64_t>(ceil_div(ntot[b], 8), 1)));
+  }
   if (split_pages > 0) {
-    for (int b = 0; b < B; ++b) nch[b] = std::max<int64_t>(1, ceil_div(ntot[b], split_pages));
+    for (int b = 0; b < B; ++b)
+      nch[b] = std::min(cap[b], std::max(nch[b], ceil_div(std::max<int64_t>(ntot[b], 1), split_pages)));
   } else {
     // waves of resident CTAs, about 16 pages or more per chunk
     int64_t waves = std::max<int64_t>(1, (sum * Hkv) / (int64_t(resident_ctas) * 48));
     waves = std::min<int64_t>(waves, 8);
     const int64_t target = std::max<int64_t>(B, waves * resident_ctas / Hkv);
-    // largest-remainder apportionment of `target` chunks to the page counts
     int64_t given = 0;
-    std::vector<std::pair<double, int>> rem(B);
-    for (int b = 0; b < B; ++b) {
-      const double share = double(ntot[b]) * double(target) / double(std::max<int64_t>(sum, 1));
-      nch[b] = std::max<int64_t>(1, int64_t(share));
-      given += nch[b];
-      rem[b] = {share - std::floor(share), b};
-    }
-    std::sort(rem.begin(), rem.end(), [](const auto& x, const auto& y) { return x.first > y.first; });
-    for (int i = 0; given < target && i < B; ++i, ++given) nch[rem[i].second] += 1;
-    for (int b = 0; b < B; ++b) {
-      nch[b] = std::min<int64_t>(nch[b], std::max<int64_t>(ceil_div(ntot[b], 8), 1));  // >= ~8 pages each
-      nch[b] = std::max<int64_t>(nch[b], ceil_div(ntot[b], kMaxChunkPages));
+    for (int b = 0; b < B; ++b) given += nch[b];
+    // greedy min-max: the next chunk goes to the sequence whose chunks are costliest
+    auto worse = [&](int x, int y) { return cost[x] * nch[y] < cost[y] * nch[x]; };
+    std::priority_queue<int, std::vector<int>, decltype(worse)> heap(worse);
+    for (int b = 0; b < B; ++b)
+      if (nch[b] < cap[b]) heap.push(b);
+    while (given < target && !heap.empty()) {
+      const int b = heap.top();
+      heap.pop();
+      ++nch[b];
+      ++given;
+      if (nch[b] < cap[b]) heap.push(b);
     }
   }
-  for (int b = 0; b < B; ++b)  // the combine kernel merges at most kMaxChunksPerSeq chunks
-    nch[b] = std::max<int64_t>(std::min<int64_t>(nch[b], kMaxChunksPerSeq), ceil_div(ntot[b], kMaxChunkPages));
   int bound = 1;
   chunk_first[0] = 0;
   for (int b = 0; b < B; ++b) {
     chunk_first[b + 1] = chunk_first[b] + static_cast<int32_t>(nch[b]);
-    bound = std::max<int>(bound, static_cast<int>(ceil_div(ntot[b], nch[b])));
+    bound = std::max<int>(bound, static_cast<int>(std::min<int64_t>(ntot[b], ceil_div(cost[b], nch[b] * kCostFull) + 1)));
   }
   return bound;
 }
@@ -600,15 +605,16 @@ tkv_status decode_step_device(tkv_ctx* h, const void* q, const void* k_new, cons
   p.B = B; p.Hq = y.Hq; p.Hkv = y.Hkv; p.D = y.D; p.G = y.G;
   p.table_stride = static_cast<int32_t>(y.maxp);
   const bool t2_read = h->cfg.t2_mode == TKV_T2_ATTEND;
-  std::vector<int64_t> ntot(B);
+  std::vector<int64_t> ntot(B), cost(B);
   for (int b = 0; b < B; ++b) {
     const Seq& sq = h->seqs[b];
     p.npages[0][b] = static_cast<int32_t>(sq.pages[0].size());
     p.npages[1][b] = static_cast<int32_t>(sq.pages[1].size());
     p.npages[2][b] = t2_read ? static_cast<int32_t>(sq.pages[2].size()) : 0;
     ntot[b] = p.npages[0][b] + p.npages[1][b] + p.npages[2][b];
+    cost[b] = int64_t(kCostFull) * (p.npages[0][b] + p.npages[1][b]) + int64_t(kCostI8) * p.npages[2][b];
   }
-  p.chunk_pages = plan_chunks(ntot, y.Hkv, h->cfg.split_pages, h->resident_ctas, p.chunk_first);
+  p.chunk_pages = plan_chunks(ntot, cost, y.Hkv, h->cfg.split_pages, h->resident_ctas, p.chunk_first);
   const int total_chunks = p.chunk_first[B];
   if (total_chunks > y.max_chunks) return fail(h, TKV_ERR_INTERNAL, "chunk table overflow");
   p.q_stride_b = int64_t(y.L) * y.Hq * y.D;
@@ -642,6 +648,8 @@ tkv_status decode_step_device(tkv_ctx* h, const void* q, const void* k_new, cons
     fill_sources(h, l, slot, p);
     const int par = l & 1;
     p.has_prev = l > 0;
+    p.ep_next = reinterpret_cast<int32_t*>(h->D(y.o_err)) + 4 + par;   // counters by layer parity
+    p.ep_clear = reinterpret_cast<int32_t*>(h->D(y.o_err)) + 4 + (par ^ 1);
     p.prev_part_o = p.part_o;
     p.prev_part_m = p.part_m;
     p.prev_part_z = p.part_z;
@@ -1295,14 +1303,15 @@ tkv_status tkv_paged_attention(int32_t batch, int32_t n_q_heads, int32_t n_kv_he
   AttnParams p{};
   p.B = batch; p.Hq = n_q_heads; p.Hkv = n_kv_heads; p.D = head_dim; p.G = G;
   p.table_stride = max_pages;
-  std::vector<int64_t> ntot(batch);
-  if (max_pages > kMaxChunksPerSeq * kMaxChunkPages) return fail(nullptr, TKV_ERR_INVALID_ARG, "max_pages above 16384");
+  std::vector<int64_t> ntot(batch), cost(batch);
+  if (max_pages > kMaxSeqPages) return fail(nullptr, TKV_ERR_INVALID_ARG, "max_pages above 16384");
   for (int b = 0; b < batch; ++b) {
     if (page_counts[b] < 1 || page_counts[b] > max_pages) return fail(nullptr, TKV_ERR_INVALID_ARG, "page_counts[%d] out of 1..max_pages", b);
     p.npages[0][b] = page_counts[b];
     ntot[b] = page_counts[b];
+    cost[b] = int64_t(kCostFull) * page_counts[b];
   }
-  p.chunk_pages = plan_chunks(ntot, n_kv_heads, 0, resident_attention_ctas(kv_dtype, G, head_dim), p.chunk_first);
+  p.chunk_pages = plan_chunks(ntot, cost, n_kv_heads, 0, resident_attention_ctas(kv_dtype, G, head_dim), p.chunk_first);
   if (p.chunk_first[batch] > s.max_chunks) return fail(nullptr, TKV_ERR_INTERNAL, "chunk plan exceeds the scratch");
   const int64_t head_full = int64_t(2) * kPage * head_dim * esz;
   p.src[0] = PageSource{static_cast<const char*>(pool), head_full * n_kv_heads, head_full, page_table, slot_mask,

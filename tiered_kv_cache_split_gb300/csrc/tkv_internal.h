@@ -23,8 +23,23 @@ constexpr int kAttnStages = TKV_ATTN_STAGES;  // shared-memory ring of page stag
 // so each warp waits on a stage's mbarrier phases one after another; otherwise
 // a warp would skip phases and a parity wait could match a stale phase.
 static_assert(kAttnStages % kAttnWarps == 0, "ring stages must be a multiple of consumer warps");
-constexpr int kMaxChunkPages = 256;   // pages one attention CTA may take
-constexpr int kMaxChunksPerSeq = 64;  // chunks of one sequence the combine kernel merges
+constexpr int kMaxChunkPages = 256;    // pages one attention CTA may take
+constexpr int kMaxChunksPerSeq = 128;  // chunks one sequence may be split into
+constexpr int kMaxSeqPages = 16384;    // pages of one sequence (all tiers)
+
+// Chunks of a sequence's page list (T0, T1, then T2 pages) are balanced by
+// cost, not page count: an 8-bit T2 page carries half the bytes of a
+// full-precision page but is widened in shared memory first, and measured
+// about twice as long to process. Costs are in half-page units.
+constexpr int kCostFull = 2, kCostI8 = 4;
+// Page index at cost c of a list of n01 full-precision pages followed by 8-bit ones.
+__host__ __device__ inline int page_at_cost(int64_t c, int n01) {
+  const int64_t full = static_cast<int64_t>(kCostFull) * n01;
+  if (c <= full) return static_cast<int>(c / kCostFull);
+  return n01 + static_cast<int>((c - full) / kCostI8);
+}
+// A chunk of cost at most this holds at most kMaxChunkPages pages.
+constexpr int64_t kMaxChunkCost = static_cast<int64_t>(kCostFull) * (kMaxChunkPages - 1);
 
 // Device-side error codes written into the handle's error word.
 enum DevError : int { DEV_OK = 0, DEV_TIMEOUT = 1, DEV_BAD_INDEX = 2 };
@@ -63,7 +78,7 @@ struct AttnParams {
   int32_t table_stride;
   int32_t npages[3][kMaxBatch];
   int32_t chunk_first[kMaxBatch + 1];   // prefix sums of chunks per sequence
-  int32_t chunk_pages;                  // upper bound of pages per chunk (chunks are balanced)
+  int32_t chunk_pages;                  // upper bound of pages per chunk
   const void* q;          // element (b, h, e) at q[b * q_stride_b + h * D + e]
   int64_t q_stride_b;
   void* out;
@@ -78,8 +93,11 @@ struct AttnParams {
   int64_t acc_stride_b, acc_stride_h;
   int32_t* err;
   // The previous layer of the same step (same chunk plan), whose output merge
-  // and score epilogue this launch's consumer warps run first (has_prev != 0).
+  // and score epilogue each CTA of this launch runs after its own pages
+  // (has_prev != 0).
   int32_t has_prev;
+  int32_t* ep_next;       // work counter of the previous layer's epilogue items (zero at launch)
+  int32_t* ep_clear;      // the other layer parity's counter, zeroed by this launch for the next one
   const float* prev_part_o;
   const float* prev_part_m;
   const float* prev_part_z;
