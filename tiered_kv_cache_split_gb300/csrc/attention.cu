@@ -30,8 +30,8 @@
 // partials, the merged output (each chunk's CTA merges a slice), and the exact
 // softmax weights alpha = exp2(l - M) / Z of the chunk's slots summed over the
 // G heads, added to a slot-indexed score accumulator (the fused score
-// epilogue) — runs in the consumer warps of the NEXT layer's attention launch,
-// before their first page, while the producer warp already fills the ring.
+// epilogue) — runs in the NEXT layer's attention launch, in each CTA after its
+// own pages, so CTAs that finish early absorb it while the last ones stream.
 // The last layer's epilogue (or a lone layer's) is attn_combine_kernel.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -203,22 +203,29 @@ struct Work {
   int b, kvh, cf, jc, nch, ntot, k0, npg;
 };
 
-__device__ __forceinline__ Work find_work(const AttnParams& p) {
+__device__ __forceinline__ Work find_work_at(const AttnParams& p, int chunk, int kvh) {
   Work wk;
-  wk.kvh = blockIdx.y;
-  const int chunk = blockIdx.x;
+  wk.kvh = kvh;
   int b = 0;
   while (b + 1 < p.B && p.chunk_first[b + 1] <= chunk) ++b;
   wk.b = b;
   wk.cf = p.chunk_first[b];
   wk.jc = chunk - wk.cf;
   wk.nch = p.chunk_first[b + 1] - wk.cf;
-  wk.ntot = p.npages[0][b] + p.npages[1][b] + p.npages[2][b];
-  // balanced split of the sequence's pages over its chunks (sizes differ by <= 1)
-  wk.k0 = static_cast<int>((static_cast<int64_t>(wk.jc) * wk.ntot) / wk.nch);
-  wk.npg = static_cast<int>((static_cast<int64_t>(wk.jc + 1) * wk.ntot) / wk.nch) - wk.k0;
+  const int n01 = p.npages[0][b] + p.npages[1][b];
+  wk.ntot = n01 + p.npages[2][b];
+  // cost-balanced split of the sequence's pages over its chunks
+  const int64_t cost = static_cast<int64_t>(kCostFull) * n01 + static_cast<int64_t>(kCostI8) * p.npages[2][b];
+  wk.k0 = page_at_cost((wk.jc * cost) / wk.nch, n01);
+  wk.npg = page_at_cost(((wk.jc + 1) * cost) / wk.nch, n01) - wk.k0;
+  if (wk.npg > kMaxChunkPages) {  // the host plan never makes one; refuse rather than overrun shared memory
+    if (threadIdx.x == 0) atomicExch(p.err, DEV_BAD_INDEX);
+    wk.npg = 0;
+  }
   return wk;
 }
+
+__device__ __forceinline__ Work find_work(const AttnParams& p) { return find_work_at(p, blockIdx.x, blockIdx.y); }
 
 // Initialises the ring's full and empty barriers (thread 0); a CTA barrier
 // must follow before any thread uses them.
@@ -275,37 +282,49 @@ __device__ __forceinline__ uint32_t page_flags(uint32_t valid, bool i8, bool per
          (static_cast<uint32_t>(swz & 7) << kFlagSwzShift);
 }
 
-// The producer warp's job: resolve every page of the chunk (one lane per page:
-// source, pool page, valid mask and copy descriptor, published in shared
-// memory), then let lane 0 keep the ring full. Returns the pages issued (lane 0).
+// Resolves page i of the chunk (source, pool page, valid mask and traits, copy
+// descriptor) and publishes it in shared memory.
+__device__ __forceinline__ void resolve_page(const AttnParams& p, const Work& wk, int i, int* pg, uint32_t* pmask,
+                                             PageCopy* desc) {
+  int src, page;
+  page_ref(p, wk.b, wk.k0 + i, src, page);
+  const PageSource& ps = p.src[src];
+  pg[i] = (src << 28) | page;
+  const bool i8 = ps.kind == SRC_INT8;
+  pmask[i] = page_flags(ps.mask[page], i8, ps.scale_per_head != 0, ps.swz);
+  PageCopy c;
+  c.src = reinterpret_cast<unsigned long long>(ps.base + static_cast<int64_t>(page) * ps.page_bytes +
+                                               static_cast<int64_t>(wk.kvh) * ps.head_bytes) |
+          (i8 ? 1ull : 0ull) | ((i8 && ps.scale_per_head) ? 2ull : 0ull);
+  c.scales = i8 ? reinterpret_cast<unsigned long long>(ps.scales + static_cast<int64_t>(page) * ps.scale_page_bytes +
+                                                       (ps.scale_per_head ? static_cast<int64_t>(wk.kvh) * 64 : 0))
+                : 0ull;
+  desc[i] = c;
+}
+
+// The producer warp's job: resolve the chunk's pages (one lane per page) and
+// let lane 0 keep the ring full. The first 32 pages are resolved first and the
+// ring's first stages issued at once; the rest are resolved while those copies
+// are in flight. Returns the pages issued (lane 0).
 template <typename S>
 __device__ int produce(const AttnParams& p, const Work& wk, int* pg, uint32_t* pmask, PageCopy* desc,
                        char* ring, uint32_t full0, uint32_t empty0, volatile int* abort_flag) {
+  static_assert(kAttnStages <= 32, "the first resolved round must cover the ring");
   const int lane = threadIdx.x & 31;
-  for (int i = lane; i < wk.npg; i += 32) {
-    int src, page;
-    page_ref(p, wk.b, wk.k0 + i, src, page);
-    const PageSource& ps = p.src[src];
-    pg[i] = (src << 28) | page;
-    const bool i8 = ps.kind == SRC_INT8;
-    pmask[i] = page_flags(ps.mask[page], i8, ps.scale_per_head != 0, ps.swz);
-    PageCopy c;
-    c.src = reinterpret_cast<unsigned long long>(ps.base + static_cast<int64_t>(page) * ps.page_bytes +
-                                                 static_cast<int64_t>(wk.kvh) * ps.head_bytes) |
-            (i8 ? 1ull : 0ull) | ((i8 && ps.scale_per_head) ? 2ull : 0ull);
-    c.scales = i8 ? reinterpret_cast<unsigned long long>(ps.scales + static_cast<int64_t>(page) * ps.scale_page_bytes +
-                                                         (ps.scale_per_head ? static_cast<int64_t>(wk.kvh) * 64 : 0))
-                  : 0ull;
-    desc[i] = c;
-  }
+  if (lane < wk.npg) resolve_page(p, wk, lane, pg, pmask, desc);
   __syncwarp();
-  int issued = 0;
+  uint64_t policy;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(policy));
+  const int first = wk.npg < kAttnStages ? wk.npg : kAttnStages;
+  if (lane == 0)
+    for (int i = 0; i < first; ++i) issue_page<S>(desc[i], i, ring, full0, policy);
+  for (int i = 32 + lane; i < wk.npg; i += 32) resolve_page(p, wk, i, pg, pmask, desc);
+  __syncwarp();
+  int issued = first;
   if (lane == 0) {
-    uint64_t policy;
-    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(policy));
-    for (int i = 0; i < wk.npg; ++i) {
+    for (int i = first; i < wk.npg; ++i) {
       const int st = i % kAttnStages;
-      if (i >= kAttnStages && !mbar_wait(empty0 + st * 8, ((i / kAttnStages) - 1) & 1)) {
+      if (!mbar_wait(empty0 + st * 8, ((i / kAttnStages) - 1) & 1)) {
         *abort_flag = 1;
         break;
       }
@@ -486,19 +505,47 @@ __global__ void __launch_bounds__(kCombineThreads) attn_combine_kernel(const __g
   layer_epilogue<T, G, D, kCombineThreads>(p, lb, wk, threadIdx.x, sM, sIZ, [] { __syncthreads(); });
 }
 
-// The previous layer's epilogue, run by an attention CTA's consumer warps
-// before they take their first page (the producer warp meanwhile fills the
-// ring): the same (chunk, KV head) split, since every layer of a step has the
-// same chunk plan.
+// The previous layer's epilogue, run by all warps of an attention CTA once its
+// own pages are done and its partial is written: CTAs that finish early do it
+// while the last ones still stream, and it never holds up the ring. Same
+// (chunk, KV head) split, since every layer of a step has the same chunk plan.
+// The items — one per (chunk, KV head) — are handed out by a counter, so CTAs
+// that finish their pages early take most of them and the last CTAs to finish
+// find none left.
 template <typename T, int G, int D>
-__device__ __forceinline__ void prev_layer_epilogue(const AttnParams& p, const Work& wk, int tid, float* sM,
-                                                    float* sIZ) {
+__device__ __forceinline__ void prev_layer_epilogue(const AttnParams& p, int tid, float* sM, float* sIZ,
+                                                    volatile int* s_item) {
   if (!p.has_prev) return;
   const LayerBufs lb{p.prev_part_o, p.prev_part_m, p.prev_part_z, p.prev_spill, p.prev_out};
-  layer_epilogue<T, G, D, kAttnWarps * 32>(p, lb, wk, tid, sM, sIZ, [] { consumer_sync(); });
+  const int items = static_cast<int>(gridDim.x * gridDim.y);
+  for (;;) {
+    __syncthreads();
+    if (tid == 0) *s_item = atomicAdd(p.ep_next, 1);
+    __syncthreads();
+    const int item = *s_item;
+    if (item >= items) break;
+    const Work wk = find_work_at(p, item % static_cast<int>(gridDim.x), item / static_cast<int>(gridDim.x));
+    layer_epilogue<T, G, D, (kAttnWarps + 1) * 32>(p, lb, wk, tid, sM, sIZ, [] { __syncthreads(); });
+  }
 }
 
 // ===================================================================== MMA
+// Four signed 8-bit codes (one word, byte 0 first) as two bf16x2 words, exactly,
+// without conversion instructions: byte b + 128 placed in the low mantissa bits
+// of 2^23 gives the float 2^23 + b + 128; subtracting 2^23 + 128 leaves b; the
+// upper half of that float is its bf16 (|b| <= 128 needs 8 significant bits).
+__device__ __forceinline__ void i8x4_to_bf16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  const uint32_t u = w ^ 0x80808080u;  // b + 128 as unsigned bytes
+  const float2 bias = make_float2(-8388736.f, -8388736.f);
+  const float2 one = make_float2(1.f, 1.f);
+  const float2 a = ffma2(make_float2(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7440)),
+                                     __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7441))), one, bias);
+  const float2 b = ffma2(make_float2(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7442)),
+                                     __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7443))), one, bias);
+  lo = __byte_perm(__float_as_uint(a.x), __float_as_uint(a.y), 0x7632);
+  hi = __byte_perm(__float_as_uint(b.x), __float_as_uint(b.y), 0x7632);
+}
+
 // Widens an 8-bit page (codes at stage + 0: K block then V block, unswizzled)
 // into bf16 K and V blocks in the swizzled layout, in place. The V codes are
 // widened first (their bf16 block lies past the codes), then the K codes, each
@@ -516,16 +563,11 @@ __device__ __forceinline__ void widen_i8_block(char* stage, int kv, int lane) {
   for (int i = 0; i < PER_LANE; ++i) {
     const int vec = lane + 32 * i;                 // 16 codes: row r, columns [16c, 16c + 16)
     const int r = vec / (D / 16), c = vec % (D / 16);
-    const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
     uint4 lo, hi;
-    lo.x = pack_bf16(i8f(w[0], 0), i8f(w[0], 1));
-    lo.y = pack_bf16(i8f(w[0], 2), i8f(w[0], 3));
-    lo.z = pack_bf16(i8f(w[1], 0), i8f(w[1], 1));
-    lo.w = pack_bf16(i8f(w[1], 2), i8f(w[1], 3));
-    hi.x = pack_bf16(i8f(w[2], 0), i8f(w[2], 1));
-    hi.y = pack_bf16(i8f(w[2], 2), i8f(w[2], 3));
-    hi.z = pack_bf16(i8f(w[3], 0), i8f(w[3], 1));
-    hi.w = pack_bf16(i8f(w[3], 2), i8f(w[3], 3));
+    i8x4_to_bf16x4(v[i].x, lo.x, lo.y);
+    i8x4_to_bf16x4(v[i].y, lo.z, lo.w);
+    i8x4_to_bf16x4(v[i].z, hi.x, hi.y);
+    i8x4_to_bf16x4(v[i].w, hi.z, hi.w);
     char* rowp = stage + kv * kPage * ROWB + r * ROWB;
     *reinterpret_cast<uint4*>(rowp + swz_chunk(2 * c, r, kSwizzle) * 16) = lo;
     *reinterpret_cast<uint4*>(rowp + swz_chunk(2 * c + 1, r, kSwizzle) * 16) = hi;
@@ -550,12 +592,14 @@ __global__ void __launch_bounds__((kAttnWarps + 1) * 32, 3)
   extern __shared__ __align__(128) char smem[];
   __shared__ volatile int s_abort;
   __shared__ float s_epM[8], s_epIZ[8];  // previous layer's (M, 1 / Z) per head
+  __shared__ volatile int s_item;
 
   const int tid = threadIdx.x;
   const int w = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, t = lane & 3;  // fragment row group and column pair
   const Work wk = find_work(p);
   if (tid == 0) s_abort = 0;
+  if (tid == 0 && blockIdx.x == 0 && blockIdx.y == 0 && p.ep_clear) *p.ep_clear = 0;
   init_barriers<L>(smem);
   __syncthreads();
 
@@ -568,8 +612,6 @@ __global__ void __launch_bounds__((kAttnWarps + 1) * 32, 3)
   int issued = 0;
   if (!consumer)
     issued = produce<S>(p, wk, pg, pmask, reinterpret_cast<PageCopy*>(smem + L::off_desc), ring, full0, empty0, &s_abort);
-
-  if (consumer) prev_layer_epilogue<T, G, D>(p, wk, tid, s_epM, s_epIZ);
 
   // Q fragments (A operand, heads as rows; rows 8..15 of the tile are zero)
   uint32_t qa[KS][2];
@@ -745,6 +787,7 @@ __global__ void __launch_bounds__((kAttnWarps + 1) * 32, 3)
   }
   __syncthreads();
   write_partial<T, G, D>(p, wk, smem);
+  prev_layer_epilogue<T, G, D>(p, tid, s_epM, s_epIZ, &s_item);
 }
 
 // ===================================================================== FP32
@@ -834,12 +877,14 @@ __global__ void __launch_bounds__((kAttnWarps + 1) * 32)
   extern __shared__ __align__(128) char smem[];
   __shared__ volatile int s_abort;
   __shared__ float s_epM[8], s_epIZ[8];  // previous layer's (M, 1 / Z) per head
+  __shared__ volatile int s_item;
 
   const int tid = threadIdx.x;
   const int w = tid >> 5, lane = tid & 31;
   const int r = lane >> 3, c = lane & 7;
   const Work wk = find_work(p);
   if (tid == 0) s_abort = 0;
+  if (tid == 0 && blockIdx.x == 0 && blockIdx.y == 0 && p.ep_clear) *p.ep_clear = 0;
   init_barriers<L>(smem);
   __syncthreads();
 
@@ -872,7 +917,6 @@ __global__ void __launch_bounds__((kAttnWarps + 1) * 32)
     }
   }
   if (consumer) consumer_sync();
-  if (consumer) prev_layer_epilogue<T, G, D>(p, wk, tid, s_epM, s_epIZ);
 
   float m_run = -INFINITY, z_run = 0.f;  // for the head this lane owns
   float2 acc[G][S::VPL];
@@ -1095,6 +1139,7 @@ __global__ void __launch_bounds__((kAttnWarps + 1) * 32)
   }
   __syncthreads();
   write_partial<T, G, D>(p, wk, smem);
+  prev_layer_epilogue<T, G, D>(p, tid, s_epM, s_epIZ, &s_item);
 }
 
 template <typename K>
