@@ -141,7 +141,7 @@ def test_paged_attention_and_fused_alpha(dtype, G, d):
 
 def test_proposition_1_bitwise_on_the_gpu():
     """Attention over T0 + prefetched T1 gives the same bits as the same pages,
-    in the same order, all resident in HBM (same kernel, same chunking)."""
+    in the same order, all resident in HBM (same kernel, same fixed chunking)."""
     from tiered_kv_cache_split_gb300 import TieredKVCache, paged_attention
     from helpers import prefill_cache
     torch.cuda.set_device(DEV)
@@ -173,3 +173,4 @@ def test_proposition_1_bitwise_on_the_gpu():
     ref = paged_attention(q[0, 0].unsqueeze(0).to(DEV), pool, table, mask_t, [len(rows)])
     assert torch.equal(ref[0].cpu(), out[0, 0].cpu())
     cache.close()
+

@@ -142,6 +142,12 @@ __device__ __forceinline__ float i8f(uint32_t w, int byte) {
 }
 __device__ __forceinline__ int swz_chunk(int chunk, int row, int swz) { return chunk ^ (row & swz); }
 
+// Pages of a CTA pass through ring positions 0, 1, 2, ...; position i uses
+// ring stage i % kAttnStages and consumer warp i % kAttnWarps, and its page
+// index and flags sit at slot i % kMeta (the producer resolves at most 32
+// positions ahead of those still in the ring).
+constexpr int kMeta = 64;
+
 template <typename T, int G, int D>
 struct Shape {
   static constexpr int GP = G <= 1 ? 1 : G <= 2 ? 2 : G <= 4 ? 4 : 8;
@@ -170,8 +176,8 @@ struct Smem {
   static constexpr int QS = FMA ? S::GP * D * 4 : 0;
   static constexpr int PSW = S::GP * kPage + 8;   // floats per warp: p[GP][16], corr[GP]
   static constexpr int PS = FMA ? kAttnWarps * PSW * 4 : 0;
-  static constexpr int PG = kMaxChunkPages * 8;   // page reference + valid mask per page
-  static constexpr int DESC = kMaxChunkPages * 16; // producer's copy descriptors per page
+  static constexpr int PG = kMeta * 8;     // per ring position: page index, flags word
+  static constexpr int DESC = kMeta * 16;  // producer's copy descriptors per ring position
   static constexpr int BARS = 2 * kAttnStages * 8;  // full[stages], empty[stages]
   static constexpr int MERGE = kAttnWarps * (G * D + 2 * S::GP) * 4;
   static constexpr int BODY = ((RING > MERGE ? RING : MERGE) + 127) / 128 * 128;
@@ -200,7 +206,7 @@ __device__ __forceinline__ void page_ref(const AttnParams& p, int b, int k, int&
 
 // What a CTA needs to know about its work item.
 struct Work {
-  int b, kvh, cf, jc, nch, ntot, k0, npg;
+  int b, kvh, cf, jc, nch, ntot, k0, npg;  // the chunk: pages [k0, k0 + npg) of sequence b
 };
 
 __device__ __forceinline__ Work find_work_at(const AttnParams& p, int chunk, int kvh) {
@@ -218,7 +224,7 @@ __device__ __forceinline__ Work find_work_at(const AttnParams& p, int chunk, int
   const int64_t cost = static_cast<int64_t>(kCostFull) * n01 + static_cast<int64_t>(kCostI8) * p.npages[2][b];
   wk.k0 = page_at_cost((wk.jc * cost) / wk.nch, n01);
   wk.npg = page_at_cost(((wk.jc + 1) * cost) / wk.nch, n01) - wk.k0;
-  if (wk.npg > kMaxChunkPages) {  // the host plan never makes one; refuse rather than overrun shared memory
+  if (wk.npg > kMaxChunkPages) {  // the host plan never makes one
     if (threadIdx.x == 0) atomicExch(p.err, DEV_BAD_INDEX);
     wk.npg = 0;
   }
@@ -284,14 +290,14 @@ __device__ __forceinline__ uint32_t page_flags(uint32_t valid, bool i8, bool per
 
 // Resolves page i of the chunk (source, pool page, valid mask and traits, copy
 // descriptor) and publishes it in shared memory.
-__device__ __forceinline__ void resolve_page(const AttnParams& p, const Work& wk, int i, int* pg, uint32_t* pmask,
-                                             PageCopy* desc) {
+__device__ __forceinline__ void resolve_page(const AttnParams& p, const Work& wk, int k, int slot, int32_t* meta_k,
+                                             uint32_t* meta_f, PageCopy* desc) {
   int src, page;
-  page_ref(p, wk.b, wk.k0 + i, src, page);
+  page_ref(p, wk.b, k, src, page);
   const PageSource& ps = p.src[src];
-  pg[i] = (src << 28) | page;
+  meta_k[slot] = k;
   const bool i8 = ps.kind == SRC_INT8;
-  pmask[i] = page_flags(ps.mask[page], i8, ps.scale_per_head != 0, ps.swz);
+  meta_f[slot] = page_flags(ps.mask[page], i8, ps.scale_per_head != 0, ps.swz);
   PageCopy c;
   c.src = reinterpret_cast<unsigned long long>(ps.base + static_cast<int64_t>(page) * ps.page_bytes +
                                                static_cast<int64_t>(wk.kvh) * ps.head_bytes) |
@@ -299,37 +305,60 @@ __device__ __forceinline__ void resolve_page(const AttnParams& p, const Work& wk
   c.scales = i8 ? reinterpret_cast<unsigned long long>(ps.scales + static_cast<int64_t>(page) * ps.scale_page_bytes +
                                                        (ps.scale_per_head ? static_cast<int64_t>(wk.kvh) * 64 : 0))
                 : 0ull;
-  desc[i] = c;
+  desc[slot] = c;
 }
 
-// The producer warp's job: resolve the chunk's pages (one lane per page) and
-// let lane 0 keep the ring full. The first 32 pages are resolved first and the
-// ring's first stages issued at once; the rest are resolved while those copies
-// are in flight. Returns the pages issued (lane 0).
+// The producer warp's job: resolve the chunk's pages (one lane per page, 32
+// per round; the first round's copies go out at once, later rounds are
+// resolved while the ring is full) and let lane 0 keep the ring full; then one
+// end marker per consumer warp (a position whose page index is -1, completed
+// by a plain arrive). Returns the pages issued (lane 0).
 template <typename S>
-__device__ int produce(const AttnParams& p, const Work& wk, int* pg, uint32_t* pmask, PageCopy* desc,
+__device__ int produce(const AttnParams& p, const Work& wk, int32_t* meta_k, uint32_t* meta_f, PageCopy* desc,
                        char* ring, uint32_t full0, uint32_t empty0, volatile int* abort_flag) {
-  static_assert(kAttnStages <= 32, "the first resolved round must cover the ring");
+  static_assert(kMeta >= 32 + kAttnStages, "metadata ring too small");
   const int lane = threadIdx.x & 31;
-  if (lane < wk.npg) resolve_page(p, wk, lane, pg, pmask, desc);
-  __syncwarp();
   uint64_t policy;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(policy));
-  const int first = wk.npg < kAttnStages ? wk.npg : kAttnStages;
-  if (lane == 0)
-    for (int i = 0; i < first; ++i) issue_page<S>(desc[i], i, ring, full0, policy);
-  for (int i = 32 + lane; i < wk.npg; i += 32) resolve_page(p, wk, i, pg, pmask, desc);
-  __syncwarp();
-  int issued = first;
-  if (lane == 0) {
-    for (int i = first; i < wk.npg; ++i) {
-      const int st = i % kAttnStages;
-      if (!mbar_wait(empty0 + st * 8, ((i / kAttnStages) - 1) & 1)) {
+  int pos = 0, issued = 0;
+  bool ok = true;  // lane 0: no bounded wait gave up
+  auto stage_free = [&](int i) {  // position i's stage has been released by position i - stages
+    return i < kAttnStages || mbar_wait(empty0 + (i % kAttnStages) * 8, ((i / kAttnStages) - 1) & 1);
+  };
+  auto resolve = [&](int first_page, int n) {
+    if (lane < n) resolve_page(p, wk, first_page + lane, (pos + lane) % kMeta, meta_k, meta_f, desc);
+    __syncwarp();
+  };
+  auto issue = [&](int n) {
+    if (lane == 0) {
+      for (int j = 0; j < n && ok; ++j) {
+        const int i = pos + j;
+        if (!stage_free(i)) {
+          ok = false;
+          *abort_flag = 1;
+          break;
+        }
+        issue_page<S>(desc[i % kMeta], i % kAttnStages, ring, full0, policy);
+        ++issued;
+      }
+    }
+    pos += n;
+    __syncwarp();
+  };
+  for (int r = 0; r < wk.npg; r += 32) {
+    const int n = min(32, wk.npg - r);
+    resolve(wk.k0 + r, n);
+    issue(n);
+  }
+  if (lane == 0 && ok) {
+    for (int j = 0; j < kAttnWarps; ++j) {
+      const int i = pos + j;
+      if (!stage_free(i)) {
         *abort_flag = 1;
         break;
       }
-      issue_page<S>(desc[i], st, ring, full0, policy);
-      ++issued;
+      meta_k[i % kMeta] = -1;
+      mbar_arrive(full0 + (i % kAttnStages) * 8);
     }
   }
   __syncwarp();
@@ -405,9 +434,11 @@ struct LayerBufs {
   void* out;
 };
 
+// `part` / `parts` take a share of the chunk's slots (the output merge goes with
+// part 0), so that the work can be handed out in smaller pieces.
 template <typename T, int G, int D, int NT, typename Sync>
 __device__ void layer_epilogue(const AttnParams& p, const LayerBufs& lb, const Work& wk, int tid,
-                               float* sM, float* sIZ, Sync sync) {
+                               float* sM, float* sIZ, Sync sync, int part = 0, int parts = 1) {
   const int warp = tid >> 5, lane = tid & 31;
   const int64_t base = static_cast<int64_t>(wk.cf) * p.Hkv + wk.kvh;  // partial of chunk j: base + j * Hkv
   const int nch = wk.nch;
@@ -431,7 +462,7 @@ __device__ void layer_epilogue(const AttnParams& p, const LayerBufs& lb, const W
     }
   }
   sync();
-  {
+  if (part == 0) {
     // this chunk's slice of the G * D outputs
     const int lo = static_cast<int>((static_cast<int64_t>(wk.jc) * G * D) / nch);
     const int hi = static_cast<int>((static_cast<int64_t>(wk.jc + 1) * G * D) / nch);
@@ -463,8 +494,10 @@ __device__ void layer_epilogue(const AttnParams& p, const LayerBufs& lb, const W
     IZ[g] = sIZ[g];
   }
   constexpr int U = 4;
-  const int items = wk.npg * kPage;
-  for (int first = tid; first < items; first += NT * U) {
+  const int all = wk.npg * kPage;
+  const int lo = static_cast<int>((static_cast<int64_t>(part) * all) / parts);
+  const int items = static_cast<int>((static_cast<int64_t>(part + 1) * all) / parts);
+  for (int first = lo + tid; first < items; first += NT * U) {
     float l[U][G], old[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
@@ -517,15 +550,18 @@ __device__ __forceinline__ void prev_layer_epilogue(const AttnParams& p, int tid
                                                     volatile int* s_item) {
   if (!p.has_prev) return;
   const LayerBufs lb{p.prev_part_o, p.prev_part_m, p.prev_part_z, p.prev_spill, p.prev_out};
-  const int items = static_cast<int>(gridDim.x * gridDim.y);
+  constexpr int kParts = 1;  // pieces per (chunk, KV head)
+  const int items = static_cast<int>(gridDim.x * gridDim.y) * kParts;
   for (;;) {
     __syncthreads();
     if (tid == 0) *s_item = atomicAdd(p.ep_next, 1);
     __syncthreads();
     const int item = *s_item;
     if (item >= items) break;
-    const Work wk = find_work_at(p, item % static_cast<int>(gridDim.x), item / static_cast<int>(gridDim.x));
-    layer_epilogue<T, G, D, (kAttnWarps + 1) * 32>(p, lb, wk, tid, sM, sIZ, [] { __syncthreads(); });
+    const int unit = item / kParts;
+    const Work wk = find_work_at(p, unit % static_cast<int>(gridDim.x), unit / static_cast<int>(gridDim.x));
+    layer_epilogue<T, G, D, (kAttnWarps + 1) * 32>(p, lb, wk, tid, sM, sIZ, [] { __syncthreads(); },
+                                                   item % kParts, kParts);
   }
 }
 
@@ -599,19 +635,20 @@ __global__ void __launch_bounds__((kAttnWarps + 1) * 32, 3)
   const int g = lane >> 2, t = lane & 3;  // fragment row group and column pair
   const Work wk = find_work(p);
   if (tid == 0) s_abort = 0;
-  if (tid == 0 && blockIdx.x == 0 && blockIdx.y == 0 && p.ep_clear) *p.ep_clear = 0;
+  if (tid == 0 && blockIdx.x == 0 && blockIdx.y == 0 && p.ep_clear) *p.ep_clear = 0;  // the next launch's counter
   init_barriers<L>(smem);
   __syncthreads();
 
-  int* pg = reinterpret_cast<int*>(smem + L::off_pg);
-  uint32_t* pmask = reinterpret_cast<uint32_t*>(pg + kMaxChunkPages);
+  int32_t* meta_k = reinterpret_cast<int32_t*>(smem + L::off_pg);
+  uint32_t* meta_f = reinterpret_cast<uint32_t*>(meta_k + kMeta);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::off_bar);
   char* ring = smem;
   const uint32_t full0 = smem_u32(bars), empty0 = full0 + kAttnStages * 8;
   const bool consumer = w < kAttnWarps;
   int issued = 0;
   if (!consumer)
-    issued = produce<S>(p, wk, pg, pmask, reinterpret_cast<PageCopy*>(smem + L::off_desc), ring, full0, empty0, &s_abort);
+    issued = produce<S>(p, wk, meta_k, meta_f, reinterpret_cast<PageCopy*>(smem + L::off_desc), ring, full0, empty0,
+                        &s_abort);
 
   // Q fragments (A operand, heads as rows; rows 8..15 of the tile are zero)
   uint32_t qa[KS][2];
@@ -638,16 +675,17 @@ __global__ void __launch_bounds__((kAttnWarps + 1) * 32, 3)
   const int lrow = ((lane >> 4) << 3) | (lane & 7);
   const int lchunk = (lane >> 3) & 1;
 
-  for (int i = w; consumer && i < wk.npg; i += kAttnWarps) {
+  for (int i = w; consumer; i += kAttnWarps) {
     const int st = i % kAttnStages;
     const bool ok = __all_sync(kFull, mbar_wait(full0 + st * 8, (i / kAttnStages) & 1));
     if (!ok) {
       if (lane == 0) s_abort = 1;
       break;
     }
+    const int k = meta_k[i % kMeta];  // page index in the sequence's list; -1 ends this warp's pages
+    if (k < 0) break;
     char* stage = ring + st * S::STAGE;
-    const int k = wk.k0 + i;
-    const uint32_t flags = pmask[i];
+    const uint32_t flags = meta_f[i % kMeta];
     const uint32_t mask = flags & 0xffffu;
     const bool i8 = (flags & kFlagI8) != 0;
     const int swz = i8 ? kSwizzle : static_cast<int>((flags >> kFlagSwzShift) & 7u);
@@ -884,19 +922,20 @@ __global__ void __launch_bounds__((kAttnWarps + 1) * 32)
   const int r = lane >> 3, c = lane & 7;
   const Work wk = find_work(p);
   if (tid == 0) s_abort = 0;
-  if (tid == 0 && blockIdx.x == 0 && blockIdx.y == 0 && p.ep_clear) *p.ep_clear = 0;
+  if (tid == 0 && blockIdx.x == 0 && blockIdx.y == 0 && p.ep_clear) *p.ep_clear = 0;  // the next launch's counter
   init_barriers<L>(smem);
   __syncthreads();
 
-  int* pg = reinterpret_cast<int*>(smem + L::off_pg);
-  uint32_t* pmask = reinterpret_cast<uint32_t*>(pg + kMaxChunkPages);
+  int32_t* meta_k = reinterpret_cast<int32_t*>(smem + L::off_pg);
+  uint32_t* meta_f = reinterpret_cast<uint32_t*>(meta_k + kMeta);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::off_bar);
   char* ring = smem;
   const uint32_t full0 = smem_u32(bars), empty0 = full0 + kAttnStages * 8;
   const bool consumer = w < kAttnWarps;
   int issued = 0;
   if (!consumer)
-    issued = produce<S>(p, wk, pg, pmask, reinterpret_cast<PageCopy*>(smem + L::off_desc), ring, full0, empty0, &s_abort);
+    issued = produce<S>(p, wk, meta_k, meta_f, reinterpret_cast<PageCopy*>(smem + L::off_desc), ring, full0, empty0,
+                        &s_abort);
 
   float* q_s = reinterpret_cast<float*>(smem + L::off_q);
   float* p_s = reinterpret_cast<float*>(smem + L::off_p) + w * L::PSW;
@@ -932,16 +971,17 @@ __global__ void __launch_bounds__((kAttnWarps + 1) * 32)
 
   float* spill_b = p.spill + (static_cast<int64_t>(wk.b) * p.Hkv + wk.kvh) * p.spill_stride;
 
-  for (int i = w; consumer && i < wk.npg; i += kAttnWarps) {
+  for (int i = w; consumer; i += kAttnWarps) {
     const int st = i % kAttnStages;
     const bool ok = __all_sync(kFull, mbar_wait(full0 + st * 8, (i / kAttnStages) & 1));
     if (!ok) {
       if (lane == 0) s_abort = 1;
       break;
     }
+    const int k = meta_k[i % kMeta];  // page index in the sequence's list; -1 ends this warp's pages
+    if (k < 0) break;
     const char* stage = ring + st * S::STAGE;
-    const int k = wk.k0 + i;
-    const uint32_t flags = pmask[i];
+    const uint32_t flags = meta_f[i % kMeta];
     const uint32_t mask = flags & 0xffffu;
     const bool i8 = (flags & kFlagI8) != 0;
     const bool per_head = (flags & kFlagPerHead) != 0;

@@ -205,6 +205,7 @@ struct tkv_ctx {
   cudaEvent_t ev_ready[2] = {nullptr, nullptr}, ev_free[2] = {nullptr, nullptr};
   int slot_rr = 0;
   int64_t steps = 0;
+  int64_t attn_launch_seq = 0;    // attention launches so far: their parity picks buffers and counters
   int64_t next_page[3] = {0, 0, 0};
   MinHeap free_pages[3];          // freed page ids per tier pool
   std::vector<Seq> seqs;
@@ -646,7 +647,9 @@ tkv_status decode_step_device(tkv_ctx* h, const void* q, const void* k_new, cons
     if (st) return st;
     if (h->xs != h->cs) CK(h, cudaStreamWaitEvent(h->cs, h->ev_ready[slot], 0));
     fill_sources(h, l, slot, p);
-    const int par = l & 1;
+    // consecutive launches alternate parity, across steps too (a step may have an odd layer count)
+    const int par = static_cast<int>(h->attn_launch_seq & 1);
+    h->attn_launch_seq += 1;
     p.has_prev = l > 0;
     p.ep_next = reinterpret_cast<int32_t*>(h->D(y.o_err)) + 4 + par;   // counters by layer parity
     p.ep_clear = reinterpret_cast<int32_t*>(h->D(y.o_err)) + 4 + (par ^ 1);

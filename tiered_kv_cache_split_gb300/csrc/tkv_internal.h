@@ -28,10 +28,10 @@ constexpr int kMaxChunksPerSeq = 128;  // chunks one sequence may be split into
 constexpr int kMaxSeqPages = 16384;    // pages of one sequence (all tiers)
 
 // Chunks of a sequence's page list (T0, T1, then T2 pages) are balanced by
-// cost, not page count: an 8-bit T2 page carries half the bytes of a
+// cost, in half-page units per page: a T2 page carries half the bytes of a
 // full-precision page but is widened in shared memory first, and measured
-// about twice as long to process. Costs are in half-page units.
-constexpr int kCostFull = 2, kCostI8 = 4;
+// about 1.5 times as long to process.
+constexpr int kCostFull = 2, kCostI8 = 3;
 // Page index at cost c of a list of n01 full-precision pages followed by 8-bit ones.
 __host__ __device__ inline int page_at_cost(int64_t c, int n01) {
   const int64_t full = static_cast<int64_t>(kCostFull) * n01;
