@@ -635,7 +635,12 @@ __global__ void __launch_bounds__((kAttnWarps + 1) * 32, 3)
   const int g = lane >> 2, t = lane & 3;  // fragment row group and column pair
   const Work wk = find_work(p);
   if (tid == 0) s_abort = 0;
-  if (tid == 0 && blockIdx.x == 0 && blockIdx.y == 0 && p.ep_clear) *p.ep_clear = 0;  // the next launch's counter
+  if (tid == 0 && blockIdx.x == 0 && blockIdx.y == 0) {
+    if (p.ep_clear) *p.ep_clear = 0;  // the next launch's counter
+    if (p.started) {                  // tells the copy stream this launch is under way
+      asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p.started), "r"(p.launch_seq) : "memory");
+    }
+  }
   init_barriers<L>(smem);
   __syncthreads();
 
@@ -922,7 +927,12 @@ __global__ void __launch_bounds__((kAttnWarps + 1) * 32)
   const int r = lane >> 3, c = lane & 7;
   const Work wk = find_work(p);
   if (tid == 0) s_abort = 0;
-  if (tid == 0 && blockIdx.x == 0 && blockIdx.y == 0 && p.ep_clear) *p.ep_clear = 0;  // the next launch's counter
+  if (tid == 0 && blockIdx.x == 0 && blockIdx.y == 0) {
+    if (p.ep_clear) *p.ep_clear = 0;  // the next launch's counter
+    if (p.started) {                  // tells the copy stream this launch is under way
+      asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p.started), "r"(p.launch_seq) : "memory");
+    }
+  }
   init_barriers<L>(smem);
   __syncthreads();
 

@@ -42,6 +42,7 @@ namespace {
 thread_local std::string g_last_error = "no error";
 
 constexpr size_t kAlign = 256;
+constexpr size_t kStartedWordOffset = 32;  // byte offset of the started word in the error region
 size_t align_up(size_t x, size_t a = kAlign) { return (x + a - 1) / a * a; }
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -160,7 +161,8 @@ Layout make_layout(const tkv_config& c) {
   y.o_part_z = take(2 * size_t(y.max_chunks) * y.Hkv * y.G * 4);
   y.o_spill = take(2 * size_t(y.maxb) * y.Hkv * y.spill_stride * 4);
   y.o_keys = take(size_t(y.maxb) * y.maxtok * 8);
-  y.o_err = take(64);   // int32 [0]: device error word; [4], [5]: epilogue work counters by layer parity
+  y.o_err = take(64);   // int32 [0]: device error word; [4], [5]: epilogue work counters by layer parity;
+                        // [8]: sequence number of the last attention launch that started
   y.o_movers = take(2 * size_t(y.maxb) * y.maxtok * sizeof(Mover));
   y.o_temp = take(size_t(y.temp_rows) * y.L * 2 * y.Hkv * y.D * y.esz);
   y.o_locs = take(size_t(y.maxtok) * 4);
@@ -187,6 +189,12 @@ Layout make_layout(const tkv_config& c) {
   return y;
 }
 
+// The driver's stream memory wait (cuStreamWaitValue32, "wait until
+// (int32_t)(*addr - value) >= 0"), obtained at run time so that the library
+// links against the runtime alone.
+typedef int (*WaitValue32Fn)(void* stream, unsigned long long addr, unsigned int value, unsigned int flags);
+constexpr unsigned int kWaitGeq = 0;
+
 struct TimedPair {
   cudaEvent_t a, b;
   int kind;  // 0 attention stream kernel, 1 prefetch, 2 combine / score kernel
@@ -206,6 +214,10 @@ struct tkv_ctx {
   int slot_rr = 0;
   int64_t steps = 0;
   int64_t attn_launch_seq = 0;    // attention launches so far: their parity picks buffers and counters
+  // Copy-stream gate: a prefetch waits (stream memory wait) until the previous
+  // attention launch has started, so that launch is not made behind a host
+  // link that the next prefetch already saturates. Null where unsupported.
+  WaitValue32Fn wait_value = nullptr;
   int64_t next_page[3] = {0, 0, 0};
   MinHeap free_pages[3];          // freed page ids per tier pool
   std::vector<Seq> seqs;
@@ -492,11 +504,17 @@ int plan_chunks(const std::vector<int64_t>& ntot, const std::vector<int64_t>& co
   return bound;
 }
 
-tkv_status enqueue_prefetch(tkv_ctx* h, int layer, int slot) {
+// gate_seq != 0: first wait until the attention launch with that sequence
+// number has started (its first CTA writes the number to the started word).
+tkv_status enqueue_prefetch(tkv_ctx* h, int layer, int slot, uint32_t gate_seq = 0) {
   const Layout& y = h->y;
   const bool timing = h->cfg.flags & TKV_FLAG_TIMING;
   TimedPair tp{};
   if (h->xs != h->cs) CK(h, cudaStreamWaitEvent(h->xs, h->ev_free[slot], 0));
+  if (gate_seq != 0 && h->wait_value && h->xs != h->cs) {
+    const unsigned long long addr = reinterpret_cast<unsigned long long>(h->D(y.o_err)) + kStartedWordOffset;
+    if (h->wait_value(h->xs, addr, gate_seq, kWaitGeq) != 0) h->wait_value = nullptr;  // unsupported: ungated from now on
+  }
   if (timing) {
     tkv_status st = timed_pair(h, 1, &tp);
     if (st) return st;
@@ -643,13 +661,15 @@ tkv_status decode_step_device(tkv_ctx* h, const void* q, const void* k_new, cons
   for (int l = 0; l < y.L; ++l) {
     const int slot = h->slot_rr;
     h->slot_rr ^= 1;
-    tkv_status st = enqueue_prefetch(h, l, slot);
+    tkv_status st = enqueue_prefetch(h, l, slot, static_cast<uint32_t>(h->attn_launch_seq));
     if (st) return st;
     if (h->xs != h->cs) CK(h, cudaStreamWaitEvent(h->cs, h->ev_ready[slot], 0));
     fill_sources(h, l, slot, p);
     // consecutive launches alternate parity, across steps too (a step may have an odd layer count)
     const int par = static_cast<int>(h->attn_launch_seq & 1);
     h->attn_launch_seq += 1;
+    p.started = reinterpret_cast<uint32_t*>(h->D(y.o_err) + kStartedWordOffset);
+    p.launch_seq = static_cast<uint32_t>(h->attn_launch_seq);
     p.has_prev = l > 0;
     p.ep_next = reinterpret_cast<int32_t*>(h->D(y.o_err)) + 4 + par;   // counters by layer parity
     p.ep_clear = reinterpret_cast<int32_t*>(h->D(y.o_err)) + 4 + (par ^ 1);
@@ -982,6 +1002,14 @@ tkv_status tkv_create(const tkv_config* cfg, void* dev_ws, size_t dev_bytes, voi
   h->d_tier = reinterpret_cast<uint8_t*>(h->D(y.o_tier));
   h->d_tier_new = reinterpret_cast<uint8_t*>(h->D(y.o_tier_new));
   h->resident_ctas = resident_attention_ctas(cfg->kv_dtype, y.G, y.D);
+  {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuStreamWaitValue32", &fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      h->wait_value = reinterpret_cast<WaitValue32Fn>(fn);
+    (void)cudaGetLastError();
+  }
   // zero what must start at zero: pools (holes must hold finite values), tables,
   // masks, accumulators, scores, the error word; posmaps start at -1
   struct Z { size_t off, bytes; int val; } zs[] = {

@@ -98,6 +98,8 @@ struct AttnParams {
   int32_t has_prev;
   int32_t* ep_next;       // work counter of the previous layer's epilogue items (zero at launch)
   int32_t* ep_clear;      // the other layer parity's counter, zeroed by this launch for the next one
+  uint32_t* started;      // if set, the first CTA writes launch_seq here at entry
+  uint32_t launch_seq;
   const float* prev_part_o;
   const float* prev_part_m;
   const float* prev_part_z;
