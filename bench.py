@@ -255,6 +255,8 @@ def run_gpu(args):
     pair = bytes_per_launch / ((attn_ms + combine_ms) * 1e6) if attn_ms > 0 else 0.0
     prefetch_gbs = st["prefetch_bytes"] / (st["prefetch_ms"] * 1e6) if st["prefetch_ms"] > 0 else None
     launches = st["kernel_launches"]   # counted by the library over the timed region
+    span_us = 1000.0 * st["attn_span_ms"] / max(st["attn_launches"], 1) if st["attn_span_ms"] > 0 else None
+    span_gbs = bytes_per_launch / (span_us * 1e3) if span_us else None
     clocks = clk.summary()
     traffic = _traffic(w.name)
     line = {
@@ -266,7 +268,11 @@ def run_gpu(args):
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": traffic, "bytes_per_launch": bytes_per_launch,
                      "launch_ms": attn_ms, "combine_ms_per_layer": combine_ms,
-                     "with_combine": {"achieved": pair, "frac": pair / peak}},
+                     "with_combine": {"achieved": pair, "frac": pair / peak},
+                     # the kernel body alone: first CTA start to last CTA end (%globaltimer),
+                     # without the launch and event overhead the CUDA-event figure includes
+                     "device_span": {"us_per_launch": span_us, "achieved": span_gbs,
+                                     "frac": span_gbs / peak if span_gbs else None}},
         "kv_read_gbs": achieved,
         "link": {"prefetch_gbs": prefetch_gbs, "probe_h2d_gbs": link_gbs,
                  "frac": (prefetch_gbs / link_gbs) if prefetch_gbs else None,

@@ -93,7 +93,9 @@ typedef struct {
   int32_t t2_scale_dtype;                             /* TKV_SCALE_F32 | TKV_SCALE_F16 */
   int32_t t2_mode;                                    /* TKV_T2_ATTEND | TKV_T2_MASK */
   int64_t t0_pages, t1_pages, t2_pages;               /* pool capacities; 0 = derived */
-  int64_t max_staged_movers;                          /* mover staging rows; 0 = derived */
+  int64_t max_staged_movers;                          /* staging rows (one layer each) for moves into
+                                                         slots vacated in the same reassignment;
+                                                         0 = one per position (always enough) */
   int32_t split_pages;                                /* pages per attention CTA; 0 = auto */
   int32_t flags;                                      /* TKV_FLAG_* */
 } tkv_config;
@@ -113,6 +115,8 @@ typedef struct {
   double prefetch_ms;          /* summed prefetch copy time      (TKV_FLAG_TIMING) */
   double reclassify_ms;        /* summed reclassify wall time    (TKV_FLAG_TIMING) */
   int64_t kernel_launches;     /* kernels this handle launched (steps, reclassify, prefill) */
+  double attn_span_ms;         /* summed device span of the attention launches: first CTA start to
+                                  last CTA end, %globaltimer (TKV_FLAG_TIMING; last 4096 launches) */
 } tkv_stats;
 
 /* Device and pinned-host bytes tkv_create needs for this configuration. */

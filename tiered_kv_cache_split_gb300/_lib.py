@@ -40,7 +40,7 @@ class Stats(ctypes.Structure):
         ("d2h_move_bytes", c_i64), ("tier_counts", c_i64 * 4), ("attn_ms", ctypes.c_double),
         ("combine_ms", ctypes.c_double),
         ("prefetch_ms", ctypes.c_double), ("reclassify_ms", ctypes.c_double),
-        ("kernel_launches", c_i64),
+        ("kernel_launches", c_i64), ("attn_span_ms", ctypes.c_double),
     ]
 
 

@@ -443,17 +443,30 @@ __device__ void layer_epilogue(const AttnParams& p, const LayerBufs& lb, const W
   const int64_t base = static_cast<int64_t>(wk.cf) * p.Hkv + wk.kvh;  // partial of chunk j: base + j * Hkv
   const int nch = wk.nch;
   for (int g = warp; g < G; g += NT / 32) {
-    float M = -INFINITY;
-    for (int j = lane; j < nch; j += 32) M = fmaxf(M, __ldg(lb.part_m + (base + static_cast<int64_t>(j) * p.Hkv) * G + g));
+    // one round of loads: up to 64 chunks per lane pair (m, z) in registers
+    float mj[2], zj[2];
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const int j = lane + 32 * r;
+      const int64_t pj = (base + static_cast<int64_t>(j) * p.Hkv) * G + g;
+      mj[r] = j < nch ? __ldg(lb.part_m + pj) : -INFINITY;
+      zj[r] = j < nch ? __ldg(lb.part_z + pj) : 0.f;
+    }
+    float M = fmaxf(mj[0], mj[1]);
+    for (int j = lane + 64; j < nch; j += 32) M = fmaxf(M, __ldg(lb.part_m + (base + static_cast<int64_t>(j) * p.Hkv) * G + g));
 #pragma unroll
     for (int m = 16; m >= 1; m >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, m));
     float Z = 0.f;
-    if (M != -INFINITY)
-      for (int j = lane; j < nch; j += 32) {
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int r = 0; r < 2; ++r)
+        if (mj[r] != -INFINITY) Z += zj[r] * exp2f(mj[r] - M);
+      for (int j = lane + 64; j < nch; j += 32) {
         const int64_t pj = (base + static_cast<int64_t>(j) * p.Hkv) * G + g;
-        const float mj = __ldg(lb.part_m + pj);
-        if (mj != -INFINITY) Z += __ldg(lb.part_z + pj) * exp2f(mj - M);
+        const float m2 = __ldg(lb.part_m + pj);
+        if (m2 != -INFINITY) Z += __ldg(lb.part_z + pj) * exp2f(m2 - M);
       }
+    }
 #pragma unroll
     for (int m = 16; m >= 1; m >>= 1) Z += __shfl_xor_sync(kFull, Z, m);
     if (lane == 0) {
@@ -635,7 +648,12 @@ __global__ void __launch_bounds__((kAttnWarps + 1) * 32, 3)
   const int g = lane >> 2, t = lane & 3;  // fragment row group and column pair
   const Work wk = find_work(p);
   if (tid == 0) s_abort = 0;
+  if (tid == 0 && p.span) atomicMin(p.span, global_ns());
   if (tid == 0 && blockIdx.x == 0 && blockIdx.y == 0) {
+    if (p.span_next) {
+      p.span_next[0] = ~0ull;
+      p.span_next[1] = 0ull;
+    }
     if (p.ep_clear) *p.ep_clear = 0;  // the next launch's counter
     if (p.started) {                  // tells the copy stream this launch is under way
       asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p.started), "r"(p.launch_seq) : "memory");
@@ -831,6 +849,7 @@ __global__ void __launch_bounds__((kAttnWarps + 1) * 32, 3)
   __syncthreads();
   write_partial<T, G, D>(p, wk, smem);
   prev_layer_epilogue<T, G, D>(p, tid, s_epM, s_epIZ, &s_item);
+  if (tid == 0 && p.span) atomicMax(p.span + 1, global_ns());
 }
 
 // ===================================================================== FP32
@@ -927,7 +946,12 @@ __global__ void __launch_bounds__((kAttnWarps + 1) * 32)
   const int r = lane >> 3, c = lane & 7;
   const Work wk = find_work(p);
   if (tid == 0) s_abort = 0;
+  if (tid == 0 && p.span) atomicMin(p.span, global_ns());
   if (tid == 0 && blockIdx.x == 0 && blockIdx.y == 0) {
+    if (p.span_next) {
+      p.span_next[0] = ~0ull;
+      p.span_next[1] = 0ull;
+    }
     if (p.ep_clear) *p.ep_clear = 0;  // the next launch's counter
     if (p.started) {                  // tells the copy stream this launch is under way
       asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p.started), "r"(p.launch_seq) : "memory");
@@ -1190,6 +1214,7 @@ __global__ void __launch_bounds__((kAttnWarps + 1) * 32)
   __syncthreads();
   write_partial<T, G, D>(p, wk, smem);
   prev_layer_epilogue<T, G, D>(p, tid, s_epM, s_epIZ, &s_item);
+  if (tid == 0 && p.span) atomicMax(p.span + 1, global_ns());
 }
 
 template <typename K>

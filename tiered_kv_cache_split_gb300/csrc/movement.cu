@@ -140,12 +140,12 @@ __global__ void prefill_kernel(const __grid_constant__ PrefillParams p) {
 constexpr int kMoveThreads = 128;
 
 // Full-precision chunk c of row hk (= head * 2 + kv) of a location: a pool slot
-// (tier 0 or 1), or a staging row of `temp` (plain layout [rows][L][2][Hkv][D]).
+// (tier 0 or 1), or a staging row of `temp` (one layer, plain layout [rows][2][Hkv][D]).
 __device__ __forceinline__ char* full_chunk(const MoveParams& p, int tier, int loc, int temp_row, int l,
                                            int hk, int c, int64_t row_bytes) {
   if (tier < 0) {
     const int h = hk >> 1, kv = hk & 1;
-    return p.temp + (((static_cast<int64_t>(temp_row) * p.L + l) * 2 + kv) * p.Hkv + h) * row_bytes + c * 16;
+    return p.temp + ((static_cast<int64_t>(temp_row) * 2 + kv) * p.Hkv + h) * row_bytes + c * 16;
   }
   const int page = loc >> 4, slot = loc & 15;
   const TierPools& P = p.pools;
@@ -166,7 +166,7 @@ __global__ void __launch_bounds__(kMoveThreads) move_kernel(const __grid_constan
                                                             const Mover* __restrict__ movers) {
   extern __shared__ float row_s[];  // [2][Hkv][D] float32 (rows entering T2)
   const Mover mv = movers[blockIdx.x];
-  const int l = blockIdx.y;
+  const int l = p.layer0 + blockIdx.y;
   const int tid = threadIdx.x;
   const int esz = p.kv_dtype == 1 ? 2 : 4;
   const int64_t row_bytes = static_cast<int64_t>(p.D) * esz;
@@ -356,8 +356,8 @@ cudaError_t launch_prefill(const PrefillParams& p, cudaStream_t s) {
   return cudaGetLastError();
 }
 
-cudaError_t launch_move(const MoveParams& p, const Mover* movers, int64_t count, cudaStream_t s) {
-  if (count <= 0) return cudaSuccess;
+cudaError_t launch_move(const MoveParams& p, const Mover* movers, int64_t count, int layers, cudaStream_t s) {
+  if (count <= 0 || layers <= 0) return cudaSuccess;
   const size_t smem = static_cast<size_t>(2) * p.Hkv * p.D * sizeof(float);
   static bool configured = false;
   if (!configured) {
@@ -366,7 +366,7 @@ cudaError_t launch_move(const MoveParams& p, const Mover* movers, int64_t count,
     configured = true;
   }
   if (smem > 96 * 1024) return cudaErrorInvalidValue;
-  move_kernel<<<dim3(static_cast<unsigned>(count), p.L), kMoveThreads, smem, s>>>(p, movers);
+  move_kernel<<<dim3(static_cast<unsigned>(count), static_cast<unsigned>(layers)), kMoveThreads, smem, s>>>(p, movers);
   return cudaGetLastError();
 }
 

@@ -67,7 +67,7 @@ struct Layout {
   int64_t max_chunks, spill_stride, temp_rows;
   // device offsets
   size_t o_pool0, o_stage1, o_stage2c, o_stage2s, o_table, o_mask, o_posmap, o_tier, o_tier_new,
-      o_s, o_acc, o_part_o, o_part_m, o_part_z, o_spill, o_keys, o_err, o_movers,
+      o_s, o_acc, o_part_o, o_part_m, o_part_z, o_spill, o_keys, o_err, o_span, o_movers,
       o_temp, o_locs, o_io, dev_bytes;
   size_t io_q, io_k, io_out;
   // pinned offsets
@@ -139,8 +139,9 @@ Layout make_layout(const tkv_config& c) {
   y.scale_rec = c.t2_scale_gran == TKV_SCALE_PER_TOKEN ? 2 * kPage * 4 : int64_t(y.Hkv) * 2 * kPage * 2;
   y.max_chunks = int64_t(y.maxb) * (ceil_div(3 * y.maxp, 8) + 1);
   y.spill_stride = 3 * y.maxp * y.G * kPage;
-  y.temp_rows = c.max_staged_movers ? c.max_staged_movers
-                                    : std::max<int64_t>(4096, int64_t(y.maxb) * y.maxtok / 10);
+  // staging rows hold one layer (phase-2 moves run layer by layer); by default
+  // one per position, so any reassignment fits
+  y.temp_rows = c.max_staged_movers ? c.max_staged_movers : int64_t(y.maxb) * y.maxtok;
   size_t o = 0;
   auto take = [&](size_t bytes) { size_t at = o; o = align_up(o + bytes); return at; };
   y.o_pool0 = take(size_t(y.L) * y.cap[0] * y.plb[0]);
@@ -163,8 +164,9 @@ Layout make_layout(const tkv_config& c) {
   y.o_keys = take(size_t(y.maxb) * y.maxtok * 8);
   y.o_err = take(64);   // int32 [0]: device error word; [4], [5]: epilogue work counters by layer parity;
                         // [8]: sequence number of the last attention launch that started
+  y.o_span = take(size_t(kSpanSlots) * 16);  // device span (start, end) of attention launches, by sequence number
   y.o_movers = take(2 * size_t(y.maxb) * y.maxtok * sizeof(Mover));
-  y.o_temp = take(size_t(y.temp_rows) * y.L * 2 * y.Hkv * y.D * y.esz);
+  y.o_temp = take(size_t(y.temp_rows) * 2 * y.Hkv * y.D * y.esz);
   y.o_locs = take(size_t(y.maxtok) * 4);
   const size_t q_bytes = size_t(y.maxb) * y.L * y.Hq * y.D * y.esz;
   const size_t kv_bytes = size_t(y.maxb) * y.L * y.Hkv * y.D * y.esz;
@@ -214,6 +216,7 @@ struct tkv_ctx {
   int slot_rr = 0;
   int64_t steps = 0;
   int64_t attn_launch_seq = 0;    // attention launches so far: their parity picks buffers and counters
+  int64_t span_from = 0;          // first attention launch counted in attn_span_ms
   // Copy-stream gate: a prefetch waits (stream memory wait) until the previous
   // attention launch has started, so that launch is not made behind a host
   // link that the next prefetch already saturates. Null where unsupported.
@@ -670,6 +673,11 @@ tkv_status decode_step_device(tkv_ctx* h, const void* q, const void* k_new, cons
     h->attn_launch_seq += 1;
     p.started = reinterpret_cast<uint32_t*>(h->D(y.o_err) + kStartedWordOffset);
     p.launch_seq = static_cast<uint32_t>(h->attn_launch_seq);
+    if (timing) {
+      unsigned long long* spans = reinterpret_cast<unsigned long long*>(h->D(y.o_span));
+      p.span = spans + 2 * (h->attn_launch_seq % kSpanSlots);
+      p.span_next = spans + 2 * ((h->attn_launch_seq + 1) % kSpanSlots);
+    }
     p.has_prev = l > 0;
     p.ep_next = reinterpret_cast<int32_t*>(h->D(y.o_err)) + 4 + par;   // counters by layer parity
     p.ep_clear = reinterpret_cast<int32_t*>(h->D(y.o_err)) + 4 + (par ^ 1);
@@ -914,15 +922,24 @@ tkv_status do_reclassify(tkv_ctx* h) {
   mp.pools.scale_per_head = h->cfg.t2_scale_gran == TKV_SCALE_PER_TOKEN_HEAD;
   mp.pools.scale_f16 = h->cfg.t2_scale_dtype == TKV_SCALE_F16;
   mp.temp = h->D(y.o_temp);
-  mp.mode = MOVE_GATHER;
-  LK(h, launch_move(mp, dm, int64_t(phase2.size()), h->cs), !phase2.empty());
+  // Every source is read before any slot is written that a mover vacated:
+  // phase 1 (destinations no mover vacated) reads its sources and writes at
+  // once, for all layers; then, layer by layer, phase 2 gathers its sources
+  // into the staging rows and scatters them to the recycled slots.
   mp.mode = MOVE_DIRECT;
-  LK(h, launch_move(mp, dm + phase2.size(), int64_t(phase1.size()), h->cs), !phase1.empty());
-  mp.mode = MOVE_SCATTER;
-  LK(h, launch_move(mp, dm, int64_t(phase2.size()), h->cs), !phase2.empty());
+  mp.layer0 = 0;
+  LK(h, launch_move(mp, dm + phase2.size(), int64_t(phase1.size()), y.L, h->cs), !phase1.empty());
+  for (int l = 0; l < y.L && !phase2.empty(); ++l) {
+    mp.layer0 = l;
+    mp.mode = MOVE_GATHER;
+    LK(h, launch_move(mp, dm, int64_t(phase2.size()), 1, h->cs), true);
+    mp.mode = MOVE_SCATTER;
+    LK(h, launch_move(mp, dm, int64_t(phase2.size()), 1, h->cs), true);
+  }
   // T0 compaction last: every slot it writes has been read by the moves above
   mp.mode = MOVE_DIRECT;
-  LK(h, launch_move(mp, dm + phase2.size() + phase1.size(), int64_t(compaction.size()), h->cs), !compaction.empty());
+  mp.layer0 = 0;
+  LK(h, launch_move(mp, dm + phase2.size() + phase1.size(), int64_t(compaction.size()), y.L, h->cs), !compaction.empty());
   tkv_status st = upload_metadata(h);
   if (st) return st;
   std::swap(h->d_tier, h->d_tier_new);
@@ -1024,6 +1041,12 @@ tkv_status tkv_create(const tkv_config* cfg, void* dev_ws, size_t dev_bytes, voi
   for (const Z& z : zs)
     if ((e = cudaMemsetAsync(h->D(z.off), z.val, z.bytes, h->cs)) != cudaSuccess)
       return bail(fail_cuda(nullptr, "cudaMemsetAsync", e));
+  {
+    std::vector<unsigned long long> init(2 * size_t(kSpanSlots), 0ull);
+    for (int i = 0; i < kSpanSlots; ++i) init[2 * size_t(i)] = ~0ull;
+    if ((e = cudaMemcpy(h->D(y.o_span), init.data(), init.size() * 8, cudaMemcpyHostToDevice)) != cudaSuccess)
+      return bail(fail_cuda(nullptr, "cudaMemcpy", e));
+  }
   if ((e = cudaStreamSynchronize(h->cs)) != cudaSuccess) return bail(fail_cuda(nullptr, "cudaStreamSynchronize", e));
   for (int t = 0; t < 3; ++t) {
     h->mask[t].assign(size_t(y.cap[t]), 0u);
@@ -1265,6 +1288,16 @@ tkv_status tkv_get_stats(tkv_handle h, tkv_stats* out) {
   for (int t = 0; t < 4; ++t) h->stats.tier_counts[t] = 0;
   for (const Seq& sq : h->seqs)
     for (int64_t i = 0; i < sq.N; ++i) h->stats.tier_counts[sq.tier[i]] += 1;
+  h->stats.attn_span_ms = 0.0;
+  if ((h->cfg.flags & TKV_FLAG_TIMING) && !h->broken && h->attn_launch_seq > h->span_from) {
+    std::vector<unsigned long long> sp(2 * size_t(kSpanSlots));
+    CK(h, cudaMemcpy(sp.data(), h->D(h->y.o_span), sp.size() * 8, cudaMemcpyDeviceToHost));
+    const int64_t lo = std::max<int64_t>(h->span_from, h->attn_launch_seq - kSpanSlots);
+    for (int64_t q = lo + 1; q <= h->attn_launch_seq; ++q) {  // launch q used slot q % kSpanSlots
+      const size_t i = 2 * size_t(q % kSpanSlots);
+      if (sp[i + 1] > sp[i]) h->stats.attn_span_ms += double(sp[i + 1] - sp[i]) * 1e-6;
+    }
+  }
   *out = h->stats;
   return TKV_OK;
 }
@@ -1275,6 +1308,7 @@ tkv_status tkv_reset_stats(tkv_handle h) {
     if (tkv_status st = sync_all(h)) return st;
   }
   h->stats = tkv_stats{};
+  h->span_from = h->attn_launch_seq;
   return TKV_OK;
 }
 

@@ -26,6 +26,7 @@ static_assert(kAttnStages % kAttnWarps == 0, "ring stages must be a multiple of 
 constexpr int kMaxChunkPages = 256;    // pages one attention CTA may take
 constexpr int kMaxChunksPerSeq = 128;  // chunks one sequence may be split into
 constexpr int kMaxSeqPages = 16384;    // pages of one sequence (all tiers)
+constexpr int kSpanSlots = 4096;       // attention launches whose device span is kept
 
 // Chunks of a sequence's page list (T0, T1, then T2 pages) are balanced by
 // cost, in half-page units per page: a T2 page carries half the bytes of a
@@ -100,6 +101,10 @@ struct AttnParams {
   int32_t* ep_clear;      // the other layer parity's counter, zeroed by this launch for the next one
   uint32_t* started;      // if set, the first CTA writes launch_seq here at entry
   uint32_t launch_seq;
+  // if set: span[0] = min CTA start, span[1] = max CTA end (%globaltimer ns) of
+  // this launch; span_next (the next launch's pair) is reset to (max, 0)
+  unsigned long long* span;
+  unsigned long long* span_next;
   const float* prev_part_o;
   const float* prev_part_m;
   const float* prev_part_z;
@@ -177,10 +182,11 @@ enum MoveMode : int { MOVE_DIRECT = 0, MOVE_GATHER = 1, MOVE_SCATTER = 2 };
 struct MoveParams {
   int32_t L, Hkv, D, kv_dtype;
   TierPools pools;
-  char* temp;              // [rows][L][2][Hkv][D] in the KV dtype
+  char* temp;              // staging rows of one layer: [rows][2][Hkv][D] in the KV dtype
   int32_t mode;
+  int32_t layer0;          // the launch covers layers [layer0, layer0 + gridDim.y)
 };
-cudaError_t launch_move(const MoveParams& p, const Mover* movers, int64_t count, cudaStream_t s);
+cudaError_t launch_move(const MoveParams& p, const Mover* movers, int64_t count, int layers, cudaStream_t s);
 
 // s[b][pos] += (sum over KV heads of acc at the slot holding pos) / (L * Hq);
 // slots follow the attention page order (T0, T1, then T2 page lists).
