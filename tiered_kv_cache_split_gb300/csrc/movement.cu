@@ -177,11 +177,14 @@ __global__ void __launch_bounds__(kMoveThreads) move_kernel(const __grid_constan
   const int st = p.mode == MOVE_SCATTER ? -1 : mv.src_tier;  // -1: the staging rows
   const int dt = p.mode == MOVE_GATHER ? -1 : mv.dst_tier;
 
+  // staging row of this (mover, layer): one per mover when the launch covers one
+  // layer, one per (mover, layer) when it covers several
+  const int trow = mv.temp_row * static_cast<int>(gridDim.y) + static_cast<int>(blockIdx.y);
   if (st != 2 && dt != 2) {  // full precision -> full precision
     for (int j = tid; j < nchunk; j += kMoveThreads) {
       const int hk = j / cpr, c = j % cpr;
-      const uint4 v = *reinterpret_cast<const uint4*>(full_chunk(p, st, mv.src_loc, mv.temp_row, l, hk, c, row_bytes));
-      *reinterpret_cast<uint4*>(full_chunk(p, dt, mv.dst_loc, mv.temp_row, l, hk, c, row_bytes)) = v;
+      const uint4 v = *reinterpret_cast<const uint4*>(full_chunk(p, st, mv.src_loc, trow, l, hk, c, row_bytes));
+      *reinterpret_cast<uint4*>(full_chunk(p, dt, mv.dst_loc, trow, l, hk, c, row_bytes)) = v;
     }
     return;
   }
@@ -217,7 +220,7 @@ __global__ void __launch_bounds__(kMoveThreads) move_kernel(const __grid_constan
           f[q] = __fmul_rn(static_cast<float>(static_cast<int8_t>((word >> (8 * q)) & 0xffu)), scale);
         out = make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]), __float_as_uint(f[3]));
       }
-      *reinterpret_cast<uint4*>(full_chunk(p, dt, mv.dst_loc, mv.temp_row, l, hk, c, row_bytes)) = out;
+      *reinterpret_cast<uint4*>(full_chunk(p, dt, mv.dst_loc, trow, l, hk, c, row_bytes)) = out;
     }
     return;
   }
@@ -227,7 +230,7 @@ __global__ void __launch_bounds__(kMoveThreads) move_kernel(const __grid_constan
   for (int j = tid; j < nchunk; j += kMoveThreads) {
     const int hk = j / cpr, c = j % cpr;
     const int h = hk >> 1, kv = hk & 1;
-    const uint4 v = *reinterpret_cast<const uint4*>(full_chunk(p, st, mv.src_loc, mv.temp_row, l, hk, c, row_bytes));
+    const uint4 v = *reinterpret_cast<const uint4*>(full_chunk(p, st, mv.src_loc, trow, l, hk, c, row_bytes));
     float* dst = row_s + kv * HD + h * p.D + c * epc;
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
     if (esz == 2) {
