@@ -119,15 +119,21 @@ typedef struct {
                                   last CTA end, %globaltimer (TKV_FLAG_TIMING; last 4096 launches) */
 } tkv_stats;
 
-/* Device and pinned-host bytes tkv_create needs for this configuration. */
+/* Device and pinned-host bytes tkv_create needs for this configuration: the
+ * HBM tier and staging (T0 pool, two T1/T2 staging slots, metadata) on the
+ * device, the T1 and T2 pools in pinned host memory (Methodology 1; the
+ * Problem statement's ~800 MB per 2,000-token chain is what the tiers split).
+ * Errors: TKV_ERR_INVALID_ARG for an invalid configuration (message says why). */
 TKV_API tkv_status tkv_workspace_size(const tkv_config* cfg, size_t* dev_bytes, size_t* pinned_bytes);
 
-/* Build a handle over caller-owned memory. dev_ws: device memory of at least
+/* Build a handle over caller-owned memory (no allocation inside the library
+ * beyond host bookkeeping). dev_ws: device memory of at least
  * dev_bytes (256-byte aligned); pinned_ws: page-locked host memory of at
  * least pinned_bytes (from cudaHostAlloc / pin_memory). The current CUDA
  * device must be the one that owns dev_ws. */
 TKV_API tkv_status tkv_create(const tkv_config* cfg, void* dev_ws, size_t dev_bytes, void* pinned_ws,
                       size_t pinned_bytes, tkv_stream compute, tkv_stream copy, tkv_handle* out);
+/* Release the handle's events and bookkeeping (the caller frees the memory). */
 TKV_API tkv_status tkv_destroy(tkv_handle h);
 
 /* Prefill: append n_tokens positions (device k, v [L][n][Hkv][d]) to sequence
@@ -138,15 +144,19 @@ TKV_API tkv_status tkv_append(tkv_handle h, int32_t seq, const void* k, const vo
                       int32_t is_prompt);
 
 /* One decode step for every sequence (device pointers, layouts above):
- * append each new token to T0, prefetch T1 and T2 of each layer on the copy
- * stream, attend over T0 + T1 + T2 (T3 absent) with the score update fused in,
- * fold the step's score increments into s, and reassign tiers when the step
- * count reaches a multiple of Delta. */
+ * append each new token to T0 (Methodology 1: the recent window is in T0),
+ * prefetch T1 and T2 of each layer on the copy stream (Methodology 1, 4),
+ * attend over T0 + T1 + T2 with T3 absent (Methodology 3) with the score
+ * update of Methodology 2 fused in, fold the step's score increments into s,
+ * and reassign tiers when the step count reaches a multiple of Delta
+ * (Methodology 4). Errors: TKV_ERR_CAPACITY when a sequence or pool is full
+ * (state unchanged); TKV_ERR_CUDA marks the handle broken. */
 TKV_API tkv_status tkv_decode_step(tkv_handle h, const void* q, const void* k_new, const void* v_new,
                            void* out);
 
-/* The same step with HOST buffers: copies q, k_new, v_new in and out back,
- * inside the call; returns once out holds the result. */
+/* The same step (as tkv_decode_step) with HOST buffers: copies q, k_new, v_new
+ * in and out back inside the call; returns once out holds the result. Pinned
+ * host buffers make the copies asynchronous. */
 TKV_API tkv_status tkv_decode_step_host(tkv_handle h, const void* q, const void* k_new, const void* v_new,
                                 void* out);
 
@@ -155,13 +165,20 @@ TKV_API tkv_status tkv_decode_step_host(tkv_handle h, const void* q, const void*
 TKV_API tkv_status tkv_reclassify(tkv_handle h);
 
 /* Enqueue the copy of layer `layer`'s T1 pages and T2 codes into staging slot
- * `slot` (0 or 1) on the copy stream. decode_step calls this itself. */
+ * `slot` (0 or 1) on the copy stream: T1 is prefetched to the GPU before each
+ * attention step (Methodology 1), asynchronously (Methodology 4).
+ * decode_step calls this itself. Errors: TKV_ERR_INVALID_ARG for a bad layer
+ * or slot. */
 TKV_API tkv_status tkv_prefetch(tkv_handle h, int32_t layer, int32_t slot);
 
-/* Wait for all enqueued work; reports a device-side timeout flag. */
+/* Wait for all enqueued work; reports a device-side timeout flag
+ * (TKV_ERR_TIMEOUT). Library plumbing: the paper has no counterpart. */
 TKV_API tkv_status tkv_synchronize(tkv_handle h);
 
-/* Introspection and test hooks (host buffers; each synchronises). */
+/* Introspection and test hooks (host buffers; each synchronises). The scores
+ * are the s_i of Methodology 2, the tiers those of Methodology 1; page tables
+ * follow this library's slot rule (the paper fixes none). Errors:
+ * TKV_ERR_INVALID_ARG for a bad sequence, position or tier. */
 TKV_API tkv_status tkv_num_sequences(tkv_handle h, int32_t* n);
 TKV_API tkv_status tkv_seq_len(tkv_handle h, int32_t seq, int64_t* n_tokens);
 TKV_API tkv_status tkv_get_scores(tkv_handle h, int32_t seq, double* host_out, int64_t n);
@@ -177,7 +194,8 @@ TKV_API tkv_status tkv_get_page_table(tkv_handle h, int32_t seq, int32_t tier, i
 /* 8-bit codes of a T2 position: codes [L][2][Hkv][d] (K then V), scales
  * [L][2] float32 (per token) or [L][2][Hkv] float16 (per token and head). */
 TKV_API tkv_status tkv_get_t2_row(tkv_handle h, int32_t seq, int64_t pos, int8_t* codes, void* scales);
-/* Values held by a T0 or T1 position: k, v [L][Hkv][d] in the KV dtype. */
+/* Values held by a T0 or T1 position: k, v [L][Hkv][d] in the KV dtype, the
+ * full-precision values Proposition 1 relies on (Methodology 3). */
 TKV_API tkv_status tkv_get_kv_row(tkv_handle h, int32_t seq, int64_t pos, void* k, void* v);
 TKV_API tkv_status tkv_get_stats(tkv_handle h, tkv_stats* out);
 TKV_API tkv_status tkv_reset_stats(tkv_handle h);
