@@ -39,3 +39,29 @@ def test_workload_shapes():
     assert len(lens) == 32 and min(lens) >= 1024 and max(lens) <= 8192
     assert BATCH32.queries(1).shape == (32, 28, 28, 128)
     assert TINY.spike_positions(0).numel() == 16
+
+
+def test_delayed_spikes_stay_silent_until_their_group_activates():
+    # The MHA configuration's delayed spikes: a spike key carries 6 sqrt(d) along its
+    # group's direction e_j; a query has no component along any e_j until the
+    # group's first spike is 500 positions behind it, and exactly 1 after.
+    from synth import MHA16K
+    w = MHA16K.replace(n_layers=1, n_q_heads=2, n_kv_heads=2, batch=1, context=("fixed", 1200),
+                       prompt_len=64, key_scale=("delayed_spikes", 0.02, 6.0, 300, 4), n_steps=8)
+    grp, first = w.spike_groups(0)
+    assert grp.numel() > 0 and first.numel() == 4
+    e = __import__("synth.workloads", fromlist=["_spike_dirs"])._spike_dirs(w, 0, 0)  # [groups, d]
+    np.testing.assert_allclose((e @ e.T).numpy(), np.eye(4), atol=1e-10)
+    q = w.queries(1)[0, 0, 0].to(torch.float64)            # position 1200: step 1
+    pos = w.step_positions(1)[0]
+    comp = (e @ q).numpy()
+    active = (first + 300 <= pos).numpy()
+    # the stored query is bf16: its rounding (2^-9 relative per element) bounds the error
+    np.testing.assert_allclose(comp[active], 1.0, atol=2e-2)
+    np.testing.assert_allclose(comp[~active], 0.0, atol=2e-2)
+    # spike keys point along their group's direction, 6 sqrt(d) long beyond the noise
+    spikes = w.spike_positions(0)
+    k = w.kv("k", 0, 0, 0, w.total_len(0))[0].to(torch.float64)   # head 0, [n, d]
+    j = int(grp[0])
+    along = float(k[int(spikes[0])] @ e[j])
+    assert abs(along - 6.0 * np.sqrt(w.head_dim)) < 5.0   # noise adds N(0, 1) along e_j
