@@ -101,3 +101,30 @@ def test_long_context_shape_without_t2(t0):
     for b in range(w.batch):
         counts = np.bincount(oc.seqs[b].tier, minlength=4)
         assert counts[2] == 0 and counts[0] > 0 and counts[1] > 0 and counts[3] > 0, counts
+
+
+def test_reassignment_that_does_not_fit_changes_nothing():
+    # Failure on the host, no GPU fault: a T1 pool of two pages cannot take the
+    # tokens a reassignment sends there. The call must fail with CAPACITY and
+    # leave tiers, page tables and scores as they were, and the handle usable.
+    from tiered_kv_cache_split_gb300 import TieredKVCache, _lib as L
+    torch.cuda.set_device(DEV)
+    w = TINY
+    cache = TieredKVCache.from_workload(w, t1_pages=2)
+    prefill_cache(cache, w, DEV)
+    cache.set_scores(0, w.synthetic_scores(0, w.context_lens()[0]).numpy())
+
+    def snapshot():
+        return cache.tiers(0).copy(), [cache.page_table(0, t) for t in range(3)], cache.scores(0).copy()
+
+    before = snapshot()
+    with pytest.raises(L.TkvError) as err:
+        cache.reclassify()
+    assert err.value.status == L.ERR_CAPACITY
+    after = snapshot()
+    assert np.array_equal(before[0], after[0]) and np.array_equal(before[2], after[2])
+    for (p0, m0, q0), (p1, m1, q1) in zip(before[1], after[1]):
+        assert np.array_equal(p0, p1) and np.array_equal(m0, m1) and np.array_equal(q0, q1)
+    out = cache.decode_step(w.queries(1).to(DEV), w.kv_new("k", 1).to(DEV), w.kv_new("v", 1).to(DEV))
+    assert bool(torch.isfinite(out.float()).all())
+    cache.close()
