@@ -14,6 +14,11 @@ Per step t (steps count from 1), following "Not All Thoughts Need HBM":
 Values are held in float64 exactly as each tier stores them: the bf16 or f32
 input for T0/T1, code * scale for T2, and storage(float32(code * scale)) for a
 token promoted out of T2 (full precision is gone once a token was quantised).
+Pins: a hand-worked one-layer, two-head, two-step fixture (the new token is
+appended before attention and attended by its own query; scores accumulate the
+head-averaged weights), the increments of a step summing to 1, Proposition 1
+(a T0/T1 split changes outputs by at most 1e-12), and tier / page-table
+invariants over whole runs.
 """
 from __future__ import annotations
 

@@ -112,3 +112,14 @@ def test_protected_larger_than_t0_budget_takes_from_t3_first():
     # filled and only the rest is evicted.
     new = classify(s, old, 6, 0, 0, 4, 2, 1)
     assert new.tolist() == [0, 0, 0, 0, 0, 0, 3, 2, 1, 1]
+
+
+def test_protected_sets_by_hand(golden_dir):
+    g = json.load(open(os.path.join(golden_dir, "protected_sets.json")))
+    for c in g["cases"]:
+        P = protected_mask(c["N"], c["prompt_len"], c["n_sink"], c["recent_window"])
+        assert np.nonzero(P)[0].tolist() == c["protected"], c["name"]
+    x = g["classify_with_sinks_beyond_prompt"]
+    new = classify(x["scores"], x["old_tier"], x["prompt_len"], x["n_sink"], x["recent_window"],
+                   x["n0"], x["n1"], x["n2"])
+    assert new.tolist() == x["new_tier"]

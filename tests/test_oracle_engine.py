@@ -92,3 +92,25 @@ def test_kv_size_of_a_2000_token_chain_is_about_800_mb():
     # Problem statement: a 2,000-token chain on a 7B model holds ~800 MB of KV.
     # 28 layers x 28 KV heads x 128 dims x (K, V) x 2 bytes x 2,000 tokens:
     assert 2000 * 28 * 28 * 128 * 2 * 2 == 802_816_000
+
+
+def test_one_layer_two_steps_by_hand(golden_dir):
+    """The new token is appended before attention (its own query sees it) and
+    scores accumulate the head- and layer-averaged weights across steps."""
+    import json
+    import os
+    g = json.load(open(os.path.join(golden_dir, "decode_step_1layer.json")))
+    oc = OracleCache(g["n_layers"], g["n_q_heads"], g["n_kv_heads"], g["head_dim"], "f32", n_sink=0,
+                     recent_window=0, budget_mode="count", budgets=(100, 0, 0, 0), reclassify_interval=1000)
+    k = np.array(g["prompt_k"], dtype=np.float64)[None]     # [L, n, Hkv, d]
+    v = np.array(g["prompt_v"], dtype=np.float64)[None]
+    oc.append(0, k, v, True)
+    for st in g["steps"]:
+        q = np.array(st["q"], dtype=np.float64)[None, None]           # [B, L, Hq, d]
+        kn = np.array(st["k_new"], dtype=np.float64)[None, None]      # [B, L, Hkv, d]
+        vn = np.array(st["v_new"], dtype=np.float64)[None, None]
+        out, deltas = oc.decode_step(q, kn, vn)
+        np.testing.assert_allclose(out[0, 0], np.array(st["out"]), rtol=0, atol=1e-15)
+        np.testing.assert_allclose(oc.seqs[0].s, np.array(st["s"]), rtol=0, atol=1e-15)
+        R, ds = deltas[0]
+        assert R.tolist() == list(range(oc.seqs[0].N))
