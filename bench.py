@@ -163,7 +163,8 @@ def run_gpu(args):
     total_steps = untimed + K + e2e_untimed + K
     w = w.replace(n_steps=total_steps + 1)
 
-    cache = TieredKVCache.from_workload(w, timing=True, split_pages=args.split_pages)
+    cache = TieredKVCache.from_workload(w, timing=True, split_pages=args.split_pages, host_tiers=args.host_tiers,
+                                        layers_per_launch=args.layers_per_launch)
     t0 = time.time()
     for b in range(w.batch):
         n, P = w.context_lens()[b], w.prompt_lens()[b]
@@ -373,6 +374,10 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--layers", type=int, default=0, help="override the layer count (profiling a small case)")
     ap.add_argument("--split-pages", type=int, default=0, help="pages per attention CTA (0: planned)")
+    ap.add_argument("--host-tiers", choices=["stream", "mirror", "zerocopy"], default="stream",
+                    help="T1/T2 reach attention by per-step copies (stream), a device mirror updated at "
+                         "reassignment (mirror), or in place from pinned host memory (zerocopy)")
+    ap.add_argument("--layers-per-launch", type=int, default=0, help="layers per attention launch (0: auto)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

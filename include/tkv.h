@@ -73,6 +73,17 @@ enum { TKV_SCALE_F32 = 0, TKV_SCALE_F16 = 1 };
 enum { TKV_T2_ATTEND = 0, TKV_T2_MASK = 1 };
 enum { TKV_T0 = 0, TKV_T1 = 1, TKV_T2 = 2, TKV_T3 = 3 };
 enum { TKV_FLAG_TIMING = 1 }; /* record CUDA events around attention, prefetch, reclassify */
+/* Where attention finds the host tiers T1 and T2 (Methodology 1 and 4):
+ *   STREAM   every step copies each layer group's used T1 / T2 range from the pinned host
+ *            pools into a two-slot device staging ring on the copy stream, overlapped with
+ *            the previous group's attention (T1 is prefetched before each attention step);
+ *   MIRROR   device-resident copies of the T1 / T2 pools are kept in step with the host
+ *            pools: only tokens whose tier changes cross the host link, at reassignment
+ *            (the differential transfer of newly promoted tokens); no per-step copies;
+ *   ZEROCOPY attention reads T1 / T2 pages in place from the pinned host pools through
+ *            device-mapped pointers (no staging copy, no HBM write of staged pages).
+ * The three give bitwise identical attention outputs (the same pages in the same order). */
+enum { TKV_HOST_TIERS_STREAM = 0, TKV_HOST_TIERS_MIRROR = 1, TKV_HOST_TIERS_ZEROCOPY = 2 };
 
 /* Configuration. Budgets (Methodology 1): in PERCENT mode budget[k] are the
  * integer percentages of T0..T3 (n_k = floor(budget[k] * N / 100) for k = 1..3,
@@ -98,11 +109,15 @@ typedef struct {
                                                          0 = one per position (always enough) */
   int32_t split_pages;                                /* pages per attention CTA; 0 = auto */
   int32_t flags;                                      /* TKV_FLAG_* */
+  int32_t host_tiers;                                 /* TKV_HOST_TIERS_* */
+  int32_t layers_per_launch;                          /* layers one attention launch covers (and one
+                                                         prefetch copies in STREAM mode); 0 = auto:
+                                                         the largest divisor of n_layers up to 7 */
 } tkv_config;
 
 typedef struct {
   int64_t steps, reclassifies, movers;
-  int64_t attn_launches;       /* attention kernel launches (one per layer per step) */
+  int64_t attn_launches;       /* attention kernel launches (one per layer group per step) */
   int64_t attn_bytes;          /* algorithmic KV bytes the attention kernels read */
   int64_t prefetch_bytes;      /* T1 + T2 bytes copied host -> device by prefetch */
   int64_t h2d_move_bytes;      /* bytes moved host -> device at reclassify */
@@ -117,6 +132,10 @@ typedef struct {
   int64_t kernel_launches;     /* kernels this handle launched (steps, reclassify, prefill) */
   double attn_span_ms;         /* summed device span of the attention launches: first CTA start to
                                   last CTA end, %globaltimer (TKV_FLAG_TIMING; last 4096 launches) */
+  int64_t attn_layers;         /* layers attended (attn_launches x layers per launch) */
+  double classify_ms;          /* reassignment phases, host wall time (TKV_FLAG_TIMING): classifier */
+  double allocate_ms;          /*   host slot allocator                                           */
+  double move_ms;              /*   data movement kernels and metadata upload                     */
 } tkv_stats;
 
 /* Device and pinned-host bytes tkv_create needs for this configuration: the
@@ -174,6 +193,14 @@ TKV_API tkv_status tkv_prefetch(tkv_handle h, int32_t layer, int32_t slot);
 /* Wait for all enqueued work; reports a device-side timeout flag
  * (TKV_ERR_TIMEOUT). Library plumbing: the paper has no counterpart. */
 TKV_API tkv_status tkv_synchronize(tkv_handle h);
+
+/* Test hook for the bounded device waits (the paper has no counterpart): the
+ * next attention launch of h withholds the first page copy of one CTA, and from
+ * now on h's device waits give up after wait_limit_ns (1 ms .. 2 s) instead of
+ * 2 s. The waiting warp gives up, the CTA lands every copy still in flight and
+ * publishes an empty partial, and the next synchronising call returns
+ * TKV_ERR_TIMEOUT and marks h broken. No kernel traps or hangs. */
+TKV_API tkv_status tkv_test_stall_next_attention(tkv_handle h, uint64_t wait_limit_ns);
 
 /* Introspection and test hooks (host buffers; each synchronises). The scores
  * are the s_i of Methodology 2, the tiers those of Methodology 1; page tables
@@ -243,16 +270,27 @@ TKV_API tkv_status tkv_paged_attention(int32_t batch, int32_t n_q_heads, int32_t
  *   Set-up: the first call on a device looks up the array's device address
  *   (cudaGetSymbolAddress, with that device current); make that first call
  *   before any stream capture.
+ *   The cached address is valid for the device's current context only: after
+ *   cudaDeviceReset the library must be reloaded.
  *   Sharing: every call on a device uses the same array and the array keeps
  *   the last call's contents; each call clears the parts that must start at
  *   zero. Calls that overlap on the GPU (other streams, other threads) race on
- *   it: serialise them. */
+ *   it: serialise them.
+ *   Status: the kernels' error word sits in that array, out of the caller's
+ *   reach; read it with tkv_paged_attention_noalloc_status. */
 TKV_API tkv_status tkv_paged_attention_noalloc(int32_t batch, int32_t n_q_heads, int32_t n_kv_heads,
                                                int32_t head_dim, int32_t kv_dtype, const void* q,
                                                const void* pool, const int32_t* page_table,
                                                const uint32_t* slot_mask, const int32_t* page_counts,
                                                int32_t max_pages, void* out, float* alpha_sum,
                                                tkv_stream stream);
+/* Device status word of the last allocation-free call on the current device:
+ * after the work enqueued on `stream` so far, *host_out = 0 (no error), 1 (a
+ * bounded device wait gave up; that call's output is not valid) or 2 (an
+ * internal index check failed). Copies 4 bytes to the host and synchronises
+ * `stream`; allocates nothing. TKV_ERR_STATE if no allocation-free call has
+ * run on this device. The paper has no counterpart. */
+TKV_API tkv_status tkv_paged_attention_noalloc_status(int32_t* host_out, tkv_stream stream);
 
 /* Tier reassignment of Methodology 1 for B sequences (device buffers):
  *   scores   double [B][stride], old_tier uint8 [B][stride], new_tier uint8 [B][stride]

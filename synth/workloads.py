@@ -290,5 +290,18 @@ def long128k(t0: int) -> Workload:
         prompt_len=0, key_scale=("lognormal", 1.0), n_steps=64, seed=15)
 
 
+def batch32_budget(name: str, budgets: tuple) -> Workload:
+    """The batch-32 serving shape under another tier budget (the pages'
+    experimental axes, measured here as system cost): full cache, eviction
+    without offload, and the share of HBM at fixed eviction."""
+    return BATCH32.replace(name=name, budgets=budgets)
+
+
+BUDGET_VARIANTS = [batch32_budget("batch32_full", (100, 0, 0, 0)),
+                   batch32_budget("batch32_evict50", (50, 0, 0, 50)),
+                   batch32_budget("batch32_hbm30", (30, 50, 10, 10)),
+                   batch32_budget("batch32_hbm50", (50, 30, 10, 10)),
+                   batch32_budget("batch32_hbm70", (70, 10, 10, 10))]
+
 WORKLOADS = {w.name: w for w in (TINY, CHAIN7B, BATCH32, MHA16K,
-                                 long128k(25), long128k(50), long128k(75))}
+                                 long128k(25), long128k(50), long128k(75), *BUDGET_VARIANTS)}

@@ -63,12 +63,14 @@ def oracle_t2_codes(w, b, pos):
     return out
 
 
-def layer_attention(w, b, layer, q_bl, tiers, n_total):
+def layer_attention(w, b, layer, q_bl, tiers, n_total, gen_device="cpu"):
     """Oracle outputs [Hq, d] and alphas [Hq, |R|] of all heads of one (request,
     layer) over the retained set, T2 rows dequantised from the oracle's codes
-    (valid while no token has been promoted out of T2)."""
-    K = w.kv("k", b, layer, 0, n_total).float().numpy().astype(np.float64).transpose(1, 0, 2)
-    V = w.kv("v", b, layer, 0, n_total).float().numpy().astype(np.float64).transpose(1, 0, 2)
+    (valid while no token has been promoted out of T2). The seeded inputs may be
+    regenerated on a CUDA device (bit-identical to the CPU generator) and are
+    brought back to the CPU before any oracle arithmetic."""
+    K = w.kv("k", b, layer, 0, n_total, gen_device).cpu().float().numpy().astype(np.float64).transpose(1, 0, 2)
+    V = w.kv("v", b, layer, 0, n_total, gen_device).cpu().float().numpy().astype(np.float64).transpose(1, 0, 2)
     t2 = np.nonzero(tiers == 2)[0]
     if t2.size:
         for X in (K, V):

@@ -92,3 +92,35 @@ def test_stateless_shape_checks(lib):
     assert lib.tkv_paged_attention_scratch_size(2, 30, 4, 128, 100, ctypes.byref(n)) == L.ERR_INVALID_ARG
     assert lib.tkv_classify_scratch_size(4, 1000, ctypes.byref(n)) == L.OK and n.value >= 32000
     assert lib.tkv_quantize_rows(None, 1, 1, 8, None, None, 0, None) == L.ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("mode", [0, 1, 2])
+def test_workspace_by_host_tier_mode(lib, mode):
+    """STREAM holds a two-slot staging ring of layer groups, MIRROR a device copy
+    of every layer of T1 / T2, ZEROCOPY neither; the pinned pools are the same."""
+    d, p = ctypes.c_size_t(), ctypes.c_size_t()
+    base_d, base_p = ctypes.c_size_t(), ctypes.c_size_t()
+    assert lib.tkv_workspace_size(ctypes.byref(_cfg(host_tiers=2, layers_per_launch=4)), ctypes.byref(base_d),
+                                  ctypes.byref(base_p)) == L.OK
+    assert lib.tkv_workspace_size(ctypes.byref(_cfg(host_tiers=mode, layers_per_launch=4)), ctypes.byref(d),
+                                  ctypes.byref(p)) == L.OK
+    assert p.value == base_p.value
+    t1_layer = (32 * (40 * 8448 // 100 // 16 + 2)) * 4 * 2 * 16 * 128 * 2   # about one layer of the T1 pool
+    if mode == 0:
+        assert 2 * 4 * 0.9 * t1_layer < d.value - base_d.value < 2 * 4 * 1.5 * t1_layer
+    elif mode == 1:
+        assert 28 * 0.9 * t1_layer < d.value - base_d.value < 28 * 1.5 * t1_layer
+    else:
+        assert d.value == base_d.value
+
+
+@pytest.mark.parametrize("field,value", [("host_tiers", 3), ("layers_per_launch", -1)])
+def test_invalid_mode_fields_are_rejected(lib, field, value):
+    d, p = ctypes.c_size_t(), ctypes.c_size_t()
+    assert lib.tkv_workspace_size(ctypes.byref(_cfg(**{field: value})), ctypes.byref(d), ctypes.byref(p)) == L.ERR_INVALID_ARG
+    assert field.encode() in lib.tkv_last_error(None)
+
+
+def test_test_hook_and_status_calls_fail_cleanly_without_a_handle(lib):
+    assert lib.tkv_test_stall_next_attention(None, 5_000_000) == L.ERR_INVALID_ARG
+    assert lib.tkv_paged_attention_noalloc_status(None, None) == L.ERR_INVALID_ARG

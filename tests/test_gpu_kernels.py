@@ -139,6 +139,40 @@ def test_paged_attention_and_fused_alpha(dtype, G, d):
             assert np.all(alpha[b, h, rest] == 0)
 
 
+@pytest.mark.parametrize("dtype,G", [("bf16", 8), ("f32", 4)])
+def test_paged_attention_with_more_than_64_chunks_per_sequence(dtype, G):
+    """One long sequence on one KV head is split into up to 128 chunks: the
+    epilogue's global (M, Z) then reduces partials beyond its first 64 per lane
+    pair, and the output merge runs over every chunk."""
+    from tiered_kv_cache_split_gb300 import paged_attention
+    rng = np.random.default_rng(77 + G)
+    B, Hkv, d = 1, 1, 128
+    Hq = Hkv * G
+    counts = [1200]
+    pool, table, masks = _random_pool(rng, B, Hkv, d, counts, dtype)
+    q = rng.standard_normal((B, Hq, d)).astype(np.float32)
+    tq = torch.from_numpy(q).to(torch.bfloat16 if dtype == "bf16" else torch.float32)
+    q = tq.float().numpy()
+    pool32 = pool.float().numpy()
+    alpha = torch.zeros((B, Hkv, counts[0] * 16), dtype=torch.float32, device=DEV)
+    out = paged_attention(tq.to(DEV), pool.to(DEV), torch.from_numpy(table).to(DEV),
+                          torch.from_numpy(masks.view(np.int32)).to(DEV), counts, alpha_sum=alpha)
+    out = out.float().cpu().numpy()
+    alpha = alpha.cpu().numpy()
+    K, V, slots = [], [], []
+    for k, p in enumerate(table[0, :counts[0]]):
+        for j in range(16):
+            if (masks[p] >> j) & 1:
+                K.append(pool32[p, :, 0, j])
+                V.append(pool32[p, :, 1, j])
+                slots.append(16 * k + j)
+    ref, a = decode_attention(q[0], np.array(K), np.array(V))
+    assert np.max(np.abs(out[0] - ref)) <= (OUT_ATOL if dtype == "bf16" else 1e-4)
+    want = a.sum(0)
+    got = alpha[0, 0, slots]
+    assert np.all(np.abs(got - want) <= SCORE_RTOL * want + SCORE_ATOL)
+
+
 def test_proposition_1_bitwise_on_the_gpu():
     """Attention over T0 + prefetched T1 gives the same bits as the same pages,
     in the same order, all resident in HBM (same kernel, same fixed chunking)."""

@@ -65,6 +65,10 @@ def test_noalloc_matches_caller_scratch_on_two_calls_in_a_row():
         assert torch.max(torch.abs(out.float() - ref.float())).item() <= 2e-2, f"call {call}"
         want, got = a_ref.cpu().numpy(), a.cpu().numpy()
         assert np.all(np.abs(got - want) <= SCORE_RTOL * np.abs(want) + SCORE_ATOL), f"call {call}"
+        status = ctypes.c_int32(-1)
+        L.check(lib.tkv_paged_attention_noalloc_status(ctypes.byref(status),
+                                                       torch.cuda.current_stream(DEV).cuda_stream))
+        assert status.value == 0, f"call {call}: device status {status.value}"
 
 
 def test_noalloc_refuses_shapes_beyond_its_scratch():

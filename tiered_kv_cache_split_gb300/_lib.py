@@ -17,6 +17,7 @@ BUDGET_PERCENT, BUDGET_COUNT = 0, 1
 SCALE_PER_TOKEN, SCALE_PER_TOKEN_HEAD = 0, 1
 SCALE_F32, SCALE_F16 = 0, 1
 T2_ATTEND, T2_MASK = 0, 1
+HOST_TIERS = {"stream": 0, "mirror": 1, "zerocopy": 2}
 FLAG_TIMING = 1
 
 c_i32, c_i64, c_sz, c_vp = ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t, ctypes.c_void_p
@@ -30,6 +31,7 @@ class Config(ctypes.Structure):
         ("budget", c_i64 * 4), ("reclassify_interval", c_i32), ("t2_scale_gran", c_i32),
         ("t2_scale_dtype", c_i32), ("t2_mode", c_i32), ("t0_pages", c_i64), ("t1_pages", c_i64),
         ("t2_pages", c_i64), ("max_staged_movers", c_i64), ("split_pages", c_i32), ("flags", c_i32),
+        ("host_tiers", c_i32), ("layers_per_launch", c_i32),
     ]
 
 
@@ -40,7 +42,8 @@ class Stats(ctypes.Structure):
         ("d2h_move_bytes", c_i64), ("tier_counts", c_i64 * 4), ("attn_ms", ctypes.c_double),
         ("combine_ms", ctypes.c_double),
         ("prefetch_ms", ctypes.c_double), ("reclassify_ms", ctypes.c_double),
-        ("kernel_launches", c_i64), ("attn_span_ms", ctypes.c_double),
+        ("kernel_launches", c_i64), ("attn_span_ms", ctypes.c_double), ("attn_layers", c_i64),
+        ("classify_ms", ctypes.c_double), ("allocate_ms", ctypes.c_double), ("move_ms", ctypes.c_double),
     ]
 
 
@@ -76,6 +79,8 @@ _SIGS = {
                             c_vp, c_vp, c_vp, c_sz, c_vp],
     "tkv_paged_attention_noalloc": [c_i32, c_i32, c_i32, c_i32, c_i32, c_vp, c_vp, c_vp, c_vp, c_vp, c_i32,
                                     c_vp, c_vp, c_vp],
+    "tkv_paged_attention_noalloc_status": [ctypes.POINTER(c_i32), c_vp],
+    "tkv_test_stall_next_attention": [c_vp, ctypes.c_uint64],
     "tkv_classify_scratch_size": [c_i32, c_i64, ctypes.POINTER(c_sz)],
     "tkv_classify": [c_i32, c_vp, c_vp, c_vp, c_i64, c_vp, c_i32, c_i32, c_vp, c_sz, c_vp],
     "tkv_quantize_rows": [c_vp, c_i32, c_i64, c_i32, c_vp, c_vp, c_i32, c_vp],

@@ -28,7 +28,8 @@ class TieredKVCache:
                  max_tokens=4096, n_sink=4, recent_window=128, budget_mode="percent",
                  budgets=(50, 30, 10, 10), reclassify_interval=64, t2_scale_gran="token",
                  t2_scale_dtype="f32", t2_mode="attend", t0_pages=0, t1_pages=0, t2_pages=0,
-                 max_staged_movers=0, split_pages=0, timing=False, device="cuda"):
+                 max_staged_movers=0, split_pages=0, timing=False, host_tiers="stream",
+                 layers_per_launch=0, device="cuda"):
         self.lib = L.load()
         self.device = torch.device(device)
         self.kv_dtype = kv_dtype
@@ -53,6 +54,8 @@ class TieredKVCache:
         cfg.max_staged_movers = max_staged_movers
         cfg.split_pages = split_pages
         cfg.flags = L.FLAG_TIMING if timing else 0
+        cfg.host_tiers = L.HOST_TIERS[host_tiers]
+        cfg.layers_per_launch = layers_per_launch
         self.cfg = cfg
         dev_b, pin_b = ctypes.c_size_t(), ctypes.c_size_t()
         L.check(self.lib.tkv_workspace_size(ctypes.byref(cfg), ctypes.byref(dev_b), ctypes.byref(pin_b)))
@@ -137,6 +140,11 @@ class TieredKVCache:
 
     def synchronize(self):
         self._check(self.lib.tkv_synchronize(self.h))
+
+    def test_stall_next_attention(self, wait_limit_ns: int):
+        """Test hook: the next attention launch withholds one page copy, so a
+        bounded device wait (limit wait_limit_ns) runs out; see tkv.h."""
+        self._check(self.lib.tkv_test_stall_next_attention(self.h, int(wait_limit_ns)))
 
     def num_sequences(self) -> int:
         n = ctypes.c_int32()

@@ -85,13 +85,14 @@ __device__ __forceinline__ uint64_t global_ns() {
   return t;
 }
 
-// Wait for phase `parity` of an mbarrier; gives up after about two seconds.
-__device__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+// Wait for phase `parity` of an mbarrier; gives up after limit_ns nanoseconds
+// (or 2^30 polls, whichever comes first).
+__device__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
   if (mbar_try(bar, parity)) return true;
   const uint64_t t0 = global_ns();
   for (uint32_t it = 1; it < (1u << 30); ++it) {
     if (mbar_try(bar, parity)) return true;
-    if ((it & 1023u) == 0 && global_ns() - t0 > 2000000000ull) return false;
+    if ((it & 63u) == 0 && global_ns() - t0 > limit_ns) return false;
   }
   return false;
 }
@@ -206,12 +207,18 @@ __device__ __forceinline__ void page_ref(const AttnParams& p, int b, int k, int&
 
 // What a CTA needs to know about its work item.
 struct Work {
-  int b, kvh, cf, jc, nch, ntot, k0, npg;  // the chunk: pages [k0, k0 + npg) of sequence b
+  int b, kvh, z, cf, jc, nch, ntot, k0, npg;  // the chunk: pages [k0, k0 + npg) of sequence b at layer z
 };
 
-__device__ __forceinline__ Work find_work_at(const AttnParams& p, int chunk, int kvh) {
+// Index of work unit (layer z, chunk, KV head) in the partial buffers.
+__device__ __forceinline__ int64_t unit_index(const AttnParams& p, int z, int chunk, int kvh) {
+  return (static_cast<int64_t>(z) * p.total_chunks + chunk) * p.Hkv + kvh;
+}
+
+__device__ __forceinline__ Work find_work_at(const AttnParams& p, int chunk, int kvh, int z) {
   Work wk;
   wk.kvh = kvh;
+  wk.z = z;
   int b = 0;
   while (b + 1 < p.B && p.chunk_first[b + 1] <= chunk) ++b;
   wk.b = b;
@@ -231,7 +238,15 @@ __device__ __forceinline__ Work find_work_at(const AttnParams& p, int chunk, int
   return wk;
 }
 
-__device__ __forceinline__ Work find_work(const AttnParams& p) { return find_work_at(p, blockIdx.x, blockIdx.y); }
+__device__ __forceinline__ Work find_work(const AttnParams& p) {
+  return find_work_at(p, blockIdx.x, blockIdx.y, blockIdx.z);
+}
+
+// This work unit's spilled logits (k-th page of the sequence at slot (k * G + g) * 16 + row).
+__device__ __forceinline__ float* spill_of(const AttnParams& p, float* spill, const Work& wk) {
+  return spill + wk.z * p.spill_stride_l + static_cast<int64_t>(wk.b) * p.spill_stride_b +
+         static_cast<int64_t>(wk.kvh) * p.spill_stride_h + static_cast<int64_t>(p.page_base[wk.b]) * p.G * kPage;
+}
 
 // Initialises the ring's full and empty barriers (thread 0); a CTA barrier
 // must follow before any thread uses them.
@@ -258,6 +273,10 @@ struct PageCopy {
   unsigned long long scales;
 };
 
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
 // Producer lane: bulk-copy page i of the chunk into ring stage st, completing
 // the stage's "full" barrier with the page's byte count.
 template <typename S>
@@ -274,18 +293,14 @@ __device__ __forceinline__ void issue_page(const PageCopy& c, int st, char* ring
   if (sbytes) bulk_g2s(dst + 2 * S::BLK, reinterpret_cast<const char*>(c.scales), sbytes, bar, policy);
 }
 
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-
 // Per-page word the producer publishes for the consumers: valid-slot bits in
 // the low 16 bits, then the page's source traits, so that the consumers never
 // index the source table.
-constexpr uint32_t kFlagI8 = 1u << 16, kFlagPerHead = 1u << 17;
+constexpr uint32_t kFlagI8 = 1u << 16, kFlagPerHead = 1u << 17, kFlagHost = 1u << 21;
 constexpr int kFlagSwzShift = 18;
-__device__ __forceinline__ uint32_t page_flags(uint32_t valid, bool i8, bool per_head, int swz) {
+__device__ __forceinline__ uint32_t page_flags(uint32_t valid, bool i8, bool per_head, int swz, bool host) {
   return (valid & 0xffffu) | (i8 ? kFlagI8 : 0u) | (per_head ? kFlagPerHead : 0u) |
-         (static_cast<uint32_t>(swz & 7) << kFlagSwzShift);
+         (static_cast<uint32_t>(swz & 7) << kFlagSwzShift) | (host ? kFlagHost : 0u);
 }
 
 // Resolves page i of the chunk (source, pool page, valid mask and traits, copy
@@ -297,15 +312,49 @@ __device__ __forceinline__ void resolve_page(const AttnParams& p, const Work& wk
   const PageSource& ps = p.src[src];
   meta_k[slot] = k;
   const bool i8 = ps.kind == SRC_INT8;
-  meta_f[slot] = page_flags(ps.mask[page], i8, ps.scale_per_head != 0, ps.swz);
+  meta_f[slot] = page_flags(ps.mask[page], i8, ps.scale_per_head != 0, ps.swz, ps.host != 0);
   PageCopy c;
-  c.src = reinterpret_cast<unsigned long long>(ps.base + static_cast<int64_t>(page) * ps.page_bytes +
+  c.src = reinterpret_cast<unsigned long long>(ps.base + wk.z * ps.layer_bytes + static_cast<int64_t>(page) * ps.page_bytes +
                                                static_cast<int64_t>(wk.kvh) * ps.head_bytes) |
-          (i8 ? 1ull : 0ull) | ((i8 && ps.scale_per_head) ? 2ull : 0ull);
-  c.scales = i8 ? reinterpret_cast<unsigned long long>(ps.scales + static_cast<int64_t>(page) * ps.scale_page_bytes +
+          (i8 ? 1ull : 0ull) | ((i8 && ps.scale_per_head) ? 2ull : 0ull) | (ps.host ? 4ull : 0ull);
+  c.scales = i8 ? reinterpret_cast<unsigned long long>(ps.scales + wk.z * ps.scale_layer_bytes +
+                                                       static_cast<int64_t>(page) * ps.scale_page_bytes +
                                                        (ps.scale_per_head ? static_cast<int64_t>(wk.kvh) * 64 : 0))
                 : 0ull;
   desc[slot] = c;
+}
+
+// Producer warp: read a page that sits in pinned host memory into its ring
+// stage with plain 16-byte loads (K block then V block; for an 8-bit page the
+// codes, then its scale record at the stage's scale area). All loads of a
+// batch are issued before any store, so the warp keeps 8 x 512 B in flight over
+// the host link.
+template <typename S>
+__device__ __forceinline__ void load_host_page(const PageCopy& c, char* stage, int lane) {
+  const bool i8 = c.src & 1ull;
+  const uint4* src = reinterpret_cast<const uint4*>(c.src & ~15ull);
+  uint4* dst = reinterpret_cast<uint4*>(stage);
+  const int n = (i8 ? 2 * kPage * (S::ROWB / S::ESZ) : 2 * S::BLK) / 16;
+  constexpr int kBatch = 8;
+  for (int base = 0; base < n; base += 32 * kBatch) {
+    uint4 v[kBatch];
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      const int i = base + j * 32 + lane;
+      if (i < n) v[j] = src[i];
+    }
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      const int i = base + j * 32 + lane;
+      if (i < n) dst[i] = v[j];
+    }
+  }
+  if (i8) {
+    const int sn = ((c.src & 2ull) ? 64 : 128) / 16;
+    if (lane < sn)
+      reinterpret_cast<uint4*>(stage + 2 * S::BLK)[lane] = reinterpret_cast<const uint4*>(c.scales)[lane];
+  }
+  __syncwarp();
 }
 
 // The producer warp's job: resolve the chunk's pages (one lane per page, 32
@@ -323,24 +372,42 @@ __device__ int produce(const AttnParams& p, const Work& wk, int32_t* meta_k, uin
   int pos = 0, issued = 0;
   bool ok = true;  // lane 0: no bounded wait gave up
   auto stage_free = [&](int i) {  // position i's stage has been released by position i - stages
-    return i < kAttnStages || mbar_wait(empty0 + (i % kAttnStages) * 8, ((i / kAttnStages) - 1) & 1);
+    return i < kAttnStages || mbar_wait(empty0 + (i % kAttnStages) * 8, ((i / kAttnStages) - 1) & 1, p.wait_limit_ns);
   };
+  // test hook: the first CTA withholds its first page, so that a consumer's
+  // bounded wait runs out (nothing is in flight for that stage)
+  const bool stall = p.stall_first_page && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0;
   auto resolve = [&](int first_page, int n) {
     if (lane < n) resolve_page(p, wk, first_page + lane, (pos + lane) % kMeta, meta_k, meta_f, desc);
     __syncwarp();
   };
+  // Lane 0 waits for each stage and issues its bulk copy; a page in pinned host
+  // memory is instead read by the whole warp with plain loads (load_host_page)
+  // and its stage completed with a plain arrive.
   auto issue = [&](int n) {
-    if (lane == 0) {
-      for (int j = 0; j < n && ok; ++j) {
-        const int i = pos + j;
-        if (!stage_free(i)) {
+    for (int j = 0; j < n; ++j) {
+      const int i = pos + j;
+      int go = 0;
+      if (lane == 0) go = ok && stage_free(i);
+      go = __shfl_sync(kFull, go, 0);
+      if (!go) {
+        if (lane == 0 && ok) {
           ok = false;
           *abort_flag = 1;
-          break;
         }
-        issue_page<S>(desc[i % kMeta], i % kAttnStages, ring, full0, policy);
-        ++issued;
+        break;
       }
+      const int st = i % kAttnStages;
+      const PageCopy c = desc[i % kMeta];
+      if (c.src & 4ull) {
+        if (!(stall && i == 0)) {
+          load_host_page<S>(c, ring + st * S::STAGE, lane);
+          if (lane == 0) mbar_arrive(full0 + st * 8);
+        }
+      } else if (lane == 0 && !(stall && i == 0)) {
+        issue_page<S>(c, st, ring, full0, policy);
+      }
+      if (lane == 0) ++issued;
     }
     pos += n;
     __syncwarp();
@@ -366,10 +433,12 @@ __device__ int produce(const AttnParams& p, const Work& wk, int32_t* meta_k, uin
 }
 
 // After an abort: wait (bounded) for the copies still in flight to land.
-__device__ void drain(int issued, uint32_t full0) {
+__device__ void drain(int issued, uint32_t full0, uint64_t limit_ns) {
   const int lo = issued > kAttnStages ? issued - kAttnStages : 0;
-  for (int i = lo; i < issued; ++i) (void)mbar_wait(full0 + (i % kAttnStages) * 8, (i / kAttnStages) & 1);
+  for (int i = lo; i < issued; ++i) (void)mbar_wait(full0 + (i % kAttnStages) * 8, (i / kAttnStages) & 1, limit_ns);
 }
+
+
 
 __device__ __forceinline__ float t2_scale(const char* stage_scales, bool per_head, int idx) {
   return per_head ? __half2float(reinterpret_cast<const __half*>(stage_scales)[idx])
@@ -388,7 +457,7 @@ __device__ void write_partial(const AttnParams& p, const Work& wk, char* smem) {
   float* mo = reinterpret_cast<float*>(smem);           // [warps][G][D]
   float* mm = mo + kAttnWarps * G * D;                  // [warps][GP]
   float* mz = mm + kAttnWarps * S::GP;                  // [warps][GP]
-  const int64_t pidx = static_cast<int64_t>(wk.cf + wk.jc) * p.Hkv + wk.kvh;
+  const int64_t pidx = unit_index(p, wk.z, wk.cf + wk.jc, wk.kvh);
   for (int idx = tid; idx < G * D; idx += blockDim.x) {
     const int g = idx / D;
     float M = -INFINITY;
@@ -440,7 +509,7 @@ template <typename T, int G, int D, int NT, typename Sync>
 __device__ void layer_epilogue(const AttnParams& p, const LayerBufs& lb, const Work& wk, int tid,
                                float* sM, float* sIZ, Sync sync, int part = 0, int parts = 1) {
   const int warp = tid >> 5, lane = tid & 31;
-  const int64_t base = static_cast<int64_t>(wk.cf) * p.Hkv + wk.kvh;  // partial of chunk j: base + j * Hkv
+  const int64_t base = unit_index(p, wk.z, wk.cf, wk.kvh);  // partial of chunk j: base + j * Hkv
   const int nch = wk.nch;
   for (int g = warp; g < G; g += NT / 32) {
     // one round of loads: up to 64 chunks per lane pair (m, z) in registers
@@ -479,7 +548,7 @@ __device__ void layer_epilogue(const AttnParams& p, const LayerBufs& lb, const W
     // this chunk's slice of the G * D outputs
     const int lo = static_cast<int>((static_cast<int64_t>(wk.jc) * G * D) / nch);
     const int hi = static_cast<int>((static_cast<int64_t>(wk.jc + 1) * G * D) / nch);
-    T* out = reinterpret_cast<T*>(lb.out) + static_cast<int64_t>(wk.b) * p.out_stride_b +
+    T* out = reinterpret_cast<T*>(lb.out) + wk.z * p.out_stride_l + static_cast<int64_t>(wk.b) * p.out_stride_b +
              static_cast<int64_t>(wk.kvh) * G * D;
     for (int idx = lo + tid; idx < hi; idx += NT) {
       const int g = idx / D;
@@ -497,9 +566,9 @@ __device__ void layer_epilogue(const AttnParams& p, const LayerBufs& lb, const W
     }
   }
   if (p.acc == nullptr) return;
-  const float* __restrict__ spill_b = lb.spill + (static_cast<int64_t>(wk.b) * p.Hkv + wk.kvh) * p.spill_stride;
-  float* __restrict__ accb = p.acc + static_cast<int64_t>(wk.b) * p.acc_stride_b +
-                             static_cast<int64_t>(wk.kvh) * p.acc_stride_h;
+  const float* __restrict__ spill_b = spill_of(p, const_cast<float*>(lb.spill), wk);
+  float* __restrict__ accb = p.acc + wk.z * p.acc_stride_l + static_cast<int64_t>(wk.b) * p.acc_stride_b +
+                             static_cast<int64_t>(wk.kvh) * p.acc_stride_h + static_cast<int64_t>(p.page_base[wk.b]) * kPage;
   float M[G], IZ[G];
 #pragma unroll
   for (int g = 0; g < G; ++g) {
@@ -536,9 +605,9 @@ __device__ void layer_epilogue(const AttnParams& p, const LayerBufs& lb, const W
   }
 }
 
-// The epilogue of a layer as a kernel of its own: one CTA per (chunk, KV head),
-// launched as a programmatic dependent of that layer's attention kernel (used
-// for a single layer, and for the last layer of a decode step).
+// The epilogue of a launch's layers as a kernel of its own: one CTA per (chunk,
+// KV head, layer), launched as a programmatic dependent of that attention launch
+// (used for a lone call, and for the last launch of a decode step).
 constexpr int kCombineThreads = 256;
 
 template <typename T, int G, int D>
@@ -551,20 +620,21 @@ __global__ void __launch_bounds__(kCombineThreads) attn_combine_kernel(const __g
   layer_epilogue<T, G, D, kCombineThreads>(p, lb, wk, threadIdx.x, sM, sIZ, [] { __syncthreads(); });
 }
 
-// The previous layer's epilogue, run by all warps of an attention CTA once its
+// The previous launch's epilogue, run by all warps of an attention CTA once its
 // own pages are done and its partial is written: CTAs that finish early do it
 // while the last ones still stream, and it never holds up the ring. Same
 // (chunk, KV head) split, since every layer of a step has the same chunk plan.
-// The items — one per (chunk, KV head) — are handed out by a counter, so CTAs
-// that finish their pages early take most of them and the last CTAs to finish
-// find none left.
+// The items — one per (layer, KV head, chunk) of the previous launch — are
+// handed out by a counter, so CTAs that finish their pages early take most of
+// them and the last CTAs to finish find none left.
 template <typename T, int G, int D>
 __device__ __forceinline__ void prev_layer_epilogue(const AttnParams& p, int tid, float* sM, float* sIZ,
                                                     volatile int* s_item) {
   if (!p.has_prev) return;
   const LayerBufs lb{p.prev_part_o, p.prev_part_m, p.prev_part_z, p.prev_spill, p.prev_out};
   constexpr int kParts = 1;  // pieces per (chunk, KV head)
-  const int items = static_cast<int>(gridDim.x * gridDim.y) * kParts;
+  const int units = p.total_chunks * p.Hkv * p.prev_nlayers;  // the previous launch's (layer, KV head, chunk) items
+  const int items = units * kParts;
   for (;;) {
     __syncthreads();
     if (tid == 0) *s_item = atomicAdd(p.ep_next, 1);
@@ -572,7 +642,8 @@ __device__ __forceinline__ void prev_layer_epilogue(const AttnParams& p, int tid
     const int item = *s_item;
     if (item >= items) break;
     const int unit = item / kParts;
-    const Work wk = find_work_at(p, unit % static_cast<int>(gridDim.x), unit / static_cast<int>(gridDim.x));
+    const int cu = unit % p.total_chunks, rest = unit / p.total_chunks;
+    const Work wk = find_work_at(p, cu, rest % p.Hkv, rest / p.Hkv);
     layer_epilogue<T, G, D, (kAttnWarps + 1) * 32>(p, lb, wk, tid, sM, sIZ, [] { __syncthreads(); },
                                                    item % kParts, kParts);
   }
@@ -649,7 +720,7 @@ __global__ void __launch_bounds__((kAttnWarps + 1) * 32, 3)
   const Work wk = find_work(p);
   if (tid == 0) s_abort = 0;
   if (tid == 0 && p.span) atomicMin(p.span, global_ns());
-  if (tid == 0 && blockIdx.x == 0 && blockIdx.y == 0) {
+  if (tid == 0 && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0) {
     if (p.span_next) {
       p.span_next[0] = ~0ull;
       p.span_next[1] = 0ull;
@@ -676,7 +747,7 @@ __global__ void __launch_bounds__((kAttnWarps + 1) * 32, 3)
   // Q fragments (A operand, heads as rows; rows 8..15 of the tile are zero)
   uint32_t qa[KS][2];
   if (consumer) {
-    const T* q = reinterpret_cast<const T*>(p.q) + static_cast<int64_t>(wk.b) * p.q_stride_b +
+    const T* q = reinterpret_cast<const T*>(p.q) + wk.z * p.q_stride_l + static_cast<int64_t>(wk.b) * p.q_stride_b +
                  static_cast<int64_t>(wk.kvh) * G * D;
 #pragma unroll
     for (int ks = 0; ks < KS; ++ks) {
@@ -693,14 +764,14 @@ __global__ void __launch_bounds__((kAttnWarps + 1) * 32, 3)
   float o[KS][4];                        // O^T tiles: d rows, head columns
 #pragma unroll
   for (int mt = 0; mt < KS; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
-  float* spill_b = p.spill + (static_cast<int64_t>(wk.b) * p.Hkv + wk.kvh) * p.spill_stride;
+  float* spill_b = spill_of(p, p.spill, wk);
   // per-lane ldmatrix row / chunk selectors (matrix = lane / 8)
   const int lrow = ((lane >> 4) << 3) | (lane & 7);
   const int lchunk = (lane >> 3) & 1;
 
   for (int i = w; consumer; i += kAttnWarps) {
     const int st = i % kAttnStages;
-    const bool ok = __all_sync(kFull, mbar_wait(full0 + st * 8, (i / kAttnStages) & 1));
+    const bool ok = __all_sync(kFull, mbar_wait(full0 + st * 8, (i / kAttnStages) & 1, p.wait_limit_ns));
     if (!ok) {
       if (lane == 0) s_abort = 1;
       break;
@@ -711,6 +782,7 @@ __global__ void __launch_bounds__((kAttnWarps + 1) * 32, 3)
     const uint32_t flags = meta_f[i % kMeta];
     const uint32_t mask = flags & 0xffffu;
     const bool i8 = (flags & kFlagI8) != 0;
+    const bool host = (flags & kFlagHost) != 0;
     const int swz = i8 ? kSwizzle : static_cast<int>((flags >> kFlagSwzShift) & 7u);
     if (i8) widen_i8_page<D>(stage, lane);
     const uint32_t kbase = smem_u32(stage), vbase = kbase + S::BLK;
@@ -808,7 +880,7 @@ __global__ void __launch_bounds__((kAttnWarps + 1) * 32, 3)
     if (lane == 0) {
       // the stage was written through the generic proxy (widened codes, zeroed
       // rows): order those writes before the next bulk copy into it
-      if (i8 || mask != 0xffffu) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      if (i8 || host || mask != 0xffffu) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       mbar_arrive(empty0 + st * 8);
     }
   }
@@ -816,7 +888,7 @@ __global__ void __launch_bounds__((kAttnWarps + 1) * 32, 3)
   __syncthreads();
   if (s_abort) {  // a bounded wait gave up: land the copies in flight, publish an empty partial
     if (!consumer && lane == 0) {
-      drain(issued, full0);
+      drain(issued, full0, p.wait_limit_ns);
       atomicExch(p.err, DEV_TIMEOUT);
     }
     m_run = -INFINITY;
@@ -947,7 +1019,7 @@ __global__ void __launch_bounds__((kAttnWarps + 1) * 32)
   const Work wk = find_work(p);
   if (tid == 0) s_abort = 0;
   if (tid == 0 && p.span) atomicMin(p.span, global_ns());
-  if (tid == 0 && blockIdx.x == 0 && blockIdx.y == 0) {
+  if (tid == 0 && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0) {
     if (p.span_next) {
       p.span_next[0] = ~0ull;
       p.span_next[1] = 0ull;
@@ -975,7 +1047,7 @@ __global__ void __launch_bounds__((kAttnWarps + 1) * 32)
   float* p_s = reinterpret_cast<float*>(smem + L::off_p) + w * L::PSW;
   float* corr_s = p_s + S::GP * kPage;
   {
-    const T* q = reinterpret_cast<const T*>(p.q) + static_cast<int64_t>(wk.b) * p.q_stride_b +
+    const T* q = reinterpret_cast<const T*>(p.q) + wk.z * p.q_stride_l + static_cast<int64_t>(wk.b) * p.q_stride_b +
                  static_cast<int64_t>(wk.kvh) * G * D;
     for (int i = tid; consumer && i < S::GP * D; i += kAttnWarps * 32) {
       const int gg = i / D;
@@ -1003,23 +1075,24 @@ __global__ void __launch_bounds__((kAttnWarps + 1) * 32)
   const bool own_writer = S::NV >= 8 ? true : ((c & 1) == 0);
   const bool head_lead = r == 0 && (S::NV < 8 ? c == 0 : (c & ((8 / S::GP) - 1)) == 0);
 
-  float* spill_b = p.spill + (static_cast<int64_t>(wk.b) * p.Hkv + wk.kvh) * p.spill_stride;
+  float* spill_b = spill_of(p, p.spill, wk);
 
   for (int i = w; consumer; i += kAttnWarps) {
     const int st = i % kAttnStages;
-    const bool ok = __all_sync(kFull, mbar_wait(full0 + st * 8, (i / kAttnStages) & 1));
+    const bool ok = __all_sync(kFull, mbar_wait(full0 + st * 8, (i / kAttnStages) & 1, p.wait_limit_ns));
     if (!ok) {
       if (lane == 0) s_abort = 1;
       break;
     }
     const int k = meta_k[i % kMeta];  // page index in the sequence's list; -1 ends this warp's pages
     if (k < 0) break;
-    const char* stage = ring + st * S::STAGE;
     const uint32_t flags = meta_f[i % kMeta];
     const uint32_t mask = flags & 0xffffu;
     const bool i8 = (flags & kFlagI8) != 0;
     const bool per_head = (flags & kFlagPerHead) != 0;
+    const bool host = (flags & kFlagHost) != 0;
     const int swz = static_cast<int>((flags >> kFlagSwzShift) & 7u);
+    const char* stage = ring + st * S::STAGE;
 
     // ---- QK: 4 rows per lane, QE elements each, all heads -----------------
     float part[S::NV];
@@ -1182,13 +1255,18 @@ __global__ void __launch_bounds__((kAttnWarps + 1) * 32)
       }
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(empty0 + st * 8);
+    if (lane == 0) {
+      // a page read in place was written to the stage through the generic proxy:
+      // order those writes before the next bulk copy into it
+      if (host) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      mbar_arrive(empty0 + st * 8);
+    }
   }
 
   __syncthreads();
   if (s_abort) {  // a bounded wait gave up: land the copies in flight, publish an empty partial
     if (!consumer && lane == 0) {
-      drain(issued, full0);
+      drain(issued, full0, p.wait_limit_ns);
       atomicExch(p.err, DEV_TIMEOUT);
     }
     m_run = -INFINITY;
@@ -1225,7 +1303,7 @@ cudaError_t launch_kernel(K kern, int smem_bytes, const AttnParams& p, int total
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  dim3 grid(total_chunks, p.Hkv);
+  dim3 grid(total_chunks, p.Hkv, p.nlayers);
   kern<<<grid, (kAttnWarps + 1) * 32, smem_bytes, s>>>(p);
   return cudaGetLastError();
 }
@@ -1237,7 +1315,7 @@ cudaError_t launch_typed(const AttnParams& p, int total_chunks, cudaStream_t s, 
   using L = Smem<T, G, D, !kMma>;
   if (part == 1) {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(total_chunks, p.Hkv);
+    cfg.gridDim = dim3(total_chunks, p.Hkv, p.nlayers);
     cfg.blockDim = dim3(kCombineThreads);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = s;
@@ -1318,7 +1396,8 @@ int attention_supported(int kv_dtype, int G, int D) {
 }
 
 cudaError_t launch_attention_part(const AttnParams& p, int kv_dtype, int total_chunks, cudaStream_t s, int part) {
-  if (total_chunks <= 0) return cudaSuccess;
+  if (total_chunks <= 0 || p.nlayers <= 0) return cudaSuccess;
+  if (total_chunks != p.total_chunks || p.nlayers > 65535) return cudaErrorInvalidValue;
   if (kv_dtype == 1) return dispatch_g<__nv_bfloat16>(p, total_chunks, s, part);
   return dispatch_g<float>(p, total_chunks, s, part);
 }

@@ -153,6 +153,16 @@ __device__ __forceinline__ char* full_chunk(const MoveParams& p, int tier, int l
   return pg + (static_cast<int64_t>(hk) * kPage + slot) * row_bytes + ((c ^ (slot & kSwizzle)) << 4);
 }
 
+// The same chunk in a tier's device mirror (null when the tier has none).
+__device__ __forceinline__ char* mirror_chunk(const MoveParams& p, int tier, int loc, int l, int hk, int c,
+                                             int64_t row_bytes) {
+  if (tier < 1 || p.pools.mirror[tier] == nullptr) return nullptr;
+  const int page = loc >> 4, slot = loc & 15;
+  const TierPools& P = p.pools;
+  char* pg = P.mirror[tier] + l * P.layer_bytes[tier] + static_cast<int64_t>(page) * P.page_bytes[tier];
+  return pg + (static_cast<int64_t>(hk) * kPage + slot) * row_bytes + ((c ^ (slot & kSwizzle)) << 4);
+}
+
 __device__ __forceinline__ float t2_scale_of(const TierPools& P, const char* sc, int hk, int slot) {
   const int kv = hk & 1;
   if (P.scale_per_head) {
@@ -180,19 +190,27 @@ __global__ void __launch_bounds__(kMoveThreads) move_kernel(const __grid_constan
   // staging row of this (mover, layer): one per mover when the launch covers one
   // layer, one per (mover, layer) when it covers several
   const int trow = mv.temp_row * static_cast<int>(gridDim.y) + static_cast<int>(blockIdx.y);
+  // With a device mirror of T1 / T2, sources there are read from the mirror (no
+  // host-link read) and destinations there are written to the pool and the mirror.
+  const bool src_mirror = st >= 1 && P.mirror[st] != nullptr;
   if (st != 2 && dt != 2) {  // full precision -> full precision
     for (int j = tid; j < nchunk; j += kMoveThreads) {
       const int hk = j / cpr, c = j % cpr;
-      const uint4 v = *reinterpret_cast<const uint4*>(full_chunk(p, st, mv.src_loc, trow, l, hk, c, row_bytes));
+      const char* from = src_mirror ? mirror_chunk(p, st, mv.src_loc, l, hk, c, row_bytes)
+                                    : full_chunk(p, st, mv.src_loc, trow, l, hk, c, row_bytes);
+      const uint4 v = *reinterpret_cast<const uint4*>(from);
       *reinterpret_cast<uint4*>(full_chunk(p, dt, mv.dst_loc, trow, l, hk, c, row_bytes)) = v;
+      if (char* m = mirror_chunk(p, dt, mv.dst_loc, l, hk, c, row_bytes)) *reinterpret_cast<uint4*>(m) = v;
     }
     return;
   }
 
   if (st == 2) {  // leaving T2: dequantise to the destination's storage, chunk by chunk
     const int page = mv.src_loc >> 4, slot = mv.src_loc & 15;
-    const char* pg = P.base[2] + l * P.layer_bytes[2] + static_cast<int64_t>(page) * P.page_bytes[2];
-    const char* sc = P.t2_scales + l * P.t2_scale_layer_bytes + static_cast<int64_t>(page) * P.t2_scale_page_bytes;
+    const char* pg = (src_mirror ? P.mirror[2] : P.base[2]) + l * P.layer_bytes[2] +
+                     static_cast<int64_t>(page) * P.page_bytes[2];
+    const char* sc = (src_mirror ? P.mirror_scales : P.t2_scales) + l * P.t2_scale_layer_bytes +
+                     static_cast<int64_t>(page) * P.t2_scale_page_bytes;
     for (int j = tid; j < nchunk; j += kMoveThreads) {
       const int hk = j / cpr, c = j % cpr;
       const float scale = t2_scale_of(P, sc, hk, slot);
@@ -221,6 +239,7 @@ __global__ void __launch_bounds__(kMoveThreads) move_kernel(const __grid_constan
         out = make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]), __float_as_uint(f[3]));
       }
       *reinterpret_cast<uint4*>(full_chunk(p, dt, mv.dst_loc, trow, l, hk, c, row_bytes)) = out;
+      if (char* m = mirror_chunk(p, dt, mv.dst_loc, l, hk, c, row_bytes)) *reinterpret_cast<uint4*>(m) = out;
     }
     return;
   }
@@ -230,7 +249,9 @@ __global__ void __launch_bounds__(kMoveThreads) move_kernel(const __grid_constan
   for (int j = tid; j < nchunk; j += kMoveThreads) {
     const int hk = j / cpr, c = j % cpr;
     const int h = hk >> 1, kv = hk & 1;
-    const uint4 v = *reinterpret_cast<const uint4*>(full_chunk(p, st, mv.src_loc, trow, l, hk, c, row_bytes));
+    const char* from = src_mirror ? mirror_chunk(p, st, mv.src_loc, l, hk, c, row_bytes)
+                                  : full_chunk(p, st, mv.src_loc, trow, l, hk, c, row_bytes);
+    const uint4 v = *reinterpret_cast<const uint4*>(from);
     float* dst = row_s + kv * HD + h * p.D + c * epc;
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
     if (esz == 2) {
@@ -249,6 +270,9 @@ __global__ void __launch_bounds__(kMoveThreads) move_kernel(const __grid_constan
   const int page = mv.dst_loc >> 4, slot = mv.dst_loc & 15;
   char* pg = P.base[2] + l * P.layer_bytes[2] + static_cast<int64_t>(page) * P.page_bytes[2];
   char* sc = P.t2_scales + l * P.t2_scale_layer_bytes + static_cast<int64_t>(page) * P.t2_scale_page_bytes;
+  char* mpg = P.mirror[2] ? P.mirror[2] + l * P.layer_bytes[2] + static_cast<int64_t>(page) * P.page_bytes[2] : nullptr;
+  char* msc = P.mirror[2] ? P.mirror_scales + l * P.t2_scale_layer_bytes + static_cast<int64_t>(page) * P.t2_scale_page_bytes
+                          : nullptr;
   // scale groups: per token, one per K / V over all heads; per token and head, one per (head, K / V)
   const int ngroups = P.scale_per_head ? 2 * p.Hkv : 2;
   const int glen = P.scale_per_head ? p.D : HD;
@@ -273,17 +297,21 @@ __global__ void __launch_bounds__(kMoveThreads) move_kernel(const __grid_constan
           word |= (static_cast<uint32_t>(static_cast<uint8_t>(quant_code(x[i0 + 4 * q + bb], div)))) << (8 * bb);
         w[q] = word;
       }
-      *reinterpret_cast<uint4*>(pg + ((static_cast<int64_t>(h) * 2 + kv) * kPage + slot) * p.D + e0) =
-          make_uint4(w[0], w[1], w[2], w[3]);
+      const int64_t at = ((static_cast<int64_t>(h) * 2 + kv) * kPage + slot) * p.D + e0;
+      *reinterpret_cast<uint4*>(pg + at) = make_uint4(w[0], w[1], w[2], w[3]);
+      if (mpg) *reinterpret_cast<uint4*>(mpg + at) = make_uint4(w[0], w[1], w[2], w[3]);
     }
     if (lane == 0) {
-      if (P.scale_per_head) {
-        if (P.scale_f16)
-          reinterpret_cast<__half*>(sc)[(h0 * 2 + kv) * kPage + slot] = h16;
-        else
-          reinterpret_cast<float*>(sc)[(h0 * 2 + kv) * kPage + slot] = div;
-      } else {
-        reinterpret_cast<float*>(sc)[kv * kPage + slot] = div;
+      for (int copy = 0; copy < (mpg ? 2 : 1); ++copy) {
+        char* scp = copy ? msc : sc;
+        if (P.scale_per_head) {
+          if (P.scale_f16)
+            reinterpret_cast<__half*>(scp)[(h0 * 2 + kv) * kPage + slot] = h16;
+          else
+            reinterpret_cast<float*>(scp)[(h0 * 2 + kv) * kPage + slot] = div;
+        } else {
+          reinterpret_cast<float*>(scp)[kv * kPage + slot] = div;
+        }
       }
     }
   }
@@ -291,8 +319,8 @@ __global__ void __launch_bounds__(kMoveThreads) move_kernel(const __grid_constan
 
 // ---------------------------------------------------------------- fold
 // One thread per slot of a sequence's attention page list: the slot's position
-// gets (sum over KV heads of the accumulated weights) / (L * Hq) in float64;
-// the accumulator is cleared for the next step.
+// gets (sum over layer slices and KV heads of the accumulated weights) /
+// (L * Hq) in float64; the accumulator is cleared for the next step.
 __global__ void fold_kernel(const __grid_constant__ FoldParams p) {
   const int b = blockIdx.y;
   const int64_t slot = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -309,12 +337,14 @@ __global__ void fold_kernel(const __grid_constant__ FoldParams p) {
     }
   }
   const int page = p.table[src][static_cast<int64_t>(b) * p.table_stride + k];
+  const int64_t at = static_cast<int64_t>(p.page_base[b]) * kPage + slot;
   double sum = 0.0;
-  for (int h = 0; h < p.Hkv; ++h) {
-    float* a = p.acc + (static_cast<int64_t>(b) * p.Hkv + h) * p.acc_stride + slot;
-    sum += static_cast<double>(*a);
-    *a = 0.f;
-  }
+  for (int z = 0; z < p.nslices; ++z)
+    for (int h = 0; h < p.Hkv; ++h) {
+      float* a = p.acc + z * p.acc_stride_l + h * p.acc_stride_h + at;
+      sum += static_cast<double>(*a);
+      *a = 0.f;
+    }
   if ((p.mask[src][page] >> row) & 1u) {
     const int pos = p.posmap[src][static_cast<int64_t>(page) * kPage + row];
     if (pos >= 0) p.s[static_cast<int64_t>(b) * p.s_stride + pos] += sum * p.inv_lh;

@@ -60,13 +60,16 @@ struct Seq {
 // Sizes derived from a configuration; shared by tkv_workspace_size and tkv_create.
 struct Layout {
   int L, Hq, Hkv, D, G, esz, maxb;
+  int Lg;                // layers per attention launch (and per prefetch in STREAM mode)
+  int mode;              // TKV_HOST_TIERS_*
   int64_t maxtok, maxp;
   int64_t cap[3];
+  int64_t total_pages;   // pages of all three pools: bounds the pages of all sequences together
   int64_t plb[3];        // bytes of one page record per layer (T2: int8 codes)
   int64_t scale_rec;     // bytes of one T2 scale record per page per layer
   int64_t max_chunks, spill_stride, temp_rows;
   // device offsets
-  size_t o_pool0, o_stage1, o_stage2c, o_stage2s, o_table, o_mask, o_posmap, o_tier, o_tier_new,
+  size_t o_pool0, o_stage1, o_stage2c, o_stage2s, o_mirror1, o_mirror2c, o_mirror2s, o_table, o_mask, o_posmap, o_tier, o_tier_new,
       o_s, o_acc, o_part_o, o_part_m, o_part_z, o_spill, o_keys, o_err, o_span, o_movers,
       o_temp, o_locs, o_io, dev_bytes;
   size_t io_q, io_k, io_out;
@@ -118,12 +121,33 @@ std::string validate(const tkv_config& c) {
   if (c.t2_mode != TKV_T2_ATTEND && c.t2_mode != TKV_T2_MASK) return bad("t2_mode");
   if (c.t0_pages < 0 || c.t1_pages < 0 || c.t2_pages < 0 || c.max_staged_movers < 0) return bad("negative capacity");
   if (c.split_pages < 0 || c.split_pages > kMaxChunkPages) return bad("split_pages must be 0..256");
+  if (c.host_tiers != TKV_HOST_TIERS_STREAM && c.host_tiers != TKV_HOST_TIERS_MIRROR &&
+      c.host_tiers != TKV_HOST_TIERS_ZEROCOPY)
+    return bad("host_tiers");
+  if (c.layers_per_launch < 0) return bad("layers_per_launch must be >= 0");
   return std::string();
+}
+
+// Layers per attention launch: the configured count (at most L), else the
+// largest divisor of L up to 7. Each launch pays a fixed start-up, tail and
+// launch cost; on the batch-32 workload one layer per launch ran the kernel at
+// 60 % of the measured HBM peak, 4 layers at 67 % and 7 at 72 %. In STREAM mode
+// the staging ring holds two groups, so the grouping costs 2 x 7 layers of the
+// used T1 / T2 range in HBM.
+int layers_per_launch(const tkv_config& c) {
+  if (c.layers_per_launch > 0) return std::min(c.layers_per_launch, c.n_layers);
+  const int cap = 7;
+  int best = 1;
+  for (int g = 1; g <= std::min(cap, c.n_layers); ++g)
+    if (c.n_layers % g == 0) best = g;
+  return best;
 }
 
 Layout make_layout(const tkv_config& c) {
   Layout y{};
   y.L = c.n_layers; y.Hq = c.n_q_heads; y.Hkv = c.n_kv_heads; y.D = c.head_dim;
+  y.Lg = layers_per_launch(c);
+  y.mode = c.host_tiers;
   y.G = y.Hq / y.Hkv; y.esz = c.kv_dtype == TKV_DTYPE_BF16 ? 2 : 4; y.maxb = c.max_batch;
   y.maxtok = c.max_tokens;
   y.maxp = ceil_div(y.maxtok, kPage) + 1;
@@ -137,30 +161,40 @@ Layout make_layout(const tkv_config& c) {
   y.plb[0] = y.plb[1] = int64_t(y.Hkv) * 2 * kPage * y.D * y.esz;
   y.plb[2] = int64_t(y.Hkv) * 2 * kPage * y.D;
   y.scale_rec = c.t2_scale_gran == TKV_SCALE_PER_TOKEN ? 2 * kPage * 4 : int64_t(y.Hkv) * 2 * kPage * 2;
-  y.max_chunks = int64_t(y.maxb) * (ceil_div(3 * y.maxp, 8) + 1);
-  y.spill_stride = 3 * y.maxp * y.G * kPage;
+  y.total_pages = y.cap[0] + y.cap[1] + y.cap[2];
+  // a sequence of n pages gets at most min(128, ceil(n / 8)) chunks (plan_chunks)
+  y.max_chunks = std::min<int64_t>(int64_t(y.maxb) * kMaxChunksPerSeq, ceil_div(y.total_pages, 8) + y.maxb);
+  y.spill_stride = y.total_pages * y.G * kPage;   // floats per (layer slice, KV head)
   // staging rows hold one layer (phase-2 moves run layer by layer); by default
   // one per position, so any reassignment fits
   y.temp_rows = c.max_staged_movers ? c.max_staged_movers : int64_t(y.maxb) * y.maxtok;
   size_t o = 0;
   auto take = [&](size_t bytes) { size_t at = o; o = align_up(o + bytes); return at; };
   y.o_pool0 = take(size_t(y.L) * y.cap[0] * y.plb[0]);
-  y.o_stage1 = take(2 * size_t(y.cap[1]) * y.plb[1]);
-  y.o_stage2c = take(2 * size_t(y.cap[2]) * y.plb[2]);
-  y.o_stage2s = take(2 * size_t(y.cap[2]) * y.scale_rec);
+  // STREAM: a two-slot staging ring, each slot one layer group of the T1 / T2
+  // pools; MIRROR: device copies of all layers of those pools; ZEROCOPY: neither
+  const size_t stage_layers = y.mode == TKV_HOST_TIERS_STREAM ? 2 * size_t(y.Lg) : 0;
+  const size_t mirror_layers = y.mode == TKV_HOST_TIERS_MIRROR ? size_t(y.L) : 0;
+  y.o_stage1 = take(stage_layers * y.cap[1] * y.plb[1]);
+  y.o_stage2c = take(stage_layers * y.cap[2] * y.plb[2]);
+  y.o_stage2s = take(stage_layers * y.cap[2] * y.scale_rec);
+  y.o_mirror1 = take(mirror_layers * y.cap[1] * y.plb[1]);
+  y.o_mirror2c = take(mirror_layers * y.cap[2] * y.plb[2]);
+  y.o_mirror2s = take(mirror_layers * y.cap[2] * y.scale_rec);
   y.o_table = take(3 * size_t(y.maxb) * y.maxp * 4);
   y.o_mask = take(size_t(y.cap[0] + y.cap[1] + y.cap[2]) * 4);
   y.o_posmap = take(size_t(y.cap[0] + y.cap[1] + y.cap[2]) * kPage * 4);
   y.o_tier = take(size_t(y.maxb) * y.maxtok);
   y.o_tier_new = take(size_t(y.maxb) * y.maxtok);
   y.o_s = take(size_t(y.maxb) * y.maxtok * 8);
-  y.o_acc = take(size_t(y.maxb) * y.Hkv * 3 * y.maxp * kPage * 4);   // slot-indexed score increments
-  // partials and spilled logits: two layers' worth, since each layer's epilogue
-  // runs inside the next layer's attention launch
-  y.o_part_o = take(2 * size_t(y.max_chunks) * y.Hkv * y.G * y.D * 4);
-  y.o_part_m = take(2 * size_t(y.max_chunks) * y.Hkv * y.G * 4);
-  y.o_part_z = take(2 * size_t(y.max_chunks) * y.Hkv * y.G * 4);
-  y.o_spill = take(2 * size_t(y.maxb) * y.Hkv * y.spill_stride * 4);
+  // slot-indexed score increments, one slice per layer of a launch: [Lg][Hkv][total_pages][16]
+  y.o_acc = take(size_t(y.Lg) * y.Hkv * y.total_pages * kPage * 4);
+  // partials and spilled logits: two launches' worth, since each launch's
+  // epilogue runs inside the next attention launch
+  y.o_part_o = take(2 * size_t(y.Lg) * y.max_chunks * y.Hkv * y.G * y.D * 4);
+  y.o_part_m = take(2 * size_t(y.Lg) * y.max_chunks * y.Hkv * y.G * 4);
+  y.o_part_z = take(2 * size_t(y.Lg) * y.max_chunks * y.Hkv * y.G * 4);
+  y.o_spill = take(2 * size_t(y.Lg) * y.Hkv * y.spill_stride * 4);
   y.o_keys = take(size_t(y.maxb) * y.maxtok * 8);
   y.o_err = take(64);   // int32 [0]: device error word; [4], [5]: epilogue work counters by layer parity;
                         // [8]: sequence number of the last attention launch that started
@@ -216,6 +250,9 @@ struct tkv_ctx {
   int slot_rr = 0;
   int64_t steps = 0;
   int64_t attn_launch_seq = 0;    // attention launches so far: their parity picks buffers and counters
+  int64_t last_launch_seq = 0;    // number of the last attention launch actually enqueued (0: none)
+  bool stall_next = false;        // test hook: the next attention launch withholds one page
+  unsigned long long wait_limit_ns = 2000000000ull;  // bounded device waits give up after this long
   int64_t span_from = 0;          // first attention launch counted in attn_span_ms
   // Copy-stream gate: a prefetch waits (stream memory wait) until the previous
   // attention launch has started, so that launch is not made behind a host
@@ -510,14 +547,23 @@ int plan_chunks(const std::vector<int64_t>& ntot, const std::vector<int64_t>& co
   return bound;
 }
 
+// STREAM mode: copy the used T1 / T2 range of layers [l0, l0 + nl) into
+// staging slot `slot` on the copy stream (one copy per pool and layer).
 // gate_seq != 0: first wait until the attention launch with that sequence
 // number has started (its first CTA writes the number to the started word).
-tkv_status enqueue_prefetch(tkv_ctx* h, int layer, int slot, uint32_t gate_seq = 0) {
+// Invariant behind that wait (a stream memory wait has no time limit): gate_seq
+// is always the number of an attention launch that was already enqueued on the
+// compute stream (h->last_launch_seq), and every enqueued attention launch
+// writes its number at entry, so the wait ends once that launch starts.
+tkv_status enqueue_prefetch(tkv_ctx* h, int l0, int nl, int slot, uint32_t gate_seq = 0) {
   const Layout& y = h->y;
+  if (y.mode != TKV_HOST_TIERS_STREAM) return TKV_OK;
   const bool timing = h->cfg.flags & TKV_FLAG_TIMING;
   TimedPair tp{};
   if (h->xs != h->cs) CK(h, cudaStreamWaitEvent(h->xs, h->ev_free[slot], 0));
   if (gate_seq != 0 && h->wait_value && h->xs != h->cs) {
+    if (gate_seq > h->last_launch_seq)
+      return fail(h, TKV_ERR_INTERNAL, "prefetch gated on attention launch %u, which was never enqueued", gate_seq);
     const unsigned long long addr = reinterpret_cast<unsigned long long>(h->D(y.o_err)) + kStartedWordOffset;
     if (h->wait_value(h->xs, addr, gate_seq, kWaitGeq) != 0) h->wait_value = nullptr;  // unsupported: ungated from now on
   }
@@ -527,21 +573,25 @@ tkv_status enqueue_prefetch(tkv_ctx* h, int layer, int slot, uint32_t gate_seq =
     CK(h, cudaEventRecord(tp.a, h->xs));
   }
   const int64_t n1 = h->next_page[1], n2 = h->next_page[2];
-  if (n1 > 0) {
-    CK(h, cudaMemcpyAsync(h->D(y.o_stage1) + size_t(slot) * y.cap[1] * y.plb[1],
-                          h->P(y.p_pool1) + size_t(layer) * y.cap[1] * y.plb[1], size_t(n1) * y.plb[1],
-                          cudaMemcpyHostToDevice, h->xs));
-    h->stats.prefetch_bytes += n1 * y.plb[1];
-  }
   const bool t2_read = h->cfg.t2_mode == TKV_T2_ATTEND;
-  if (n2 > 0 && t2_read) {
-    CK(h, cudaMemcpyAsync(h->D(y.o_stage2c) + size_t(slot) * y.cap[2] * y.plb[2],
-                          h->P(y.p_pool2c) + size_t(layer) * y.cap[2] * y.plb[2], size_t(n2) * y.plb[2],
-                          cudaMemcpyHostToDevice, h->xs));
-    CK(h, cudaMemcpyAsync(h->D(y.o_stage2s) + size_t(slot) * y.cap[2] * y.scale_rec,
-                          h->P(y.p_pool2s) + size_t(layer) * y.cap[2] * y.scale_rec,
-                          size_t(n2) * y.scale_rec, cudaMemcpyHostToDevice, h->xs));
-    h->stats.prefetch_bytes += n2 * (y.plb[2] + y.scale_rec);
+  for (int j = 0; j < nl; ++j) {
+    const size_t sl = size_t(slot) * y.Lg + j;  // staging layer index
+    const int l = l0 + j;
+    if (n1 > 0) {
+      CK(h, cudaMemcpyAsync(h->D(y.o_stage1) + sl * y.cap[1] * y.plb[1],
+                            h->P(y.p_pool1) + size_t(l) * y.cap[1] * y.plb[1], size_t(n1) * y.plb[1],
+                            cudaMemcpyHostToDevice, h->xs));
+      h->stats.prefetch_bytes += n1 * y.plb[1];
+    }
+    if (n2 > 0 && t2_read) {
+      CK(h, cudaMemcpyAsync(h->D(y.o_stage2c) + sl * y.cap[2] * y.plb[2],
+                            h->P(y.p_pool2c) + size_t(l) * y.cap[2] * y.plb[2], size_t(n2) * y.plb[2],
+                            cudaMemcpyHostToDevice, h->xs));
+      CK(h, cudaMemcpyAsync(h->D(y.o_stage2s) + sl * y.cap[2] * y.scale_rec,
+                            h->P(y.p_pool2s) + size_t(l) * y.cap[2] * y.scale_rec,
+                            size_t(n2) * y.scale_rec, cudaMemcpyHostToDevice, h->xs));
+      h->stats.prefetch_bytes += n2 * (y.plb[2] + y.scale_rec);
+    }
   }
   if (timing) {
     CK(h, cudaEventRecord(tp.b, h->xs));
@@ -551,17 +601,37 @@ tkv_status enqueue_prefetch(tkv_ctx* h, int layer, int slot, uint32_t gate_seq =
   return TKV_OK;
 }
 
-void fill_sources(tkv_ctx* h, int layer, int slot, AttnParams& p) {
+// Page sources of the launch covering layers from l0: T0 from the HBM pool;
+// T1 / T2 from the staging slot (STREAM), the device mirror (MIRROR) or the
+// pinned host pools in place (ZEROCOPY).
+void fill_sources(tkv_ctx* h, int l0, int slot, AttnParams& p) {
   const Layout& y = h->y;
   const int64_t head_full = int64_t(2) * kPage * y.D * y.esz;
-  p.src[0] = PageSource{h->D(y.o_pool0) + size_t(layer) * y.cap[0] * y.plb[0], y.plb[0], head_full,
-                        d_table(h, 0), d_mask(h, 0), d_posmap(h, 0), nullptr, 0, 0, SRC_FULL, kSwizzle};
-  p.src[1] = PageSource{h->D(y.o_stage1) + size_t(slot) * y.cap[1] * y.plb[1], y.plb[1], head_full,
-                        d_table(h, 1), d_mask(h, 1), d_posmap(h, 1), nullptr, 0, 0, SRC_FULL, kSwizzle};
-  p.src[2] = PageSource{h->D(y.o_stage2c) + size_t(slot) * y.cap[2] * y.plb[2], y.plb[2],
-                        int64_t(2) * kPage * y.D, d_table(h, 2), d_mask(h, 2), d_posmap(h, 2),
-                        h->D(y.o_stage2s) + size_t(slot) * y.cap[2] * y.scale_rec, y.scale_rec,
-                        h->cfg.t2_scale_gran == TKV_SCALE_PER_TOKEN_HEAD ? 1 : 0, SRC_INT8, 0};
+  const int64_t lb0 = y.cap[0] * y.plb[0], lb1 = y.cap[1] * y.plb[1], lb2 = y.cap[2] * y.plb[2];
+  const int64_t lbs = y.cap[2] * y.scale_rec;
+  const char *b1, *b2, *b2s;
+  int host = 0;
+  if (y.mode == TKV_HOST_TIERS_STREAM) {
+    b1 = h->D(y.o_stage1) + size_t(slot) * y.Lg * lb1;
+    b2 = h->D(y.o_stage2c) + size_t(slot) * y.Lg * lb2;
+    b2s = h->D(y.o_stage2s) + size_t(slot) * y.Lg * lbs;
+  } else if (y.mode == TKV_HOST_TIERS_MIRROR) {
+    b1 = h->D(y.o_mirror1) + size_t(l0) * lb1;
+    b2 = h->D(y.o_mirror2c) + size_t(l0) * lb2;
+    b2s = h->D(y.o_mirror2s) + size_t(l0) * lbs;
+  } else {
+    b1 = h->PD(y.p_pool1) + size_t(l0) * lb1;
+    b2 = h->PD(y.p_pool2c) + size_t(l0) * lb2;
+    b2s = h->PD(y.p_pool2s) + size_t(l0) * lbs;
+    host = 1;
+  }
+  p.src[0] = PageSource{h->D(y.o_pool0) + size_t(l0) * lb0, lb0, y.plb[0], head_full, d_table(h, 0), d_mask(h, 0),
+                        d_posmap(h, 0), nullptr, 0, 0, 0, SRC_FULL, kSwizzle, 0};
+  p.src[1] = PageSource{b1, lb1, y.plb[1], head_full, d_table(h, 1), d_mask(h, 1), d_posmap(h, 1), nullptr, 0, 0, 0,
+                        SRC_FULL, kSwizzle, host};
+  p.src[2] = PageSource{b2, lb2, y.plb[2], int64_t(2) * kPage * y.D, d_table(h, 2), d_mask(h, 2), d_posmap(h, 2),
+                        b2s, lbs, y.scale_rec, h->cfg.t2_scale_gran == TKV_SCALE_PER_TOKEN_HEAD ? 1 : 0, SRC_INT8, 0,
+                        host};
   p.nsrc = 3;
 }
 
@@ -625,12 +695,13 @@ tkv_status decode_step_device(tkv_ctx* h, const void* q, const void* k_new, cons
   }
   LK(h, launch_append(ap, h->cs), B > 0);
 
-  // ---- per layer: prefetch T1/T2 (copy stream), attention + fused scores (compute stream)
+  // ---- per layer group: prefetch T1/T2 (copy stream, STREAM mode), attention + fused scores (compute stream)
   AttnParams p{};
   p.B = B; p.Hq = y.Hq; p.Hkv = y.Hkv; p.D = y.D; p.G = y.G;
   p.table_stride = static_cast<int32_t>(y.maxp);
   const bool t2_read = h->cfg.t2_mode == TKV_T2_ATTEND;
   std::vector<int64_t> ntot(B), cost(B);
+  p.page_base[0] = 0;
   for (int b = 0; b < B; ++b) {
     const Seq& sq = h->seqs[b];
     p.npages[0][b] = static_cast<int32_t>(sq.pages[0].size());
@@ -638,40 +709,53 @@ tkv_status decode_step_device(tkv_ctx* h, const void* q, const void* k_new, cons
     p.npages[2][b] = t2_read ? static_cast<int32_t>(sq.pages[2].size()) : 0;
     ntot[b] = p.npages[0][b] + p.npages[1][b] + p.npages[2][b];
     cost[b] = int64_t(kCostFull) * (p.npages[0][b] + p.npages[1][b]) + int64_t(kCostI8) * p.npages[2][b];
+    p.page_base[b + 1] = p.page_base[b] + static_cast<int32_t>(ntot[b]);
   }
+  if (p.page_base[B] > y.total_pages) return fail(h, TKV_ERR_INTERNAL, "page lists exceed the pools");
   p.chunk_pages = plan_chunks(ntot, cost, y.Hkv, h->cfg.split_pages, h->resident_ctas, p.chunk_first);
   const int total_chunks = p.chunk_first[B];
   if (total_chunks > y.max_chunks) return fail(h, TKV_ERR_INTERNAL, "chunk table overflow");
+  p.total_chunks = total_chunks;
   p.q_stride_b = int64_t(y.L) * y.Hq * y.D;
+  p.q_stride_l = int64_t(y.Hq) * y.D;
   p.out_stride_b = int64_t(y.L) * y.Hq * y.D;
+  p.out_stride_l = int64_t(y.Hq) * y.D;
   p.qscale = static_cast<float>(1.4426950408889634 / std::sqrt(double(y.D)));
-  // two buffers of partials and spilled logits, by layer parity
-  const size_t part_o_n = size_t(y.max_chunks) * y.Hkv * y.G * y.D;
-  const size_t part_mz_n = size_t(y.max_chunks) * y.Hkv * y.G;
-  const size_t spill_n = size_t(y.maxb) * y.Hkv * y.spill_stride;
+  // two buffers of partials and spilled logits, by launch parity
+  const size_t part_o_n = size_t(y.Lg) * y.max_chunks * y.Hkv * y.G * y.D;
+  const size_t part_mz_n = size_t(y.Lg) * y.max_chunks * y.Hkv * y.G;
+  const size_t spill_n = size_t(y.Lg) * y.Hkv * y.spill_stride;
   float* part_o = reinterpret_cast<float*>(h->D(y.o_part_o));
   float* part_m = reinterpret_cast<float*>(h->D(y.o_part_m));
   float* part_z = reinterpret_cast<float*>(h->D(y.o_part_z));
   float* spill = reinterpret_cast<float*>(h->D(y.o_spill));
-  p.spill_stride = y.spill_stride;
+  p.spill_stride_h = y.spill_stride;
+  p.spill_stride_l = int64_t(y.Hkv) * y.spill_stride;
+  p.spill_stride_b = 0;
   p.acc = reinterpret_cast<float*>(h->D(y.o_acc));
-  p.acc_stride_h = 3 * y.maxp * kPage;
-  p.acc_stride_b = int64_t(y.Hkv) * p.acc_stride_h;
+  p.acc_stride_h = y.total_pages * kPage;
+  p.acc_stride_l = int64_t(y.Hkv) * p.acc_stride_h;
+  p.acc_stride_b = 0;
   p.err = reinterpret_cast<int32_t*>(h->D(y.o_err));
+  p.wait_limit_ns = h->wait_limit_ns;
   const bool timing = h->cfg.flags & TKV_FLAG_TIMING;
   const int64_t abytes = attn_bytes_per_layer(h);
+  const bool stream = y.mode == TKV_HOST_TIERS_STREAM;
 
-  // Layer l's attention launch first finishes layer l - 1 (its output merge and
-  // score epilogue) in its consumer warps; the last layer's epilogue is a
-  // launch of its own after the loop.
-  for (int l = 0; l < y.L; ++l) {
+  // Each attention launch first finishes the previous launch's layers (their
+  // output merge and score epilogue) in its CTAs' tails; the last launch's
+  // epilogue is a launch of its own after the loop.
+  for (int l0 = 0; l0 < y.L; l0 += y.Lg) {
+    const int nl = std::min(y.Lg, y.L - l0);
     const int slot = h->slot_rr;
-    h->slot_rr ^= 1;
-    tkv_status st = enqueue_prefetch(h, l, slot, static_cast<uint32_t>(h->attn_launch_seq));
-    if (st) return st;
-    if (h->xs != h->cs) CK(h, cudaStreamWaitEvent(h->cs, h->ev_ready[slot], 0));
-    fill_sources(h, l, slot, p);
-    // consecutive launches alternate parity, across steps too (a step may have an odd layer count)
+    if (stream) {
+      h->slot_rr ^= 1;
+      tkv_status st = enqueue_prefetch(h, l0, nl, slot, static_cast<uint32_t>(h->last_launch_seq));
+      if (st) return st;
+      if (h->xs != h->cs) CK(h, cudaStreamWaitEvent(h->cs, h->ev_ready[slot], 0));
+    }
+    fill_sources(h, l0, slot, p);
+    // consecutive launches alternate parity, across steps too (a step may have an odd launch count)
     const int par = static_cast<int>(h->attn_launch_seq & 1);
     h->attn_launch_seq += 1;
     p.started = reinterpret_cast<uint32_t*>(h->D(y.o_err) + kStartedWordOffset);
@@ -681,8 +765,10 @@ tkv_status decode_step_device(tkv_ctx* h, const void* q, const void* k_new, cons
       p.span = spans + 2 * (h->attn_launch_seq % kSpanSlots);
       p.span_next = spans + 2 * ((h->attn_launch_seq + 1) % kSpanSlots);
     }
-    p.has_prev = l > 0;
-    p.ep_next = reinterpret_cast<int32_t*>(h->D(y.o_err)) + 4 + par;   // counters by layer parity
+    p.has_prev = l0 > 0;
+    p.prev_nlayers = p.nlayers;
+    p.nlayers = nl;
+    p.ep_next = reinterpret_cast<int32_t*>(h->D(y.o_err)) + 4 + par;   // counters by launch parity
     p.ep_clear = reinterpret_cast<int32_t*>(h->D(y.o_err)) + 4 + (par ^ 1);
     p.prev_part_o = p.part_o;
     p.prev_part_m = p.part_m;
@@ -693,22 +779,26 @@ tkv_status decode_step_device(tkv_ctx* h, const void* q, const void* k_new, cons
     p.part_m = part_m + par * part_mz_n;
     p.part_z = part_z + par * part_mz_n;
     p.spill = spill + par * spill_n;
-    p.q = static_cast<const char*>(q) + size_t(l) * y.Hq * y.D * y.esz;
-    p.out = static_cast<char*>(out) + size_t(l) * y.Hq * y.D * y.esz;
+    p.q = static_cast<const char*>(q) + size_t(l0) * y.Hq * y.D * y.esz;
+    p.out = static_cast<char*>(out) + size_t(l0) * y.Hq * y.D * y.esz;
+    p.stall_first_page = h->stall_next ? 1 : 0;
+    h->stall_next = false;
     TimedPair tp{};
     if (timing) {
-      st = timed_pair(h, 0, &tp);
+      tkv_status st = timed_pair(h, 0, &tp);
       if (st) return st;
       CK(h, cudaEventRecord(tp.a, h->cs));
     }
     LK(h, launch_attention_part(p, h->cfg.kv_dtype, total_chunks, h->cs, 0), total_chunks > 0);
+    if (total_chunks > 0) h->last_launch_seq = h->attn_launch_seq;
     if (timing) {
       CK(h, cudaEventRecord(tp.b, h->cs));
       h->pending.push_back(tp);
     }
-    CK(h, cudaEventRecord(h->ev_free[slot], h->cs));
+    if (stream) CK(h, cudaEventRecord(h->ev_free[slot], h->cs));
     h->stats.attn_launches += 1;
-    h->stats.attn_bytes += abytes;
+    h->stats.attn_layers += nl;
+    h->stats.attn_bytes += abytes * nl;
   }
   {
     TimedPair tc{};
@@ -725,12 +815,13 @@ tkv_status decode_step_device(tkv_ctx* h, const void* q, const void* k_new, cons
 
   // ---- fold this step's score increments into s (float64)
   FoldParams fp{};
-  fp.B = B; fp.Hkv = y.Hkv;
+  fp.B = B; fp.Hkv = y.Hkv; fp.nslices = y.Lg;
   fp.max_slots = 0;
   for (int b = 0; b < B; ++b) {
     for (int t = 0; t < 3; ++t) fp.npages[t][b] = p.npages[t][b];
     fp.max_slots = std::max<int64_t>(fp.max_slots, ntot[b] * kPage);
   }
+  for (int b = 0; b <= B; ++b) fp.page_base[b] = p.page_base[b];
   for (int t = 0; t < 3; ++t) {
     fp.table[t] = d_table(h, t);
     fp.mask[t] = d_mask(h, t);
@@ -740,7 +831,8 @@ tkv_status decode_step_device(tkv_ctx* h, const void* q, const void* k_new, cons
   fp.s = reinterpret_cast<double*>(h->D(y.o_s));
   fp.s_stride = y.maxtok;
   fp.acc = reinterpret_cast<float*>(h->D(y.o_acc));
-  fp.acc_stride = 3 * y.maxp * kPage;
+  fp.acc_stride_h = p.acc_stride_h;
+  fp.acc_stride_l = p.acc_stride_l;
   fp.inv_lh = 1.0 / (double(y.L) * double(y.Hq));
   LK(h, launch_fold(fp, h->cs), fp.B > 0 && fp.max_slots > 0);
 
@@ -801,6 +893,7 @@ tkv_status do_reclassify(tkv_ctx* h) {
     tkv_status st = sync_all(h);
     if (st) return st;
   }
+  const auto t_classified = std::chrono::steady_clock::now();
   const uint8_t* new_tiers = reinterpret_cast<const uint8_t*>(h->P(y.p_arena));
 
   // ---- allocator on a copy of the bookkeeping: a capacity failure changes nothing
@@ -887,8 +980,9 @@ tkv_status do_reclassify(tkv_ctx* h) {
       } else {
         phase1.push_back(mv);
       }
-      if (src_tier[m] == 1) h2d += row_full;
-      if (src_tier[m] == 2) h2d += row_i8;
+      const bool mirrored = y.mode == TKV_HOST_TIERS_MIRROR;  // T1 / T2 sources read from the device copy
+      if (src_tier[m] == 1 && !mirrored) h2d += row_full;
+      if (src_tier[m] == 2 && !mirrored) h2d += row_i8;
       if (dt == 1) d2h += row_full;
       if (dt == 2) d2h += row_i8;
     }
@@ -900,6 +994,7 @@ tkv_status do_reclassify(tkv_ctx* h) {
   }
 
   // ---- commit the bookkeeping, then move the data
+  const auto t_allocated = std::chrono::steady_clock::now();
   h->seqs.swap(seqs);
   char* arena = h->P(y.p_arena);
   const size_t moff = align_up(size_t(y.maxb) * y.maxtok);
@@ -923,6 +1018,11 @@ tkv_status do_reclassify(tkv_ctx* h) {
   mp.pools.t2_scale_layer_bytes = y.cap[2] * y.scale_rec;
   mp.pools.t2_scale_page_bytes = y.scale_rec;
   mp.pools.scale_per_head = h->cfg.t2_scale_gran == TKV_SCALE_PER_TOKEN_HEAD;
+  if (y.mode == TKV_HOST_TIERS_MIRROR) {
+    mp.pools.mirror[1] = h->D(y.o_mirror1);
+    mp.pools.mirror[2] = h->D(y.o_mirror2c);
+    mp.pools.mirror_scales = h->D(y.o_mirror2s);
+  }
   mp.pools.scale_f16 = h->cfg.t2_scale_dtype == TKV_SCALE_F16;
   mp.temp = h->D(y.o_temp);
   // Every source is read before any slot is written that a mover vacated:
@@ -955,9 +1055,14 @@ tkv_status do_reclassify(tkv_ctx* h) {
   h->stats.movers += int64_t(nmov);
   h->stats.d2h_move_bytes += d2h;
   h->stats.h2d_move_bytes += h2d;
-  if (h->cfg.flags & TKV_FLAG_TIMING)
-    h->stats.reclassify_ms +=
-        std::chrono::duration<double, std::milli>(std::chrono::steady_clock::now() - t_start).count();
+  if (h->cfg.flags & TKV_FLAG_TIMING) {
+    using ms = std::chrono::duration<double, std::milli>;
+    const auto t_end = std::chrono::steady_clock::now();
+    h->stats.reclassify_ms += ms(t_end - t_start).count();
+    h->stats.classify_ms += ms(t_classified - t_start).count();
+    h->stats.allocate_ms += ms(t_allocated - t_classified).count();
+    h->stats.move_ms += ms(t_end - t_allocated).count();
+  }
   return TKV_OK;
 }
 
@@ -1041,10 +1146,14 @@ tkv_status tkv_create(const tkv_config* cfg, void* dev_ws, size_t dev_bytes, voi
       {y.o_posmap, size_t(y.cap[0] + y.cap[1] + y.cap[2]) * kPage * 4, 0xff},
       {y.o_tier, size_t(y.maxb) * y.maxtok, 0},
       {y.o_s, size_t(y.maxb) * y.maxtok * 8, 0},
-      {y.o_acc, size_t(y.maxb) * y.Hkv * 3 * y.maxp * kPage * 4, 0},
-      {y.o_err, 64, 0}};
+      {y.o_acc, size_t(y.Lg) * y.Hkv * y.total_pages * kPage * 4, 0},
+      {y.o_err, 64, 0},
+      // device mirrors of the host tiers start as the (zeroed) host pools do
+      {y.o_mirror1, y.mode == TKV_HOST_TIERS_MIRROR ? size_t(y.L) * y.cap[1] * y.plb[1] : 0, 0},
+      {y.o_mirror2c, y.mode == TKV_HOST_TIERS_MIRROR ? size_t(y.L) * y.cap[2] * y.plb[2] : 0, 0},
+      {y.o_mirror2s, y.mode == TKV_HOST_TIERS_MIRROR ? size_t(y.L) * y.cap[2] * y.scale_rec : 0, 0}};
   for (const Z& z : zs)
-    if ((e = cudaMemsetAsync(h->D(z.off), z.val, z.bytes, h->cs)) != cudaSuccess)
+    if (z.bytes && (e = cudaMemsetAsync(h->D(z.off), z.val, z.bytes, h->cs)) != cudaSuccess)
       return bail(fail_cuda(nullptr, "cudaMemsetAsync", e));
   {
     std::vector<unsigned long long> init(2 * size_t(kSpanSlots), 0ull);
@@ -1159,12 +1268,21 @@ tkv_status tkv_reclassify(tkv_handle h) {
 tkv_status tkv_prefetch(tkv_handle h, int32_t layer, int32_t slot) {
   if (tkv_status st = check_usable(h)) return st;
   if (layer < 0 || layer >= h->y.L || slot < 0 || slot > 1) return fail(h, TKV_ERR_INVALID_ARG, "bad layer or slot");
-  return enqueue_prefetch(h, layer, slot);
+  return enqueue_prefetch(h, layer, std::min(h->y.Lg, h->y.L - layer), slot);
 }
 
 tkv_status tkv_synchronize(tkv_handle h) {
   if (tkv_status st = check_usable(h)) return st;
   return sync_all(h);
+}
+
+tkv_status tkv_test_stall_next_attention(tkv_handle h, uint64_t wait_limit_ns) {
+  if (tkv_status st = check_usable(h)) return st;
+  if (wait_limit_ns < 1000000ull || wait_limit_ns > 2000000000ull)
+    return fail(h, TKV_ERR_INVALID_ARG, "wait limit must be 1 ms .. 2 s");
+  h->stall_next = true;
+  h->wait_limit_ns = wait_limit_ns;
+  return TKV_OK;
 }
 
 tkv_status tkv_num_sequences(tkv_handle h, int32_t* n) {
@@ -1384,9 +1502,12 @@ tkv_status tkv_paged_attention(int32_t batch, int32_t n_q_heads, int32_t n_kv_he
   p.chunk_pages = plan_chunks(ntot, cost, n_kv_heads, 0, resident_attention_ctas(kv_dtype, G, head_dim), p.chunk_first);
   if (p.chunk_first[batch] > s.max_chunks) return fail(nullptr, TKV_ERR_INTERNAL, "chunk plan exceeds the scratch");
   const int64_t head_full = int64_t(2) * kPage * head_dim * esz;
-  p.src[0] = PageSource{static_cast<const char*>(pool), head_full * n_kv_heads, head_full, page_table, slot_mask,
-                        nullptr, nullptr, 0, 0, SRC_FULL, 0};
+  p.src[0] = PageSource{static_cast<const char*>(pool), 0, head_full * n_kv_heads, head_full, page_table, slot_mask,
+                        nullptr, nullptr, 0, 0, 0, SRC_FULL, 0, 0};
   p.nsrc = 1;
+  p.total_chunks = p.chunk_first[batch];
+  p.nlayers = 1;
+  for (int b = 0; b <= batch; ++b) p.page_base[b] = 0;
   p.q = q; p.q_stride_b = int64_t(n_q_heads) * head_dim;
   p.out = out; p.out_stride_b = int64_t(n_q_heads) * head_dim;
   p.qscale = static_cast<float>(1.4426950408889634 / std::sqrt(double(head_dim)));
@@ -1395,11 +1516,13 @@ tkv_status tkv_paged_attention(int32_t batch, int32_t n_q_heads, int32_t n_kv_he
   p.part_m = reinterpret_cast<float*>(sc + s.o_part_m);
   p.part_z = reinterpret_cast<float*>(sc + s.o_part_z);
   p.spill = reinterpret_cast<float*>(sc + s.o_spill);
-  p.spill_stride = s.spill_stride;
+  p.spill_stride_h = s.spill_stride;
+  p.spill_stride_b = int64_t(n_kv_heads) * s.spill_stride;
   p.acc = alpha_sum;
   p.acc_stride_b = int64_t(n_kv_heads) * max_pages * kPage;
   p.acc_stride_h = int64_t(max_pages) * kPage;
   p.err = reinterpret_cast<int32_t*>(sc + s.o_err);
+  p.wait_limit_ns = 2000000000ull;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e = cudaMemsetAsync(sc + s.o_err, 0, 64, st);
   if (e != cudaSuccess) return fail_cuda(nullptr, "cudaMemsetAsync", e);
@@ -1428,6 +1551,11 @@ tkv_status tkv_paged_attention_noalloc(int32_t batch, int32_t n_q_heads, int32_t
                                        float* alpha_sum, tkv_stream stream) {
   if (batch < 1 || batch > kMaxBatch || n_kv_heads < 1 || n_q_heads % n_kv_heads || max_pages < 1)
     return fail(nullptr, TKV_ERR_INVALID_ARG, "bad paged-attention shape");
+  // the checks tkv_paged_attention makes on the shape come first, so that an
+  // unsupported shape is not reported as one that needs a caller buffer
+  if (kv_dtype != TKV_DTYPE_F32 && kv_dtype != TKV_DTYPE_BF16) return fail(nullptr, TKV_ERR_INVALID_ARG, "kv_dtype");
+  if (!attention_supported(kv_dtype, n_q_heads / n_kv_heads, head_dim))
+    return fail(nullptr, TKV_ERR_INVALID_ARG, "unsupported group size or head_dim");
   const size_t need = paged_scratch(batch, n_q_heads, n_kv_heads, head_dim, max_pages).bytes;
   if (need > kStaticScratchBytes)
     return fail(nullptr, TKV_ERR_CAPACITY,
@@ -1451,6 +1579,25 @@ tkv_status tkv_paged_attention_noalloc(int32_t batch, int32_t n_q_heads, int32_t
   }
   return tkv_paged_attention(batch, n_q_heads, n_kv_heads, head_dim, kv_dtype, q, pool, page_table, slot_mask,
                              page_counts, max_pages, out, alpha_sum, scratch, kStaticScratchBytes, stream);
+}
+
+tkv_status tkv_paged_attention_noalloc_status(int32_t* host_out, tkv_stream stream) {
+  if (!host_out) return fail(nullptr, TKV_ERR_INVALID_ARG, "null output");
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail_cuda(nullptr, "cudaGetDevice", e);
+  {
+    std::lock_guard<std::mutex> lock(g_static_mu);
+    if (dev < 0 || dev >= kMaxDevices || !g_static_addr[dev])
+      return fail(nullptr, TKV_ERR_STATE, "no allocation-free call has run on this device");
+  }
+  // the status word is the first int32 of the array (offset 0 of the scratch layout)
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  e = cudaMemcpyFromSymbolAsync(host_out, g_static_scratch, sizeof(int32_t), 0, cudaMemcpyDeviceToHost, st);
+  if (e != cudaSuccess) return fail_cuda(nullptr, "cudaMemcpyFromSymbolAsync", e);
+  e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return fail_cuda(nullptr, "cudaStreamSynchronize", e);
+  return TKV_OK;
 }
 
 tkv_status tkv_classify_scratch_size(int32_t batch, int64_t stride, size_t* scratch_bytes) {

@@ -59,19 +59,28 @@ __host__ __device__ inline int64_t swz_offset(int row, int64_t byte_in_row, int 
 
 // One page source of the attention kernel: a page pool (or one layer of it).
 struct PageSource {
-  const char* base;          // page 0 of this source at the attended layer
+  const char* base;          // page 0 of this source at the launch's first layer
+  int64_t layer_bytes;       // bytes from one layer of the source to the next
   int64_t page_bytes;        // bytes per page record (all KV heads)
   int64_t head_bytes;        // bytes per KV head in a page record (its K block then V block)
   const int32_t* table;      // [B][table_stride] page ids in page order
   const uint32_t* mask;      // [pages] valid-slot bits
   const int32_t* posmap;     // [pages][16] position held by each slot (-1 hole); may be null
-  const char* scales;        // int8 sources: scale records of page 0
+  const char* scales;        // int8 sources: scale records of page 0 at the launch's first layer
+  int64_t scale_layer_bytes; // bytes from one layer of the scale records to the next
   int64_t scale_page_bytes;  // bytes per page of scale records
   int32_t scale_per_head;    // 0: [2][16] float32 per page; 1: [Hkv][2][16] float16
   int32_t kind;              // SrcKind
   int32_t swz;               // full-precision blocks: kSwizzle (library pools) or 0 (plain)
+  int32_t host;              // 1: pages sit in pinned host memory (device-mapped) and are read
+                             // in place with plain loads, never with bulk copies
 };
 
+// One attention launch covers `nlayers` consecutive layers (gridDim.z) of the
+// same chunk plan. Work unit (layer z, chunk c, KV head h) has index
+// (z * total_chunks + c) * Hkv + h in the partial buffers; its logits and
+// score increments sit at (page_base[b] + k) * 16 + row of its (z, b, h)
+// region (k = page index in the sequence's list).
 struct AttnParams {
   int32_t B, Hq, Hkv, D, G;
   int32_t nsrc;
@@ -79,26 +88,32 @@ struct AttnParams {
   int32_t table_stride;
   int32_t npages[3][kMaxBatch];
   int32_t chunk_first[kMaxBatch + 1];   // prefix sums of chunks per sequence
+  int32_t page_base[kMaxBatch + 1];     // spill / score slot base of each sequence, in pages
   int32_t chunk_pages;                  // upper bound of pages per chunk
-  const void* q;          // element (b, h, e) at q[b * q_stride_b + h * D + e]
-  int64_t q_stride_b;
+  int32_t total_chunks;                 // chunk_first[B]
+  int32_t nlayers;                      // layers in this launch
+  const void* q;          // element (z, b, h, e) at q[z * q_stride_l + b * q_stride_b + h * D + e]
+  int64_t q_stride_b, q_stride_l;
   void* out;
-  int64_t out_stride_b;
+  int64_t out_stride_b, out_stride_l;
   float qscale;           // log2(e) / sqrt(D): logits are kept in base 2
-  float* part_o;          // [chunk * Hkv + kvh][G][D]
-  float* part_m;          // [chunk * Hkv + kvh][G]
-  float* part_z;          // [chunk * Hkv + kvh][G]
-  float* spill;           // per (b, kvh) region of spill_stride floats: [page k][G][16]
-  int64_t spill_stride;
-  float* acc;             // score accumulator at [b * acc_stride_b + kvh * acc_stride_h + 16 k + row] (may be null)
-  int64_t acc_stride_b, acc_stride_h;
+  float* part_o;          // [unit][G][D]
+  float* part_m;          // [unit][G]
+  float* part_z;          // [unit][G]
+  float* spill;           // logits of (z, b, h): spill + z * spill_stride_l + b * spill_stride_b
+  int64_t spill_stride_l, spill_stride_b, spill_stride_h;   //  + h * spill_stride_h + (page_base[b] + k) * G * 16
+  float* acc;             // score increments of (z, b, h): acc + z * acc_stride_l + b * acc_stride_b
+  int64_t acc_stride_l, acc_stride_b, acc_stride_h;         //  + h * acc_stride_h + (page_base[b] + k) * 16 (may be null)
   int32_t* err;
-  // The previous layer of the same step (same chunk plan), whose output merge
+  unsigned long long wait_limit_ns;     // bounded waits give up after this long
+  int32_t stall_first_page;             // test hook: CTA (0, 0, 0) never issues its first page's copy
+  // The previous launch of the same step (same chunk plan), whose output merge
   // and score epilogue each CTA of this launch runs after its own pages
-  // (has_prev != 0).
+  // (has_prev != 0); it covered prev_nlayers layers.
   int32_t has_prev;
-  int32_t* ep_next;       // work counter of the previous layer's epilogue items (zero at launch)
-  int32_t* ep_clear;      // the other layer parity's counter, zeroed by this launch for the next one
+  int32_t prev_nlayers;
+  int32_t* ep_next;       // work counter of the previous launch's epilogue items (zero at launch)
+  int32_t* ep_clear;      // the other parity's counter, zeroed by this launch for the next one
   uint32_t* started;      // if set, the first CTA writes launch_seq here at entry
   uint32_t launch_seq;
   // if set: span[0] = min CTA start, span[1] = max CTA end (%globaltimer ns) of
@@ -170,6 +185,9 @@ struct Mover {
 
 struct TierPools {
   char* base[3];           // layer-major page pools (T1, T2 in host memory, device-mapped)
+  char* mirror[3];         // device-resident copies of the T1 / T2 pools (same layout) or null:
+                           // tokens entering T1 / T2 are written to both, sources are read from the copy
+  char* mirror_scales;
   int64_t layer_bytes[3];
   int64_t page_bytes[3];   // page record bytes (T2: int8 codes)
   char* t2_scales;         // layer-major scale records
@@ -188,11 +206,13 @@ struct MoveParams {
 };
 cudaError_t launch_move(const MoveParams& p, const Mover* movers, int64_t count, int layers, cudaStream_t s);
 
-// s[b][pos] += (sum over KV heads of acc at the slot holding pos) / (L * Hq);
-// slots follow the attention page order (T0, T1, then T2 page lists).
+// s[b][pos] += (sum over layer slices and KV heads of acc at the slot holding
+// pos) / (L * Hq); slots follow the attention page order (T0, T1, then T2 page
+// lists) from the sequence's page base; the accumulator is cleared.
 struct FoldParams {
-  int32_t B, Hkv;
+  int32_t B, Hkv, nslices;
   int32_t npages[3][kMaxBatch];
+  int32_t page_base[kMaxBatch + 1];
   const int32_t* table[3];
   int32_t table_stride;
   const uint32_t* mask[3];
@@ -200,8 +220,8 @@ struct FoldParams {
   int64_t max_slots;       // largest 16 * (pages of a sequence)
   double* s;               // [B][s_stride]
   int64_t s_stride;
-  float* acc;              // [B][Hkv][acc_stride]
-  int64_t acc_stride;
+  float* acc;              // [nslices][Hkv][acc_stride_h]
+  int64_t acc_stride_l, acc_stride_h;
   double inv_lh;           // 1 / (L * Hq)
 };
 cudaError_t launch_fold(const FoldParams& p, cudaStream_t s);
