@@ -28,6 +28,9 @@ sys.path.insert(0, ROOT)
 METRIC = "decode steps/s (KV-read GB/s as fraction of HBM peak in roofline)"
 
 
+NOMINAL_HBM_GBS = 7900.0   # GB300 HBM3e, nominal
+
+
 def _peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -58,14 +61,18 @@ def _workload(name):
     return WORKLOADS[name]
 
 
-def _config(w, n_ranks):
+def _config(w, n_ranks, args=None):
     lens = w.context_lens()
-    return {"workload": w.name, "batch": w.batch, "layers": w.n_layers, "q_heads": w.n_q_heads,
-            "kv_heads": w.n_kv_heads, "head_dim": w.head_dim, "kv_dtype": w.kv_dtype,
-            "context_tokens": {"min": min(lens), "max": max(lens), "mean": sum(lens) / len(lens)},
-            "budgets": list(w.budgets), "budget_mode": w.budget_mode, "delta": w.reclassify_interval,
-            "page_size": 16, "parallelism": f"replicas x{n_ranks}",
-            "l2": "inputs larger than L2: each step streams GBs of KV through the 129 MB L2"}
+    c = {"workload": w.name, "batch": w.batch, "layers": w.n_layers, "q_heads": w.n_q_heads,
+         "kv_heads": w.n_kv_heads, "head_dim": w.head_dim, "kv_dtype": w.kv_dtype,
+         "context_tokens": {"min": min(lens), "max": max(lens), "mean": sum(lens) / len(lens)},
+         "budgets": list(w.budgets), "budget_mode": w.budget_mode, "delta": w.reclassify_interval,
+         "page_size": 16, "parallelism": f"replicas x{n_ranks}",
+         "l2": "inputs larger than L2: each step streams GBs of KV through the 129 MB L2"}
+    if args is not None:
+        c["host_tiers"] = args.host_tiers
+        c["layers_per_launch"] = args.layers_per_launch or "auto"
+    return c
 
 
 # ------------------------------------------------------------------ clocks
@@ -139,6 +146,13 @@ def _max_over_ranks(ws, x, device):
     return float(t.item())
 
 
+def kernel_name(w):
+    """The attention kernel the workload's shape selects."""
+    if w.kv_dtype == "bf16" and w.group >= 2:
+        return "attn_split_mma_kernel"
+    return "attn_split_fma_kernel"
+
+
 # ------------------------------------------------------------------ GPU arm
 def run_gpu(args):
     import torch
@@ -188,6 +202,7 @@ def run_gpu(args):
         out = cache.decode_step(q, k, v, out)
     timed_inputs = [inputs(step + i + 1) for i in range(K)]
     torch.cuda.synchronize()
+    launches_before = cache.stats()["kernel_launches"]   # library launches before the timed region
     cache.reset_stats()
     stream = cache.compute
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -246,11 +261,23 @@ def run_gpu(args):
         torch.cuda.synchronize()
         best = min(best, e0.elapsed_time(e1))
     link_gbs = probe_h.numel() / best / 1e6
+    # the same copy from the cache's own pinned workspace (the T1 pool is its
+    # first region): tells a slow source buffer from a slow step pattern
+    pool_view = cache._pin[:min(cache._pin.numel(), 151 << 20)]
+    best_pool = 1e30
+    for _ in range(3):
+        e0.record()
+        probe_d[:pool_view.numel()].copy_(pool_view, non_blocking=True)
+        e1.record()
+        torch.cuda.synchronize()
+        best_pool = min(best_pool, e0.elapsed_time(e1))
+    pool_link_gbs = pool_view.numel() / best_pool / 1e6
     del probe_h, probe_d
 
     peak, peak_kind = _peaks()
     attn_ms = st["attn_ms"] / max(st["attn_launches"], 1)
-    combine_ms = st["combine_ms"] / max(st["attn_launches"], 1)
+    combine_ms = st["combine_ms"] / max(st["attn_launches"], 1)   # once per step, spread over the step's launches
+    layers_per_launch = st["attn_layers"] / max(st["attn_launches"], 1)
     bytes_per_launch = st["attn_bytes"] / max(st["attn_launches"], 1)
     achieved = bytes_per_launch / (attn_ms * 1e6) if attn_ms > 0 else 0.0
     pair = bytes_per_launch / ((attn_ms + combine_ms) * 1e6) if attn_ms > 0 else 0.0
@@ -264,21 +291,26 @@ def run_gpu(args):
         "metric": METRIC, "value": ws * K / (ms_max / 1000.0), "unit": "steps/s", "n_gpus": ws,
         "steps": K, "warmup": W, "ms_per_step": ms_max / K, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": w.kv_dtype, "data": "synthetic",
-        "config": _config(w, ws),
-        "roofline": {"bound": "hbm", "kernel": "attn_split_mma_kernel", "achieved": achieved, "peak": peak,
+        "config": _config(w, ws, args),
+        "roofline": {"bound": "hbm", "kernel": kernel_name(w), "achieved": achieved, "peak": peak,
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
+                     "frac_of_nominal": achieved / NOMINAL_HBM_GBS, "nominal_peak": NOMINAL_HBM_GBS,
                      "traffic": traffic, "bytes_per_launch": bytes_per_launch,
-                     "launch_ms": attn_ms, "combine_ms_per_layer": combine_ms,
+                     "layers_per_launch": layers_per_launch,
+                     "bytes_per_layer": bytes_per_launch / max(layers_per_launch, 1),
+                     "launch_ms": attn_ms, "combine_ms_per_launch": combine_ms,
                      "with_combine": {"achieved": pair, "frac": pair / peak},
                      # the kernel body alone: first CTA start to last CTA end (%globaltimer),
                      # without the launch and event overhead the CUDA-event figure includes
                      "device_span": {"us_per_launch": span_us, "achieved": span_gbs,
                                      "frac": span_gbs / peak if span_gbs else None}},
         "kv_read_gbs": achieved,
-        "link": {"prefetch_gbs": prefetch_gbs, "probe_h2d_gbs": link_gbs,
+        "link": {"prefetch_gbs": prefetch_gbs, "probe_h2d_gbs": link_gbs, "probe_pool_h2d_gbs": pool_link_gbs,
                  "frac": (prefetch_gbs / link_gbs) if prefetch_gbs else None,
                  "prefetch_bytes_per_step": st["prefetch_bytes"] / K},
         "reclassify_ms": st["reclassify_ms"] / max(st["reclassifies"], 1) if st["reclassifies"] else None,
+        "reclassify_breakdown_ms": ({k: st[k + "_ms"] / st["reclassifies"] for k in ("classify", "allocate", "move")}
+                                    if st["reclassifies"] else None),
         "reclassifies_in_timed_region": st["reclassifies"],
         "movers_per_reclassify": st["movers"] / max(st["reclassifies"], 1),
         "move_bytes_per_reclassify": {"h2d": st["h2d_move_bytes"] / max(st["reclassifies"], 1),
@@ -287,11 +319,15 @@ def run_gpu(args):
         "e2e": {"value": ws * K / e2e_s, "unit": "steps/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": launches,
+        "gpu_launches_before_timed": launches_before,
         "clocks": clocks,
         "prefill_s": prefill_s,
     }
     if rank == 0 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
+        # the oracle on one host core and on every host core (single-threaded processes)
+        one = cpu_baseline(w, args.cpu_seconds, workers=1)
+        line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds, workers=os.cpu_count() or 1)
+        line["cpu_baseline"]["one_core"] = {k: one[k] for k in ("value", "cores", "sample")}
     cache.close()
     if ws > 1:
         import torch.distributed as dist
@@ -307,11 +343,10 @@ sys.path.insert(0, {root!r})
 import numpy as np
 from synth import WORKLOADS
 from oracle import OracleCache
-from oracle.classify import T0
 w = WORKLOADS[{name!r}]
 budget = {budget}
-# one request at a time at the workload's full shape: prefill, then decode
-# steps of the oracle as it stands, until the time budget is used
+# one request at the workload's full shape: prefill, then decode steps of the
+# oracle as it stands, until the time budget is used
 lens = w.context_lens()
 order = sorted(range(w.batch), key=lambda b: lens[b])
 b = order[len(order) // 2]
@@ -319,32 +354,65 @@ one = w.replace(batch=1, context=("fixed", lens[b]), n_steps=64)
 oc = OracleCache.from_workload(one)
 n = lens[b]
 oc.append(0, one.kv_layers("k", 0, 0, n).float().numpy(), one.kv_layers("v", 0, 0, n).float().numpy(), False)
+inputs = [(one.queries(t).float().numpy(), one.kv_new("k", t).float().numpy(), one.kv_new("v", t).float().numpy())
+          for t in range(1, 9)]
+sys.stdout.write("ready\n"); sys.stdout.flush()
+sys.stdin.readline()             # all workers start timing together
 t0 = time.perf_counter()
 steps = 0
 while time.perf_counter() - t0 < budget and steps < 64:
     steps += 1
-    oc.decode_step(one.queries(steps).float().numpy(), one.kv_new("k", steps).float().numpy(), one.kv_new("v", steps).float().numpy())
+    oc.decode_step(*inputs[(steps - 1) % len(inputs)])
 el = time.perf_counter() - t0
 print(json.dumps({{"seconds": el, "request_steps": steps, "tokens": n}}))
 """
 
 
-def cpu_baseline(w, seconds):
+def _oracle_workers(w, seconds, workers):
+    """Run `workers` single-threaded oracle processes at once, each on the
+    median-length request; returns their results once all are done."""
     env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
                CUDA_VISIBLE_DEVICES="")
     code = _ORACLE_CHILD.format(root=ROOT, name=w.name, budget=seconds)
-    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env,
-                       timeout=seconds * 10 + 600)
-    if r.returncode != 0:
-        return {"value": None, "unit": "steps/s", "cores": 1, "kind": "oracle",
-                "sample": "failed: " + r.stderr.strip().splitlines()[-1] if r.stderr else "failed"}
-    d = json.loads(r.stdout.strip().splitlines()[-1])
-    # one full-batch step = w.batch request-steps (the sampled request is the median length)
-    per_request_step = d["seconds"] / d["request_steps"]
-    return {"value": 1.0 / (per_request_step * w.batch), "unit": "steps/s", "cores": 1, "kind": "oracle",
-            "sample": f"{d['request_steps']} decode steps of one median-length request "
-                      f"({d['tokens']} tokens, all {w.n_layers} layers) in {d['seconds']:.1f} s, "
-                      f"scaled to the {w.batch}-request batch"}
+    procs = [subprocess.Popen([sys.executable, "-c", code], stdin=subprocess.PIPE, stdout=subprocess.PIPE,
+                              stderr=subprocess.PIPE, text=True, env=env) for _ in range(workers)]
+    try:
+        for p in procs:                       # wait until every worker has its inputs
+            if p.stdout.readline().strip() != "ready":
+                raise RuntimeError(p.stderr.read()[-500:])
+        for p in procs:
+            p.stdin.write("go\n")
+            p.stdin.flush()
+        out = []
+        for p in procs:
+            o, e = p.communicate(timeout=seconds * 10 + 600)
+            if p.returncode != 0:
+                raise RuntimeError(e.strip().splitlines()[-1] if e.strip() else "failed")
+            out.append(json.loads(o.strip().splitlines()[-1]))
+        return out
+    finally:
+        for p in procs:
+            if p.poll() is None:
+                p.kill()
+
+
+def cpu_baseline(w, seconds, workers=1):
+    """The oracle timed on the host: `workers` single-threaded processes at
+    once, each decoding the median-length request; the batch step rate is the
+    aggregate request-step rate divided by the batch size."""
+    try:
+        res = _oracle_workers(w, seconds, workers)
+    except Exception as e:   # noqa: BLE001 - reported in the line, not raised
+        return {"value": None, "unit": "steps/s", "cores": workers, "kind": "oracle", "sample": f"failed: {e}"}
+    req_steps = sum(r["request_steps"] for r in res)
+    wall = max(r["seconds"] for r in res)
+    rate = req_steps / wall                   # request-steps per second over all workers
+    return {"value": rate / w.batch, "unit": "steps/s", "cores": workers, "kind": "oracle",
+            "request_steps": req_steps, "seconds": wall, "request_steps_per_s": rate,
+            "batch_timed": 1, "extrapolated_to_batch": w.batch,
+            "sample": f"{workers} single-threaded oracle process(es) at once, {req_steps} decode steps in all of "
+                      f"one median-length request ({res[0]['tokens']} tokens, all {w.n_layers} layers) "
+                      f"in {wall:.1f} s; batch step rate = request-step rate / {w.batch}"}
 
 
 def run_reference(args):
@@ -352,15 +420,28 @@ def run_reference(args):
     if rank != 0:
         return
     w = _workload(args.workload)
-    K = args.steps
-    cb = cpu_baseline(w, args.cpu_seconds)
+    cores = os.cpu_count() or 1
+    cb = cpu_baseline(w, args.cpu_seconds, workers=cores)
     v = cb["value"]
+    # what was timed: request-steps (one request, all layers) on every host core
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "steps/s", "n_gpus": ws,
-            "steps": K, "warmup": args.warmup, "ms_per_step": 1000.0 / v if v else None,
+            "steps": cb.get("request_steps"), "step_unit": "one decode step of one request (all layers)",
+            "warmup": args.warmup,
+            # wall time per request-step over all cores: steps x ms_per_step = the timed seconds
+            "ms_per_step": 1000.0 * cb["seconds"] / cb["request_steps"] if v else None,
+            "batch_timed": 1, "extrapolated_to_batch": w.batch,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": _config(w, ws), "cpu_baseline": cb,
             "e2e": {"value": v, "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
+
+
+def _spawn_replicas(n):
+    """--gpus N outside torchrun: run N replica ranks (one per GPU) under
+    torch.distributed.run; rank 0 prints the line."""
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={n}",
+           "--master-addr", "127.0.0.1", "--master-port", str(29500 + os.getpid() % 1000)] + sys.argv
+    return subprocess.call(cmd)
 
 
 def main():
@@ -370,7 +451,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["gpu", "reference"], default="gpu")
     ap.add_argument("--workload", default="batch32")
-    ap.add_argument("--cpu-seconds", type=float, default=20.0)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--layers", type=int, default=0, help="override the layer count (profiling a small case)")
     ap.add_argument("--split-pages", type=int, default=0, help="pages per attention CTA (0: planned)")
@@ -381,6 +462,13 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    ws = int(os.environ.get("WORLD_SIZE", "0"))
+    if args.gpus < 1:
+        sys.exit("--gpus must be >= 1")
+    if ws == 0 and args.gpus > 1:
+        sys.exit(_spawn_replicas(args.gpus))
+    if ws and ws != args.gpus:
+        sys.exit(f"--gpus {args.gpus} but WORLD_SIZE={ws}: launch one rank per GPU")
     if args.impl == "reference":
         run_reference(args)
     else:

@@ -111,8 +111,9 @@ typedef struct {
   int32_t flags;                                      /* TKV_FLAG_* */
   int32_t host_tiers;                                 /* TKV_HOST_TIERS_* */
   int32_t layers_per_launch;                          /* layers one attention launch covers (and one
-                                                         prefetch copies in STREAM mode); 0 = auto:
-                                                         the largest divisor of n_layers up to 7 */
+                                                         prefetch copies in STREAM mode), at most 32;
+                                                         0 = auto: the largest divisor of n_layers
+                                                         up to 7 */
 } tkv_config;
 
 typedef struct {

@@ -64,3 +64,11 @@ def test_single_rank_needs_no_process_group():
 
 if __name__ == "__main__":
     pytest.main([__file__, "-q"])
+
+
+def test_bench_refuses_a_gpu_count_that_does_not_match_the_ranks():
+    import subprocess
+    env = dict(os.environ, WORLD_SIZE="1", RANK="0", LOCAL_RANK="0", CUDA_VISIBLE_DEVICES="")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--gpus", "2"], capture_output=True,
+                       text=True, env=env, timeout=120)
+    assert r.returncode != 0 and "WORLD_SIZE=1" in r.stderr

@@ -2,10 +2,11 @@
 launch configuration bench.py times: 32 requests of 1k-8k tokens, 28 layers,
 28 query / 4 KV heads, d = 128, bf16, budgets 40/40/10/10.
 
-The oracle cannot hold 8.5 GB of float64 state, so it keeps bookkeeping only
-(tiers, slots) and recomputes sampled outputs, scores and codes one by one from
-slices regenerated on the CPU. Seeded synthetic scores put the cache in a
-tiered state; then one decode step runs.
+The oracle cannot hold 8.5 GB of float64 state at once, so it keeps
+bookkeeping only (tiers, slots) and recomputes, one (request, layer) at a time
+from regenerated inputs, every request's scores and all layers and heads of
+four requests' outputs. Seeded synthetic scores put the cache in a tiered
+state; then one decode step runs.
 """
 import numpy as np
 import pytest
@@ -44,6 +45,8 @@ def state():
         oc.append(b, None, None, False, n=1)
     yield dict(w=w, cache=cache, oc=oc, s0=s0, q=q.float().numpy(), out=out, tiers=tiers_before)
     cache.close()
+    del cache
+    torch.cuda.empty_cache()
 
 
 def test_tiers_and_page_tables_bit_exact(state):
@@ -55,39 +58,53 @@ def test_tiers_and_page_tables_bit_exact(state):
     assert np.all(counts > 0)
 
 
-def test_sampled_outputs(state):
-    w, out, q = state["w"], state["out"], state["q"]
+@pytest.fixture(scope="module")
+def oracle_pass(state):
+    """The oracle over every (request, layer) of the step: all heads' outputs of
+    four requests (the shortest, two of median length, the longest), and every
+    request's score increments. Inputs are regenerated on the device (the same
+    bits as on the CPU) and all arithmetic runs in float64 on the CPU."""
+    w, q = state["w"], state["q"]
     lens = w.context_lens()
-    order = np.argsort(lens)
-    samples = [(int(order[0]), 0, 0), (int(order[0]), 27, 27), (int(order[-1]), 13, 6),
-               (int(order[-1]), 0, 7), (int(order[15]), 27, 20), (int(order[16]), 5, 13)]
-    for b, l, h in samples:
+    order = [int(i) for i in np.argsort(lens)]
+    picked = {order[0], order[15], order[16], order[-1]}
+    outs, scores = {}, {}
+    for b in range(w.batch):
         n_total = lens[b] + 1
         tiers = state["oc"].seqs[b].tier
-        ref, _, _ = layer_attention(w, b, l, q[b, l], tiers, n_total)
-        err = np.max(np.abs(out[b, l, h] - ref[h]))
-        assert err <= OUT_ATOL, (b, l, h, err)
+        acc = np.zeros(n_total)
+        for l in range(w.n_layers):
+            ref, alpha, R = layer_attention(w, b, l, q[b, l], tiers, n_total, gen_device=DEV)
+            acc[R] += alpha.mean(axis=0)
+            if b in picked:
+                outs[(b, l)] = ref
+        scores[b] = np.concatenate([state["s0"][b], [0.0]]) + acc / w.n_layers
+    return outs, scores
 
 
-def test_scores_of_two_requests_and_sum_property(state):
+def test_outputs_of_four_requests_every_layer_and_head(state, oracle_pass):
+    outs, _ = oracle_pass
+    worst = 0.0
+    for (b, l), ref in outs.items():
+        err = float(np.max(np.abs(state["out"][b, l] - ref)))
+        worst = max(worst, err)
+        assert err <= OUT_ATOL, (b, l, err)
+    assert len(outs) == 4 * state["w"].n_layers
+
+
+def test_scores_of_every_request_and_sum_property(state, oracle_pass):
     w, cache, oc = state["w"], state["cache"], state["oc"]
+    _, want = oracle_pass
     lens = w.context_lens()
     for b in range(w.batch):
-        ds = cache.scores(b)[:lens[b]] - state["s0"][b]
+        got = cache.scores(b)
+        ds = got[:lens[b]] - state["s0"][b]
         tiers = oc.seqs[b].tier
         # one step: increments over the retained set sum to 1 (the new token's
         # own weight is its score, since its previous score is 0)
-        total = ds[tiers[:lens[b]] != 3].sum() + cache.scores(b)[lens[b]]
+        total = ds[tiers[:lens[b]] != 3].sum() + got[lens[b]]
         assert abs(total - 1.0) < 1e-4, (b, total)
-    for b in [int(i) for i in np.argsort(lens)[:2]]:
-        n_total = lens[b] + 1
-        tiers = oc.seqs[b].tier
-        acc = np.zeros(n_total)
-        for l in range(w.n_layers):
-            _, alpha, R = layer_attention(w, b, l, state["q"][b, l], tiers, n_total)
-            acc[R] += alpha.mean(axis=0)
-        want = np.concatenate([state["s0"][b], [0.0]]) + acc / w.n_layers
-        assert_scores_close(cache.scores(b), want, f"request {b}")
+        assert_scores_close(got, want[b], f"request {b}")
 
 
 def test_sampled_t2_codes(state):

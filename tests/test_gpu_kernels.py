@@ -57,6 +57,35 @@ def test_classifier_is_bit_exact(seed):
         assert np.array_equal(got[b, :N], want[b, :N]), f"request {b}"
 
 
+@pytest.mark.parametrize("seed", range(4))
+def test_classifier_is_bit_exact_across_many_slices(seed):
+    """Long sequences span many 4096-position slices of the select; with only a
+    few distinct scores the ties at each boundary cross slice borders."""
+    from tiered_kv_cache_split_gb300 import classify
+    rng = np.random.default_rng(100 + seed)
+    B, stride = 3, 40000
+    s = np.zeros((B, stride))
+    old = np.zeros((B, stride), dtype=np.uint8)
+    params = np.zeros((B, 5), dtype=np.int64)
+    want = np.zeros((B, stride), dtype=np.uint8)
+    n_sink, W = 4, int(rng.integers(0, 3000))
+    for b in range(B):
+        N = int(rng.integers(stride // 2, stride + 1))
+        plen = int(rng.integers(0, 5000))
+        s[b, :N] = rng.integers(0, 6 + 10 * seed, N) / 8.0
+        P = protected_mask(N, plen, n_sink, W)
+        old[b, :N] = np.where(~P & (rng.random(N) < 0.05), 3, rng.integers(0, 3, N))
+        n1, n2 = int(rng.integers(0, N // 3)), int(rng.integers(0, N // 3))
+        n0 = int(rng.integers(0, N // 2))
+        params[b] = (N, plen, n0, n1, n2)
+        want[b, :N] = oracle_classify(s[b, :N], old[b, :N], plen, n_sink, W, n0, n1, n2)
+    got = classify(torch.from_numpy(s).to(DEV), torch.from_numpy(old).to(DEV), params, n_sink, W)
+    got = got.cpu().numpy()
+    for b in range(B):
+        N = params[b, 0]
+        assert np.array_equal(got[b, :N], want[b, :N]), f"request {b}"
+
+
 @pytest.mark.parametrize("dtype,scale", [("bf16", "f32"), ("f32", "f32"), ("bf16", "f16"), ("f32", "f16")])
 def test_quantiser_is_bit_exact(dtype, scale):
     from tiered_kv_cache_split_gb300 import quantize_rows as q_gpu

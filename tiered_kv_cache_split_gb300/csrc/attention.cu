@@ -501,13 +501,16 @@ struct LayerBufs {
   const float* part_z;
   const float* spill;
   void* out;
+  float* acc;   // score accumulator slice of the launch's first layer
 };
 
-// `part` / `parts` take a share of the chunk's slots (the output merge goes with
-// part 0), so that the work can be handed out in smaller pieces.
+// Every epilogue item is read after the grid that wrote it has finished, so the
+// read-only path is safe.
+__device__ __forceinline__ float ld_part(const float* p) { return __ldg(p); }
+
 template <typename T, int G, int D, int NT, typename Sync>
 __device__ void layer_epilogue(const AttnParams& p, const LayerBufs& lb, const Work& wk, int tid,
-                               float* sM, float* sIZ, Sync sync, int part = 0, int parts = 1) {
+                               float* sM, float* sIZ, Sync sync) {
   const int warp = tid >> 5, lane = tid & 31;
   const int64_t base = unit_index(p, wk.z, wk.cf, wk.kvh);  // partial of chunk j: base + j * Hkv
   const int nch = wk.nch;
@@ -518,11 +521,12 @@ __device__ void layer_epilogue(const AttnParams& p, const LayerBufs& lb, const W
     for (int r = 0; r < 2; ++r) {
       const int j = lane + 32 * r;
       const int64_t pj = (base + static_cast<int64_t>(j) * p.Hkv) * G + g;
-      mj[r] = j < nch ? __ldg(lb.part_m + pj) : -INFINITY;
-      zj[r] = j < nch ? __ldg(lb.part_z + pj) : 0.f;
+      mj[r] = j < nch ? ld_part(lb.part_m + pj) : -INFINITY;
+      zj[r] = j < nch ? ld_part(lb.part_z + pj) : 0.f;
     }
     float M = fmaxf(mj[0], mj[1]);
-    for (int j = lane + 64; j < nch; j += 32) M = fmaxf(M, __ldg(lb.part_m + (base + static_cast<int64_t>(j) * p.Hkv) * G + g));
+    for (int j = lane + 64; j < nch; j += 32)
+      M = fmaxf(M, ld_part(lb.part_m + (base + static_cast<int64_t>(j) * p.Hkv) * G + g));
 #pragma unroll
     for (int m = 16; m >= 1; m >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, m));
     float Z = 0.f;
@@ -532,8 +536,8 @@ __device__ void layer_epilogue(const AttnParams& p, const LayerBufs& lb, const W
         if (mj[r] != -INFINITY) Z += zj[r] * exp2f(mj[r] - M);
       for (int j = lane + 64; j < nch; j += 32) {
         const int64_t pj = (base + static_cast<int64_t>(j) * p.Hkv) * G + g;
-        const float m2 = __ldg(lb.part_m + pj);
-        if (m2 != -INFINITY) Z += __ldg(lb.part_z + pj) * exp2f(m2 - M);
+        const float m2 = ld_part(lb.part_m + pj);
+        if (m2 != -INFINITY) Z += ld_part(lb.part_z + pj) * exp2f(m2 - M);
       }
     }
 #pragma unroll
@@ -544,7 +548,7 @@ __device__ void layer_epilogue(const AttnParams& p, const LayerBufs& lb, const W
     }
   }
   sync();
-  if (part == 0) {
+  {
     // this chunk's slice of the G * D outputs
     const int lo = static_cast<int>((static_cast<int64_t>(wk.jc) * G * D) / nch);
     const int hi = static_cast<int>((static_cast<int64_t>(wk.jc + 1) * G * D) / nch);
@@ -558,16 +562,16 @@ __device__ void layer_epilogue(const AttnParams& p, const LayerBufs& lb, const W
 #pragma unroll 4
         for (int j = 0; j < nch; ++j) {
           const int64_t pj = base + static_cast<int64_t>(j) * p.Hkv;
-          const float mj = __ldg(lb.part_m + pj * G + g);
-          if (mj != -INFINITY) o += __ldg(lb.part_o + pj * G * D + idx) * (exp2f(mj - Mg) * IZg);
+          const float mj = ld_part(lb.part_m + pj * G + g);
+          if (mj != -INFINITY) o += ld_part(lb.part_o + pj * G * D + idx) * (exp2f(mj - Mg) * IZg);
         }
       }
       store_out(out + idx, o);
     }
   }
-  if (p.acc == nullptr) return;
+  if (lb.acc == nullptr) return;
   const float* __restrict__ spill_b = spill_of(p, const_cast<float*>(lb.spill), wk);
-  float* __restrict__ accb = p.acc + wk.z * p.acc_stride_l + static_cast<int64_t>(wk.b) * p.acc_stride_b +
+  float* __restrict__ accb = lb.acc + wk.z * p.acc_stride_l + static_cast<int64_t>(wk.b) * p.acc_stride_b +
                              static_cast<int64_t>(wk.kvh) * p.acc_stride_h + static_cast<int64_t>(p.page_base[wk.b]) * kPage;
   float M[G], IZ[G];
 #pragma unroll
@@ -576,10 +580,8 @@ __device__ void layer_epilogue(const AttnParams& p, const LayerBufs& lb, const W
     IZ[g] = sIZ[g];
   }
   constexpr int U = 4;
-  const int all = wk.npg * kPage;
-  const int lo = static_cast<int>((static_cast<int64_t>(part) * all) / parts);
-  const int items = static_cast<int>((static_cast<int64_t>(part + 1) * all) / parts);
-  for (int first = lo + tid; first < items; first += NT * U) {
+  const int items = wk.npg * kPage;
+  for (int first = tid; first < items; first += NT * U) {
     float l[U][G], old[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
@@ -587,8 +589,8 @@ __device__ void layer_epilogue(const AttnParams& p, const LayerBufs& lb, const W
       if (item < items) {
         const int k = wk.k0 + (item >> 4), row = item & 15;
 #pragma unroll
-        for (int g = 0; g < G; ++g) l[u][g] = __ldg(spill_b + (static_cast<int64_t>(k) * G + g) * kPage + row);
-        old[u] = accb[static_cast<int64_t>(k) * kPage + row];
+        for (int g = 0; g < G; ++g) l[u][g] = ld_part(spill_b + (static_cast<int64_t>(k) * G + g) * kPage + row);
+        old[u] = __ldcg(accb + static_cast<int64_t>(k) * kPage + row);  // neighbouring chunks share lines
       }
     }
 #pragma unroll
@@ -605,19 +607,49 @@ __device__ void layer_epilogue(const AttnParams& p, const LayerBufs& lb, const W
   }
 }
 
-// The epilogue of a launch's layers as a kernel of its own: one CTA per (chunk,
-// KV head, layer), launched as a programmatic dependent of that attention launch
-// (used for a lone call, and for the last launch of a decode step).
+// Work unit of epilogue item `item` of a launch: items run layer by layer, and
+// within a layer over (KV head, chunk).
+__device__ __forceinline__ Work epilogue_work(const AttnParams& p, int item) {
+  const int cu = item % p.total_chunks, rest = item / p.total_chunks;
+  return find_work_at(p, cu, rest % p.Hkv, rest / p.Hkv);
+}
+
+// Claims an epilogue item of a finished launch: the next unclaimed (KV head,
+// chunk) of its first layer that has one left, as layer * per_layer + index,
+// or -1 when none is left. Every claim is one fetch-and-add on that layer's
+// counter, so CTAs that finish together never retry against one another.
+__device__ __forceinline__ int claim_item(EpCounters* ctr, int nlayers, int per_layer) {
+  for (int z = 0; z < nlayers; ++z) {
+    if (*reinterpret_cast<volatile int32_t*>(ctr->claim + z) >= per_layer) continue;  // layer handed out
+    const int i = atomicAdd(ctr->claim + z, 1);
+    if (i < per_layer) return z * per_layer + i;
+  }
+  return -1;
+}
+
+// The epilogue of a launch's items left over after its own CTAs, as a kernel of
+// its own launched as a programmatic dependent of that attention launch (for a
+// lone call, and for the last launch of a decode step): CTAs claim the items
+// still unclaimed in the launch's counters.
 constexpr int kCombineThreads = 256;
 
 template <typename T, int G, int D>
 __global__ void __launch_bounds__(kCombineThreads) attn_combine_kernel(const __grid_constant__ AttnParams p) {
   __shared__ float sM[8], sIZ[8];
-  const Work wk = find_work(p);
+  __shared__ int s_item;
+  const int per_layer = p.total_chunks * p.Hkv;
   // wait here until the attention kernel's partials and spilled logits are complete and visible
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  const LayerBufs lb{p.part_o, p.part_m, p.part_z, p.spill, p.out};
-  layer_epilogue<T, G, D, kCombineThreads>(p, lb, wk, threadIdx.x, sM, sIZ, [] { __syncthreads(); });
+  const LayerBufs lb{p.part_o, p.part_m, p.part_z, p.spill, p.out, p.acc};
+  for (;;) {
+    __syncthreads();
+    if (threadIdx.x == 0) s_item = claim_item(p.ep_own, p.nlayers, per_layer);
+    __syncthreads();
+    const int item = s_item;
+    if (item < 0) break;
+    layer_epilogue<T, G, D, kCombineThreads>(p, lb, epilogue_work(p, item), threadIdx.x, sM, sIZ,
+                                             [] { __syncthreads(); });
+  }
 }
 
 // The previous launch's epilogue, run by all warps of an attention CTA once its
@@ -625,27 +657,25 @@ __global__ void __launch_bounds__(kCombineThreads) attn_combine_kernel(const __g
 // while the last ones still stream, and it never holds up the ring. Same
 // (chunk, KV head) split, since every layer of a step has the same chunk plan.
 // The items — one per (layer, KV head, chunk) of the previous launch — are
-// handed out by a counter, so CTAs that finish their pages early take most of
-// them and the last CTAs to finish find none left.
+// handed out by that launch's counters, so CTAs that finish their pages early
+// take most of them and the last CTAs to finish find none left. (Taking items
+// of this launch's own completed layers as well, with per-layer completion
+// counts, measured slower: those items then displace page streaming instead of
+// filling the launch's tail.)
 template <typename T, int G, int D>
-__device__ __forceinline__ void prev_layer_epilogue(const AttnParams& p, int tid, float* sM, float* sIZ,
-                                                    volatile int* s_item) {
+__device__ __forceinline__ void prev_launch_epilogue(const AttnParams& p, int tid, float* sM, float* sIZ,
+                                                     volatile int* s_item) {
   if (!p.has_prev) return;
-  const LayerBufs lb{p.prev_part_o, p.prev_part_m, p.prev_part_z, p.prev_spill, p.prev_out};
-  constexpr int kParts = 1;  // pieces per (chunk, KV head)
-  const int units = p.total_chunks * p.Hkv * p.prev_nlayers;  // the previous launch's (layer, KV head, chunk) items
-  const int items = units * kParts;
+  constexpr int NT = (kAttnWarps + 1) * 32;
+  const int per_layer = p.total_chunks * p.Hkv;
+  const LayerBufs lb{p.prev_part_o, p.prev_part_m, p.prev_part_z, p.prev_spill, p.prev_out, p.acc};
   for (;;) {
     __syncthreads();
-    if (tid == 0) *s_item = atomicAdd(p.ep_next, 1);
+    if (tid == 0) *s_item = claim_item(p.ep_prev, p.prev_nlayers, per_layer);
     __syncthreads();
     const int item = *s_item;
-    if (item >= items) break;
-    const int unit = item / kParts;
-    const int cu = unit % p.total_chunks, rest = unit / p.total_chunks;
-    const Work wk = find_work_at(p, cu, rest % p.Hkv, rest / p.Hkv);
-    layer_epilogue<T, G, D, (kAttnWarps + 1) * 32>(p, lb, wk, tid, sM, sIZ, [] { __syncthreads(); },
-                                                   item % kParts, kParts);
+    if (item < 0) break;
+    layer_epilogue<T, G, D, NT>(p, lb, epilogue_work(p, item), tid, sM, sIZ, [] { __syncthreads(); });
   }
 }
 
@@ -725,7 +755,8 @@ __global__ void __launch_bounds__((kAttnWarps + 1) * 32, 3)
       p.span_next[0] = ~0ull;
       p.span_next[1] = 0ull;
     }
-    if (p.ep_clear) *p.ep_clear = 0;  // the next launch's counter
+    if (p.ep_clear)  // counters of the launch after next
+      for (int z = 0; z < kMaxLaunchLayers; ++z) p.ep_clear->claim[z] = 0;
     if (p.started) {                  // tells the copy stream this launch is under way
       asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p.started), "r"(p.launch_seq) : "memory");
     }
@@ -920,7 +951,7 @@ __global__ void __launch_bounds__((kAttnWarps + 1) * 32, 3)
   }
   __syncthreads();
   write_partial<T, G, D>(p, wk, smem);
-  prev_layer_epilogue<T, G, D>(p, tid, s_epM, s_epIZ, &s_item);
+  prev_launch_epilogue<T, G, D>(p, tid, s_epM, s_epIZ, &s_item);
   if (tid == 0 && p.span) atomicMax(p.span + 1, global_ns());
 }
 
@@ -1024,7 +1055,8 @@ __global__ void __launch_bounds__((kAttnWarps + 1) * 32)
       p.span_next[0] = ~0ull;
       p.span_next[1] = 0ull;
     }
-    if (p.ep_clear) *p.ep_clear = 0;  // the next launch's counter
+    if (p.ep_clear)  // counters of the launch after next
+      for (int z = 0; z < kMaxLaunchLayers; ++z) p.ep_clear->claim[z] = 0;
     if (p.started) {                  // tells the copy stream this launch is under way
       asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p.started), "r"(p.launch_seq) : "memory");
     }
@@ -1291,7 +1323,7 @@ __global__ void __launch_bounds__((kAttnWarps + 1) * 32)
   }
   __syncthreads();
   write_partial<T, G, D>(p, wk, smem);
-  prev_layer_epilogue<T, G, D>(p, tid, s_epM, s_epIZ, &s_item);
+  prev_launch_epilogue<T, G, D>(p, tid, s_epM, s_epIZ, &s_item);
   if (tid == 0 && p.span) atomicMax(p.span + 1, global_ns());
 }
 

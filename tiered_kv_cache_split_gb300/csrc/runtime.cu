@@ -43,6 +43,9 @@ thread_local std::string g_last_error = "no error";
 
 constexpr size_t kAlign = 256;
 constexpr size_t kStartedWordOffset = 32;  // byte offset of the started word in the error region
+constexpr size_t kEpOffset = 64;           // byte offset of the epilogue counter sets in the error region
+constexpr size_t kErrRegion = 2048;        // bytes of the error region
+static_assert(kEpOffset + 4 * sizeof(EpCounters) <= kErrRegion, "error region too small");
 size_t align_up(size_t x, size_t a = kAlign) { return (x + a - 1) / a * a; }
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -70,7 +73,7 @@ struct Layout {
   int64_t max_chunks, spill_stride, temp_rows;
   // device offsets
   size_t o_pool0, o_stage1, o_stage2c, o_stage2s, o_mirror1, o_mirror2c, o_mirror2s, o_table, o_mask, o_posmap, o_tier, o_tier_new,
-      o_s, o_acc, o_part_o, o_part_m, o_part_z, o_spill, o_keys, o_err, o_span, o_movers,
+      o_s, o_acc, o_part_o, o_part_m, o_part_z, o_spill, o_keys, o_cls_state, o_cls_ties, o_err, o_span, o_movers,
       o_temp, o_locs, o_io, dev_bytes;
   size_t io_q, io_k, io_out;
   // pinned offsets
@@ -135,7 +138,7 @@ std::string validate(const tkv_config& c) {
 // the staging ring holds two groups, so the grouping costs 2 x 7 layers of the
 // used T1 / T2 range in HBM.
 int layers_per_launch(const tkv_config& c) {
-  if (c.layers_per_launch > 0) return std::min(c.layers_per_launch, c.n_layers);
+  if (c.layers_per_launch > 0) return std::min({c.layers_per_launch, c.n_layers, kMaxLaunchLayers});
   const int cap = 7;
   int best = 1;
   for (int g = 1; g <= std::min(cap, c.n_layers); ++g)
@@ -196,7 +199,9 @@ Layout make_layout(const tkv_config& c) {
   y.o_part_z = take(2 * size_t(y.Lg) * y.max_chunks * y.Hkv * y.G * 4);
   y.o_spill = take(2 * size_t(y.Lg) * y.Hkv * y.spill_stride * 4);
   y.o_keys = take(size_t(y.maxb) * y.maxtok * 8);
-  y.o_err = take(64);   // int32 [0]: device error word; [4], [5]: epilogue work counters by layer parity;
+  y.o_cls_state = take(size_t(y.maxb) * sizeof(ClassifyState));
+  y.o_cls_ties = take(size_t(y.maxb) * classify_slices(y.maxtok) * 3 * 8);
+  y.o_err = take(kErrRegion);   // int32 [0]: device error word; from byte 64: four sets of epilogue counters;
                         // [8]: sequence number of the last attention launch that started
   y.o_span = take(size_t(kSpanSlots) * 16);  // device span (start, end) of attention launches, by sequence number
   y.o_movers = take(2 * size_t(y.maxb) * y.maxtok * sizeof(Mover));
@@ -732,10 +737,11 @@ tkv_status decode_step_device(tkv_ctx* h, const void* q, const void* k_new, cons
   p.spill_stride_h = y.spill_stride;
   p.spill_stride_l = int64_t(y.Hkv) * y.spill_stride;
   p.spill_stride_b = 0;
-  p.acc = reinterpret_cast<float*>(h->D(y.o_acc));
+  float* acc = reinterpret_cast<float*>(h->D(y.o_acc));
   p.acc_stride_h = y.total_pages * kPage;
   p.acc_stride_l = int64_t(y.Hkv) * p.acc_stride_h;
   p.acc_stride_b = 0;
+  EpCounters* ring = reinterpret_cast<EpCounters*>(h->D(y.o_err) + kEpOffset);
   p.err = reinterpret_cast<int32_t*>(h->D(y.o_err));
   p.wait_limit_ns = h->wait_limit_ns;
   const bool timing = h->cfg.flags & TKV_FLAG_TIMING;
@@ -768,8 +774,12 @@ tkv_status decode_step_device(tkv_ctx* h, const void* q, const void* k_new, cons
     p.has_prev = l0 > 0;
     p.prev_nlayers = p.nlayers;
     p.nlayers = nl;
-    p.ep_next = reinterpret_cast<int32_t*>(h->D(y.o_err)) + 4 + par;   // counters by launch parity
-    p.ep_clear = reinterpret_cast<int32_t*>(h->D(y.o_err)) + 4 + (par ^ 1);
+    // counters rotate over four launches: this one's, the previous one's
+    // (leftover items), and the one after next, which this launch zeroes
+    p.ep_own = ring + h->attn_launch_seq % 4;
+    p.ep_prev = ring + (h->attn_launch_seq + 3) % 4;
+    p.ep_clear = ring + (h->attn_launch_seq + 2) % 4;
+    p.acc = acc;
     p.prev_part_o = p.part_o;
     p.prev_part_m = p.part_m;
     p.prev_part_z = p.part_z;
@@ -830,7 +840,7 @@ tkv_status decode_step_device(tkv_ctx* h, const void* q, const void* k_new, cons
   fp.table_stride = static_cast<int32_t>(y.maxp);
   fp.s = reinterpret_cast<double*>(h->D(y.o_s));
   fp.s_stride = y.maxtok;
-  fp.acc = reinterpret_cast<float*>(h->D(y.o_acc));
+  fp.acc = acc;
   fp.acc_stride_h = p.acc_stride_h;
   fp.acc_stride_l = p.acc_stride_l;
   fp.inv_lh = 1.0 / (double(y.L) * double(y.Hq));
@@ -880,7 +890,9 @@ tkv_status do_reclassify(tkv_ctx* h) {
   cp.n_sink = h->cfg.n_sink;
   cp.recent_window = h->cfg.recent_window;
   cp.keys = reinterpret_cast<unsigned long long*>(h->D(y.o_keys));
-  cp.err = reinterpret_cast<int32_t*>(h->D(y.o_err));
+  cp.state = reinterpret_cast<ClassifyState*>(h->D(y.o_cls_state));
+  cp.slice_ties = reinterpret_cast<long long*>(h->D(y.o_cls_ties));
+  cp.max_slices = classify_slices(y.maxtok);
   // the device tier array must reflect appends since the last reassignment
   {
     char* arena = h->P(y.p_arena);
@@ -888,7 +900,9 @@ tkv_status do_reclassify(tkv_ctx* h) {
     int64_t nmax = 0;
     for (const Seq& sq : h->seqs) nmax = std::max(nmax, sq.N);
     CK(h, cudaMemcpy2DAsync(h->d_tier, y.maxtok, arena, y.maxtok, nmax, B, cudaMemcpyHostToDevice, h->cs));
-    LK(h, launch_classify(cp, h->cs), cp.B > 0);
+    int nl = 0;
+    CK(h, launch_classify(cp, h->cs, &nl));
+    h->stats.kernel_launches += nl;
     CK(h, cudaMemcpy2DAsync(arena, y.maxtok, h->d_tier_new, y.maxtok, nmax, B, cudaMemcpyDeviceToHost, h->cs));
     tkv_status st = sync_all(h);
     if (st) return st;
@@ -1147,7 +1161,7 @@ tkv_status tkv_create(const tkv_config* cfg, void* dev_ws, size_t dev_bytes, voi
       {y.o_tier, size_t(y.maxb) * y.maxtok, 0},
       {y.o_s, size_t(y.maxb) * y.maxtok * 8, 0},
       {y.o_acc, size_t(y.Lg) * y.Hkv * y.total_pages * kPage * 4, 0},
-      {y.o_err, 64, 0},
+      {y.o_err, kErrRegion, 0},
       // device mirrors of the host tiers start as the (zeroed) host pools do
       {y.o_mirror1, y.mode == TKV_HOST_TIERS_MIRROR ? size_t(y.L) * y.cap[1] * y.plb[1] : 0, 0},
       {y.o_mirror2c, y.mode == TKV_HOST_TIERS_MIRROR ? size_t(y.L) * y.cap[2] * y.plb[2] : 0, 0},
@@ -1453,7 +1467,7 @@ PagedScratch paged_scratch(int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int32_
   s.spill_stride = int64_t(max_pages) * G * kPage;
   size_t o = 0;
   auto take = [&](size_t bytes) { size_t at = o; o = align_up(o + bytes); return at; };
-  s.o_err = take(64);
+  s.o_err = take(kErrRegion);   // error word, then the launch's epilogue counters
   s.o_part_o = take(size_t(s.max_chunks) * Hkv * G * D * 4);
   s.o_part_m = take(size_t(s.max_chunks) * Hkv * G * 4);
   s.o_part_z = take(size_t(s.max_chunks) * Hkv * G * 4);
@@ -1522,9 +1536,10 @@ tkv_status tkv_paged_attention(int32_t batch, int32_t n_q_heads, int32_t n_kv_he
   p.acc_stride_b = int64_t(n_kv_heads) * max_pages * kPage;
   p.acc_stride_h = int64_t(max_pages) * kPage;
   p.err = reinterpret_cast<int32_t*>(sc + s.o_err);
+  p.ep_own = reinterpret_cast<EpCounters*>(sc + s.o_err + kEpOffset);
   p.wait_limit_ns = 2000000000ull;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  cudaError_t e = cudaMemsetAsync(sc + s.o_err, 0, 64, st);
+  cudaError_t e = cudaMemsetAsync(sc + s.o_err, 0, kErrRegion, st);
   if (e != cudaSuccess) return fail_cuda(nullptr, "cudaMemsetAsync", e);
   e = launch_attention(p, kv_dtype, p.chunk_first[batch], st);
   if (e != cudaSuccess) return fail_cuda(nullptr, "attention launch", e);
@@ -1600,9 +1615,28 @@ tkv_status tkv_paged_attention_noalloc_status(int32_t* host_out, tkv_stream stre
   return TKV_OK;
 }
 
+namespace {
+// scratch of the stateless classifier: keys [B][stride], state [B], slice tie counts [B][slices][3]
+struct ClassifyScratch {
+  size_t o_keys, o_state, o_ties, bytes;
+  int64_t slices;
+};
+ClassifyScratch classify_scratch(int32_t batch, int64_t stride) {
+  ClassifyScratch c{};
+  c.slices = classify_slices(stride);
+  size_t o = 0;
+  auto take = [&](size_t bytes) { size_t at = o; o = align_up(o + bytes); return at; };
+  c.o_keys = take(size_t(batch) * stride * 8);
+  c.o_state = take(size_t(batch) * sizeof(ClassifyState));
+  c.o_ties = take(size_t(batch) * c.slices * 3 * 8);
+  c.bytes = o;
+  return c;
+}
+}  // namespace
+
 tkv_status tkv_classify_scratch_size(int32_t batch, int64_t stride, size_t* scratch_bytes) {
   if (!scratch_bytes || batch < 1 || batch > kMaxBatch || stride < 1) return fail(nullptr, TKV_ERR_INVALID_ARG, "bad shape");
-  *scratch_bytes = align_up(size_t(batch) * stride * 8);
+  *scratch_bytes = classify_scratch(batch, stride).bytes;
   return TKV_OK;
 }
 
@@ -1611,7 +1645,9 @@ tkv_status tkv_classify(int32_t batch, const double* scores, const uint8_t* old_
                         void* scratch, size_t scratch_bytes, tkv_stream stream) {
   if (batch < 1 || batch > kMaxBatch || stride < 1 || !scores || !old_tier || !new_tier || !params || !scratch)
     return fail(nullptr, TKV_ERR_INVALID_ARG, "bad classify arguments");
-  if (scratch_bytes < size_t(batch) * stride * 8) return fail(nullptr, TKV_ERR_CAPACITY, "scratch too small");
+  const ClassifyScratch cs = classify_scratch(batch, stride);
+  if (scratch_bytes < cs.bytes) return fail(nullptr, TKV_ERR_CAPACITY, "scratch too small: need %zu bytes", cs.bytes);
+  if (reinterpret_cast<uintptr_t>(scratch) % kAlign) return fail(nullptr, TKV_ERR_INVALID_ARG, "scratch not 256-byte aligned");
   if (n_sink < 0 || recent_window < 0) return fail(nullptr, TKV_ERR_INVALID_ARG, "negative protection");
   ClassifyParams cp{};
   cp.B = batch;
@@ -1623,9 +1659,13 @@ tkv_status tkv_classify(int32_t batch, const double* scores, const uint8_t* old_
     cp.N[b] = r[0]; cp.prompt_len[b] = r[1]; cp.n0[b] = r[2]; cp.n1[b] = r[3]; cp.n2[b] = r[4];
   }
   cp.n_sink = n_sink; cp.recent_window = recent_window;
-  cp.keys = static_cast<unsigned long long*>(scratch);
-  cp.err = nullptr;
-  cudaError_t e = launch_classify(cp, static_cast<cudaStream_t>(stream));
+  char* sc = static_cast<char*>(scratch);
+  cp.keys = reinterpret_cast<unsigned long long*>(sc + cs.o_keys);
+  cp.state = reinterpret_cast<ClassifyState*>(sc + cs.o_state);
+  cp.slice_ties = reinterpret_cast<long long*>(sc + cs.o_ties);
+  cp.max_slices = cs.slices;
+  int nl = 0;
+  cudaError_t e = launch_classify(cp, static_cast<cudaStream_t>(stream), &nl);
   if (e != cudaSuccess) return fail_cuda(nullptr, "classify launch", e);
   return TKV_OK;
 }

@@ -57,6 +57,14 @@ __host__ __device__ inline int64_t swz_offset(int row, int64_t byte_in_row, int 
   return (((byte_in_row >> 4) ^ (row & swz)) << 4) | (byte_in_row & 15);
 }
 
+// Epilogue work counters of one attention launch: claim[z] hands out the
+// (KV head, chunk) epilogue items of its layer z (fetch-and-add; values past
+// the item count mean none is left). Four sets rotate over consecutive launches.
+constexpr int kMaxLaunchLayers = 32;
+struct EpCounters {
+  int32_t claim[kMaxLaunchLayers];
+};
+
 // One page source of the attention kernel: a page pool (or one layer of it).
 struct PageSource {
   const char* base;          // page 0 of this source at the launch's first layer
@@ -112,8 +120,9 @@ struct AttnParams {
   // (has_prev != 0); it covered prev_nlayers layers.
   int32_t has_prev;
   int32_t prev_nlayers;
-  int32_t* ep_next;       // work counter of the previous launch's epilogue items (zero at launch)
-  int32_t* ep_clear;      // the other parity's counter, zeroed by this launch for the next one
+  EpCounters* ep_own;     // this launch's counters (zero at launch; claimed by the next launch or the combine)
+  EpCounters* ep_prev;    // the previous launch's counters (its epilogue items)
+  EpCounters* ep_clear;   // counters of the launch after next, zeroed by this launch (or null)
   uint32_t* started;      // if set, the first CTA writes launch_seq here at entry
   uint32_t launch_seq;
   // if set: span[0] = min CTA start, span[1] = max CTA end (%globaltimer ns) of
@@ -136,6 +145,15 @@ int attention_supported(int kv_dtype, int G, int D);
 int resident_attention_ctas(int kv_dtype, int G, int D);
 
 // classify.cu
+// Per-sequence state of the radix select (device scratch, zeroed per call).
+struct ClassifyState {
+  unsigned long long ncand, nprot;      // candidates and protected positions
+  unsigned long long prefix[3];         // boundary keys, narrowed 8 bits per pass
+  long long rem[3];                     // rank of each boundary among keys with its prefix
+  int done[3];                          // boundary past the last candidate
+  unsigned int hist[3][256];            // digit histograms of the current pass
+};
+
 struct ClassifyParams {
   int32_t B;
   const double* s;
@@ -145,9 +163,14 @@ struct ClassifyParams {
   int64_t N[kMaxBatch], prompt_len[kMaxBatch], n0[kMaxBatch], n1[kMaxBatch], n2[kMaxBatch];
   int32_t n_sink, recent_window;
   unsigned long long* keys;  // scratch [B][stride]
-  int32_t* err;
+  ClassifyState* state;      // scratch [B]
+  long long* slice_ties;     // scratch [B][max_slices][3]
+  int64_t max_slices;        // slices of 4096 positions per sequence the scratch holds
 };
-cudaError_t launch_classify(const ClassifyParams& p, cudaStream_t s);
+// slices of 4096 positions needed for sequences of up to `stride` positions
+int64_t classify_slices(int64_t stride);
+// launches the select's kernels (their count in *launches)
+cudaError_t launch_classify(const ClassifyParams& p, cudaStream_t s, int* launches);
 
 // movement.cu
 struct AppendParams {
