@@ -165,6 +165,8 @@ struct Shape {
   static constexpr int NV = GP * 4;           // fp32-QK partials per lane
   static constexpr int NL = NV >= 8 ? NV / 8 : 1;
   static_assert(CPL >= 1 && NCH % 8 == 0, "row must hold a multiple of 8 chunks");
+  // a consumer warp's (O, m, Z) of a unit fits the stage of its unit-end marker
+  static_assert((G * D + 2 * GP) * 4 <= STAGE, "merge data must fit a ring stage");
   static_assert(D % 32 == 0, "head_dim must be a multiple of 32");
 };
 
@@ -179,7 +181,7 @@ struct Smem {
   static constexpr int PS = FMA ? kAttnWarps * PSW * 4 : 0;
   static constexpr int PG = kMeta * 8;     // per ring position: page index, flags word
   static constexpr int DESC = kMeta * 16;  // producer's copy descriptors per ring position
-  static constexpr int BARS = 2 * kAttnStages * 8;  // full[stages], empty[stages]
+  static constexpr int BARS = (2 * kAttnStages + 1) * 8;  // full[stages], empty[stages], merge
   static constexpr int MERGE = kAttnWarps * (G * D + 2 * S::GP) * 4;
   static constexpr int BODY = ((RING > MERGE ? RING : MERGE) + 127) / 128 * 128;
   static constexpr int off_q = BODY;
@@ -238,9 +240,15 @@ __device__ __forceinline__ Work find_work_at(const AttnParams& p, int chunk, int
   return wk;
 }
 
-__device__ __forceinline__ Work find_work(const AttnParams& p) {
-  return find_work_at(p, blockIdx.x, blockIdx.y, blockIdx.z);
+// Work unit u of a launch. Units run layer by layer and within a layer over
+// (KV head, chunk); a persistent CTA takes units blockIdx.x, blockIdx.x +
+// gridDim.x, ..., which with whole waves of units per layer is the same
+// (KV head, chunk) in every layer of the launch.
+__device__ __forceinline__ Work unit_work(const AttnParams& p, int u) {
+  const int cu = u % p.total_chunks, rest = u / p.total_chunks;
+  return find_work_at(p, cu, rest % p.Hkv, rest / p.Hkv);
 }
+__device__ __forceinline__ int launch_units(const AttnParams& p) { return p.total_chunks * p.Hkv * p.nlayers; }
 
 // This work unit's spilled logits (k-th page of the sequence at slot (k * G + g) * 16 + row).
 __device__ __forceinline__ float* spill_of(const AttnParams& p, float* spill, const Work& wk) {
@@ -255,6 +263,7 @@ __device__ __forceinline__ void init_barriers(char* smem) {
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::off_bar);
   if (threadIdx.x == 0) {
     for (int s = 0; s < 2 * kAttnStages; ++s) mbar_init(smem_u32(bars + s), 1);
+    mbar_init(smem_u32(bars + 2 * kAttnStages), kAttnWarps);  // one arrival per consumer warp
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
@@ -357,15 +366,21 @@ __device__ __forceinline__ void load_host_page(const PageCopy& c, char* stage, i
   __syncwarp();
 }
 
-// The producer warp's job: resolve the chunk's pages (one lane per page, 32
-// per round; the first round's copies go out at once, later rounds are
-// resolved while the ring is full) and let lane 0 keep the ring full; then one
-// end marker per consumer warp (a position whose page index is -1, completed
-// by a plain arrive). Returns the pages issued (lane 0).
+// The producer warp's job, for each work unit of this persistent CTA in turn:
+// resolve the unit's pages (one lane per page, 32 per round; the first round's
+// copies go out at once, later rounds are resolved while the ring is full) and
+// keep the ring full; then pad positions (page index -2) up to a multiple of
+// the consumer warp count, and one unit-end marker per consumer warp (page
+// index -1, flags word = the first marker's position), each completed by a
+// plain arrive. Every unit thus starts at a multiple of the warp count, so its
+// page j always goes to consumer warp j % warps and the result does not depend
+// on which CTA runs the unit. The ring runs on across units, so the next unit's
+// pages stream in while the consumers merge the last one. Returns the ring
+// positions handled (lane 0).
 template <typename S>
-__device__ int produce(const AttnParams& p, const Work& wk, int32_t* meta_k, uint32_t* meta_f, PageCopy* desc,
-                       char* ring, uint32_t full0, uint32_t empty0, volatile int* abort_flag) {
-  static_assert(kMeta >= 32 + kAttnStages, "metadata ring too small");
+__device__ int produce(const AttnParams& p, int32_t* meta_k, uint32_t* meta_f, PageCopy* desc, char* ring,
+                       uint32_t full0, uint32_t empty0, volatile int* abort_flag) {
+  static_assert(kMeta >= 32 + kAttnStages + 2 * kAttnWarps, "metadata ring too small");
   const int lane = threadIdx.x & 31;
   uint64_t policy;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(policy));
@@ -376,11 +391,7 @@ __device__ int produce(const AttnParams& p, const Work& wk, int32_t* meta_k, uin
   };
   // test hook: the first CTA withholds its first page, so that a consumer's
   // bounded wait runs out (nothing is in flight for that stage)
-  const bool stall = p.stall_first_page && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0;
-  auto resolve = [&](int first_page, int n) {
-    if (lane < n) resolve_page(p, wk, first_page + lane, (pos + lane) % kMeta, meta_k, meta_f, desc);
-    __syncwarp();
-  };
+  const bool stall = p.stall_first_page && blockIdx.x == 0;
   // Lane 0 waits for each stage and issues its bulk copy; a page in pinned host
   // memory is instead read by the whole warp with plain loads (load_host_page)
   // and its stage completed with a plain arrive.
@@ -412,24 +423,94 @@ __device__ int produce(const AttnParams& p, const Work& wk, int32_t* meta_k, uin
     pos += n;
     __syncwarp();
   };
-  for (int r = 0; r < wk.npg; r += 32) {
-    const int n = min(32, wk.npg - r);
-    resolve(wk.k0 + r, n);
-    issue(n);
-  }
-  if (lane == 0 && ok) {
-    for (int j = 0; j < kAttnWarps; ++j) {
-      const int i = pos + j;
-      if (!stage_free(i)) {
-        *abort_flag = 1;
-        break;
-      }
-      meta_k[i % kMeta] = -1;
-      mbar_arrive(full0 + (i % kAttnStages) * 8);
+  const int units = launch_units(p);
+  for (int u = blockIdx.x; u < units; u += gridDim.x) {
+    const Work wk = unit_work(p, u);
+    for (int r = 0; r < wk.npg; r += 32) {
+      const int n = min(32, wk.npg - r);
+      if (lane < n) resolve_page(p, wk, wk.k0 + r + lane, (pos + lane) % kMeta, meta_k, meta_f, desc);
+      __syncwarp();
+      issue(n);
     }
+    const int pad = (kAttnWarps - pos % kAttnWarps) % kAttnWarps;
+    if (lane == 0 && ok) {
+      for (int j = 0; j < pad + kAttnWarps; ++j) {
+        const int i = pos + j;
+        if (!stage_free(i)) {
+          ok = false;
+          *abort_flag = 1;
+          break;
+        }
+        meta_k[i % kMeta] = j < pad ? -2 : -1;
+        meta_f[i % kMeta] = static_cast<uint32_t>(pos + pad);
+        mbar_arrive(full0 + (i % kAttnStages) * 8);
+        ++issued;
+      }
+    }
+    pos += pad + kAttnWarps;
+    __syncwarp();
+    if (!__shfl_sync(kFull, ok ? 1 : 0, 0)) break;
   }
-  __syncwarp();
   return issued;
+}
+
+// Stage of the unit-end marker that consumer warp ww takes when the unit's
+// markers start at ring position `first`, a multiple of the warp count
+// (position i goes to warp i % warps).
+__device__ __forceinline__ int marker_stage(int first, int ww) { return (first + ww) % kAttnStages; }
+
+// Merges the consumer warps' (O, m, Z) of a unit — each warp's in the stage of
+// its unit-end marker, laid out [G][D] floats, then m[GP], Z[GP] — into the
+// unit's partial: O relative to the unit's max M, and (M, Z) per head. Run by
+// the consumer threads (ctid < warps * 32).
+template <typename T, int G, int D>
+__device__ void merge_partial(const AttnParams& p, const Work& wk, const char* ring, int first, int ctid) {
+  using S = Shape<T, G, D>;
+  const float* mo[kAttnWarps];
+#pragma unroll
+  for (int ww = 0; ww < kAttnWarps; ++ww)
+    mo[ww] = reinterpret_cast<const float*>(ring + marker_stage(first, ww) * S::STAGE);
+  const int64_t pidx = unit_index(p, wk.z, wk.cf + wk.jc, wk.kvh);
+  for (int idx = ctid; idx < G * D; idx += kAttnWarps * 32) {
+    const int g = idx / D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int ww = 0; ww < kAttnWarps; ++ww) M = fmaxf(M, mo[ww][G * D + g]);
+    float o = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int ww = 0; ww < kAttnWarps; ++ww) {
+        const float mw = mo[ww][G * D + g];
+        if (mw != -INFINITY) o += mo[ww][idx] * exp2f(mw - M);
+      }
+    }
+    p.part_o[pidx * G * D + idx] = o;
+  }
+  if (ctid < G) {
+    float M = -INFINITY;
+#pragma unroll
+    for (int ww = 0; ww < kAttnWarps; ++ww) M = fmaxf(M, mo[ww][G * D + ctid]);
+    float Z = 0.f;
+    if (M != -INFINITY)
+#pragma unroll
+      for (int ww = 0; ww < kAttnWarps; ++ww) {
+        const float mw = mo[ww][G * D + ctid];
+        if (mw != -INFINITY) Z += mo[ww][G * D + S::GP + ctid] * exp2f(mw - M);
+      }
+    p.part_m[pidx * G + ctid] = M;
+    p.part_z[pidx * G + ctid] = Z;
+  }
+}
+
+// Barrier of the consumer warps at a unit end (an mbarrier with one arrival
+// per warp, so that a warp whose own wait gave up cannot hold the others for
+// ever: they give up too). Returns false when the wait gave up.
+__device__ __forceinline__ bool consumers_meet(uint32_t bar, uint32_t& phase, int lane, uint64_t limit_ns) {
+  __syncwarp();
+  if (lane == 0) mbar_arrive(bar);
+  const bool ok = __all_sync(kFull, mbar_wait(bar, phase & 1u, limit_ns));
+  ++phase;
+  return ok;
 }
 
 // After an abort: wait (bounded) for the copies still in flight to land.
@@ -447,45 +528,6 @@ __device__ __forceinline__ float t2_scale(const char* stage_scales, bool per_hea
 
 __device__ __forceinline__ void store_out(float* p, float v) { *p = v; }
 __device__ __forceinline__ void store_out(__nv_bfloat16* p, float v) { *p = __float2bfloat16_rn(v); }
-
-// Merges the warps' (m, Z, O) — already in the MERGE area of `smem` — into the
-// CTA's partial: O relative to its own max M, and (M, Z) per head.
-template <typename T, int G, int D>
-__device__ void write_partial(const AttnParams& p, const Work& wk, char* smem) {
-  using S = Shape<T, G, D>;
-  const int tid = threadIdx.x;
-  float* mo = reinterpret_cast<float*>(smem);           // [warps][G][D]
-  float* mm = mo + kAttnWarps * G * D;                  // [warps][GP]
-  float* mz = mm + kAttnWarps * S::GP;                  // [warps][GP]
-  const int64_t pidx = unit_index(p, wk.z, wk.cf + wk.jc, wk.kvh);
-  for (int idx = tid; idx < G * D; idx += blockDim.x) {
-    const int g = idx / D;
-    float M = -INFINITY;
-#pragma unroll
-    for (int ww = 0; ww < kAttnWarps; ++ww) M = fmaxf(M, mm[ww * S::GP + g]);
-    float o = 0.f;
-    if (M != -INFINITY) {
-#pragma unroll
-      for (int ww = 0; ww < kAttnWarps; ++ww) {
-        const float mw = mm[ww * S::GP + g];
-        if (mw != -INFINITY) o += mo[(ww * G) * D + idx] * exp2f(mw - M);
-      }
-    }
-    p.part_o[pidx * G * D + idx] = o;
-  }
-  if (tid < G) {
-    float M = -INFINITY;
-    for (int ww = 0; ww < kAttnWarps; ++ww) M = fmaxf(M, mm[ww * S::GP + tid]);
-    float Z = 0.f;
-    if (M != -INFINITY)
-      for (int ww = 0; ww < kAttnWarps; ++ww) {
-        const float mw = mm[ww * S::GP + tid];
-        if (mw != -INFINITY) Z += mz[ww * S::GP + tid] * exp2f(mw - M);
-      }
-    p.part_m[pidx * G + tid] = M;
-    p.part_z[pidx * G + tid] = Z;
-  }
-}
 
 // The epilogue of one (chunk, KV head) of a finished layer, run by NT threads
 // (tid < NT, NT a multiple of 32): global (M, Z) of each head from the
@@ -607,12 +649,8 @@ __device__ void layer_epilogue(const AttnParams& p, const LayerBufs& lb, const W
   }
 }
 
-// Work unit of epilogue item `item` of a launch: items run layer by layer, and
-// within a layer over (KV head, chunk).
-__device__ __forceinline__ Work epilogue_work(const AttnParams& p, int item) {
-  const int cu = item % p.total_chunks, rest = item / p.total_chunks;
-  return find_work_at(p, cu, rest % p.Hkv, rest / p.Hkv);
-}
+// Epilogue item `item` of a launch is its work unit `item`.
+__device__ __forceinline__ Work epilogue_work(const AttnParams& p, int item) { return unit_work(p, item); }
 
 // Claims an epilogue item of a finished launch: the next unclaimed (KV head,
 // chunk) of its first layer that has one left, as layer * per_layer + index,
@@ -741,16 +779,15 @@ __global__ void __launch_bounds__((kAttnWarps + 1) * 32, 3)
   static_assert(G >= 2 && G <= 8, "tensor-core path serves 2..8 query heads per KV head");
   extern __shared__ __align__(128) char smem[];
   __shared__ volatile int s_abort;
-  __shared__ float s_epM[8], s_epIZ[8];  // previous layer's (M, 1 / Z) per head
+  __shared__ float s_epM[8], s_epIZ[8];  // previous launch's (M, 1 / Z) per head
   __shared__ volatile int s_item;
 
   const int tid = threadIdx.x;
   const int w = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, t = lane & 3;  // fragment row group and column pair
-  const Work wk = find_work(p);
   if (tid == 0) s_abort = 0;
   if (tid == 0 && p.span) atomicMin(p.span, global_ns());
-  if (tid == 0 && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0) {
+  if (tid == 0 && blockIdx.x == 0) {
     if (p.span_next) {
       p.span_next[0] = ~0ull;
       p.span_next[1] = 0ull;
@@ -769,15 +806,21 @@ __global__ void __launch_bounds__((kAttnWarps + 1) * 32, 3)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::off_bar);
   char* ring = smem;
   const uint32_t full0 = smem_u32(bars), empty0 = full0 + kAttnStages * 8;
+  const uint32_t merge_bar = full0 + 2 * kAttnStages * 8;
   const bool consumer = w < kAttnWarps;
   int issued = 0;
   if (!consumer)
-    issued = produce<S>(p, wk, meta_k, meta_f, reinterpret_cast<PageCopy*>(smem + L::off_desc), ring, full0, empty0,
+    issued = produce<S>(p, meta_k, meta_f, reinterpret_cast<PageCopy*>(smem + L::off_desc), ring, full0, empty0,
                         &s_abort);
 
-  // Q fragments (A operand, heads as rows; rows 8..15 of the tile are zero)
-  uint32_t qa[KS][2];
-  if (consumer) {
+  const int units = launch_units(p);
+  int u = blockIdx.x;
+  Work wk{};
+  uint32_t qa[KS][2];                    // Q fragments (A operand, heads as rows; rows 8..15 zero)
+  float* spill_b = nullptr;
+  // the unit's query fragments and logit spill
+  auto start_unit = [&]() {
+    wk = unit_work(p, u);
     const T* q = reinterpret_cast<const T*>(p.q) + wk.z * p.q_stride_l + static_cast<int64_t>(wk.b) * p.q_stride_b +
                  static_cast<int64_t>(wk.kvh) * G * D;
 #pragma unroll
@@ -789,27 +832,75 @@ __global__ void __launch_bounds__((kAttnWarps + 1) * 32, 3)
         qa[ks][0] = qa[ks][1] = 0u;
       }
     }
-  }
+    spill_b = spill_of(p, p.spill, wk);
+  };
+  if (consumer && u < units) start_unit();
 
   float m_run = -INFINITY, z_run = 0.f;  // softmax state of head g
   float o[KS][4];                        // O^T tiles: d rows, head columns
 #pragma unroll
   for (int mt = 0; mt < KS; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
-  float* spill_b = spill_of(p, p.spill, wk);
+  uint32_t mphase = 0;                   // merge-barrier phases completed
   // per-lane ldmatrix row / chunk selectors (matrix = lane / 8)
   const int lrow = ((lane >> 4) << 3) | (lane & 7);
   const int lchunk = (lane >> 3) & 1;
 
-  for (int i = w; consumer; i += kAttnWarps) {
+  for (int i = w; consumer && u < units; i += kAttnWarps) {
     const int st = i % kAttnStages;
     const bool ok = __all_sync(kFull, mbar_wait(full0 + st * 8, (i / kAttnStages) & 1, p.wait_limit_ns));
     if (!ok) {
       if (lane == 0) s_abort = 1;
       break;
     }
-    const int k = meta_k[i % kMeta];  // page index in the sequence's list; -1 ends this warp's pages
-    if (k < 0) break;
     char* stage = ring + st * S::STAGE;
+    const int k = meta_k[i % kMeta];  // page index in the sequence's list; -1 ends the unit, -2 pads
+    if (k == -2) {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty0 + st * 8);
+      continue;
+    }
+    if (k < 0) {
+      // ---- unit end: this warp's (O, m, Z) into its marker's stage, then merge
+      const int first = static_cast<int>(meta_f[i % kMeta]);
+      float* mo = reinterpret_cast<float*>(stage);
+#pragma unroll
+      for (int mt = 0; mt < KS; ++mt) {
+        const int d0 = 16 * mt + g;
+        if (2 * t < G) {
+          mo[(2 * t) * D + d0] = o[mt][0];
+          mo[(2 * t) * D + d0 + 8] = o[mt][2];
+        }
+        if (2 * t + 1 < G) {
+          mo[(2 * t + 1) * D + d0] = o[mt][1];
+          mo[(2 * t + 1) * D + d0 + 8] = o[mt][3];
+        }
+      }
+      if (t == 0 && g < G) {
+        mo[G * D + g] = m_run;
+        mo[G * D + S::GP + g] = z_run;
+      }
+      if (!consumers_meet(merge_bar, mphase, lane, p.wait_limit_ns)) {
+        if (lane == 0) s_abort = 1;
+        break;
+      }
+      merge_partial<T, G, D>(p, wk, ring, first, tid);
+      if (!consumers_meet(merge_bar, mphase, lane, p.wait_limit_ns)) {  // every warp has read every stage
+        if (lane == 0) s_abort = 1;
+        break;
+      }
+      if (lane == 0) {
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // generic writes before the next copy
+        mbar_arrive(empty0 + st * 8);
+      }
+      u += gridDim.x;
+      if (u >= units) break;
+      start_unit();
+      m_run = -INFINITY;
+      z_run = 0.f;
+#pragma unroll
+      for (int mt = 0; mt < KS; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+      continue;
+    }
     const uint32_t flags = meta_f[i % kMeta];
     const uint32_t mask = flags & 0xffffu;
     const bool i8 = (flags & kFlagI8) != 0;
@@ -917,40 +1008,13 @@ __global__ void __launch_bounds__((kAttnWarps + 1) * 32, 3)
   }
 
   __syncthreads();
-  if (s_abort) {  // a bounded wait gave up: land the copies in flight, publish an empty partial
+  if (s_abort) {  // a bounded wait gave up: land the copies in flight; the unit's partial stays unwritten
     if (!consumer && lane == 0) {
       drain(issued, full0, p.wait_limit_ns);
       atomicExch(p.err, DEV_TIMEOUT);
     }
-    m_run = -INFINITY;
-    z_run = 0.f;
-#pragma unroll
-    for (int mt = 0; mt < KS; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
   }
   __syncthreads();
-
-  // ---- hand the consumer warps' (m, Z, O) to the CTA merge ----------------------
-  float* mo = reinterpret_cast<float*>(smem);
-  float* mm = mo + kAttnWarps * G * D;
-  float* mz = mm + kAttnWarps * S::GP;
-#pragma unroll
-  for (int mt = 0; consumer && mt < KS; ++mt) {
-    const int d0 = 16 * mt + g;
-    if (2 * t < G) {
-      mo[(w * G + 2 * t) * D + d0] = o[mt][0];
-      mo[(w * G + 2 * t) * D + d0 + 8] = o[mt][2];
-    }
-    if (2 * t + 1 < G) {
-      mo[(w * G + 2 * t + 1) * D + d0] = o[mt][1];
-      mo[(w * G + 2 * t + 1) * D + d0 + 8] = o[mt][3];
-    }
-  }
-  if (consumer && t == 0 && g < G) {
-    mm[w * S::GP + g] = m_run;
-    mz[w * S::GP + g] = z_run;
-  }
-  __syncthreads();
-  write_partial<T, G, D>(p, wk, smem);
   prev_launch_epilogue<T, G, D>(p, tid, s_epM, s_epIZ, &s_item);
   if (tid == 0 && p.span) atomicMax(p.span + 1, global_ns());
 }
@@ -1047,10 +1111,9 @@ __global__ void __launch_bounds__((kAttnWarps + 1) * 32)
   const int tid = threadIdx.x;
   const int w = tid >> 5, lane = tid & 31;
   const int r = lane >> 3, c = lane & 7;
-  const Work wk = find_work(p);
   if (tid == 0) s_abort = 0;
   if (tid == 0 && p.span) atomicMin(p.span, global_ns());
-  if (tid == 0 && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0) {
+  if (tid == 0 && blockIdx.x == 0) {
     if (p.span_next) {
       p.span_next[0] = ~0ull;
       p.span_next[1] = 0ull;
@@ -1069,19 +1132,26 @@ __global__ void __launch_bounds__((kAttnWarps + 1) * 32)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::off_bar);
   char* ring = smem;
   const uint32_t full0 = smem_u32(bars), empty0 = full0 + kAttnStages * 8;
+  const uint32_t merge_bar = full0 + 2 * kAttnStages * 8;
   const bool consumer = w < kAttnWarps;
   int issued = 0;
   if (!consumer)
-    issued = produce<S>(p, wk, meta_k, meta_f, reinterpret_cast<PageCopy*>(smem + L::off_desc), ring, full0, empty0,
+    issued = produce<S>(p, meta_k, meta_f, reinterpret_cast<PageCopy*>(smem + L::off_desc), ring, full0, empty0,
                         &s_abort);
 
   float* q_s = reinterpret_cast<float*>(smem + L::off_q);
   float* p_s = reinterpret_cast<float*>(smem + L::off_p) + w * L::PSW;
   float* corr_s = p_s + S::GP * kPage;
-  {
+  const int units = launch_units(p);
+  int u = blockIdx.x;
+  Work wk{};
+  float* spill_b = nullptr;
+  // the unit's scaled query (shared by the consumer warps) and logit spill
+  auto start_unit = [&]() {
+    wk = unit_work(p, u);
     const T* q = reinterpret_cast<const T*>(p.q) + wk.z * p.q_stride_l + static_cast<int64_t>(wk.b) * p.q_stride_b +
                  static_cast<int64_t>(wk.kvh) * G * D;
-    for (int i = tid; consumer && i < S::GP * D; i += kAttnWarps * 32) {
+    for (int i = tid; i < S::GP * D; i += kAttnWarps * 32) {
       const int gg = i / D;
       float v = 0.f;
       if (gg < G) {
@@ -1092,8 +1162,11 @@ __global__ void __launch_bounds__((kAttnWarps + 1) * 32)
       }
       q_s[i] = v * p.qscale;
     }
-  }
+    spill_b = spill_of(p, p.spill, wk);
+  };
+  if (consumer && u < units) start_unit();
   if (consumer) consumer_sync();
+  uint32_t mphase = 0;                   // merge-barrier phases completed
 
   float m_run = -INFINITY, z_run = 0.f;  // for the head this lane owns
   float2 acc[G][S::VPL];
@@ -1107,17 +1180,59 @@ __global__ void __launch_bounds__((kAttnWarps + 1) * 32)
   const bool own_writer = S::NV >= 8 ? true : ((c & 1) == 0);
   const bool head_lead = r == 0 && (S::NV < 8 ? c == 0 : (c & ((8 / S::GP) - 1)) == 0);
 
-  float* spill_b = spill_of(p, p.spill, wk);
-
-  for (int i = w; consumer; i += kAttnWarps) {
+  for (int i = w; consumer && u < units; i += kAttnWarps) {
     const int st = i % kAttnStages;
     const bool ok = __all_sync(kFull, mbar_wait(full0 + st * 8, (i / kAttnStages) & 1, p.wait_limit_ns));
     if (!ok) {
       if (lane == 0) s_abort = 1;
       break;
     }
-    const int k = meta_k[i % kMeta];  // page index in the sequence's list; -1 ends this warp's pages
-    if (k < 0) break;
+    const int k = meta_k[i % kMeta];  // page index in the sequence's list; -1 ends the unit, -2 pads
+    if (k == -2) {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty0 + st * 8);
+      continue;
+    }
+    if (k < 0) {
+      // ---- unit end: this warp's (O, m, Z) into its marker's stage, then merge
+      const int first = static_cast<int>(meta_f[i % kMeta]);
+      float* mo = reinterpret_cast<float*>(ring + st * S::STAGE);
+#pragma unroll
+      for (int g = 0; g < G; ++g)
+#pragma unroll
+        for (int e = 0; e < S::VPL; ++e) mo[g * D + lane * S::VPL + e] = acc[g][e].x + acc[g][e].y;
+      if (own_writer && own_g < G && head_lead) {
+        mo[G * D + own_g] = m_run;
+        mo[G * D + S::GP + own_g] = z_run;
+      }
+      if (!consumers_meet(merge_bar, mphase, lane, p.wait_limit_ns)) {
+        if (lane == 0) s_abort = 1;
+        break;
+      }
+      merge_partial<T, G, D>(p, wk, ring, first, tid);
+      if (!consumers_meet(merge_bar, mphase, lane, p.wait_limit_ns)) {  // every warp has read every stage
+        if (lane == 0) s_abort = 1;
+        break;
+      }
+      if (lane == 0) {
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // generic writes before the next copy
+        mbar_arrive(empty0 + st * 8);
+      }
+      u += gridDim.x;
+      if (u >= units) break;
+      start_unit();
+      if (!consumers_meet(merge_bar, mphase, lane, p.wait_limit_ns)) {  // the new query is in place
+        if (lane == 0) s_abort = 1;
+        break;
+      }
+      m_run = -INFINITY;
+      z_run = 0.f;
+#pragma unroll
+      for (int g = 0; g < G; ++g)
+#pragma unroll
+        for (int e = 0; e < S::VPL; ++e) acc[g][e] = make_float2(0.f, 0.f);
+      continue;
+    }
     const uint32_t flags = meta_f[i % kMeta];
     const uint32_t mask = flags & 0xffffu;
     const bool i8 = (flags & kFlagI8) != 0;
@@ -1296,46 +1411,39 @@ __global__ void __launch_bounds__((kAttnWarps + 1) * 32)
   }
 
   __syncthreads();
-  if (s_abort) {  // a bounded wait gave up: land the copies in flight, publish an empty partial
+  if (s_abort) {  // a bounded wait gave up: land the copies in flight; the unit's partial stays unwritten
     if (!consumer && lane == 0) {
       drain(issued, full0, p.wait_limit_ns);
       atomicExch(p.err, DEV_TIMEOUT);
     }
-    m_run = -INFINITY;
-    z_run = 0.f;
-#pragma unroll
-    for (int g = 0; g < G; ++g)
-#pragma unroll
-      for (int e = 0; e < S::VPL; ++e) acc[g][e] = make_float2(0.f, 0.f);
   }
   __syncthreads();
-  float* mo = reinterpret_cast<float*>(smem);
-  float* mm = mo + kAttnWarps * G * D;
-  float* mz = mm + kAttnWarps * S::GP;
-#pragma unroll
-  for (int g = 0; consumer && g < G; ++g)
-#pragma unroll
-    for (int e = 0; e < S::VPL; ++e)
-      mo[(w * G + g) * D + lane * S::VPL + e] = acc[g][e].x + acc[g][e].y;
-  if (consumer && own_writer && own_g < G && head_lead) {
-    mm[w * S::GP + own_g] = m_run;
-    mz[w * S::GP + own_g] = z_run;
-  }
-  __syncthreads();
-  write_partial<T, G, D>(p, wk, smem);
   prev_launch_epilogue<T, G, D>(p, tid, s_epM, s_epIZ, &s_item);
   if (tid == 0 && p.span) atomicMax(p.span + 1, global_ns());
 }
 
+// Persistent launch: as many CTAs as fit on the device at once (found once per
+// kernel and device), at most one per work unit; each CTA runs units
+// blockIdx.x, blockIdx.x + gridDim.x, ...
 template <typename K>
 cudaError_t launch_kernel(K kern, int smem_bytes, const AttnParams& p, int total_chunks, cudaStream_t s,
-                          bool& configured) {
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+                          int (&resident)[64]) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (resident[dev] == 0) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
     if (e != cudaSuccess) return e;
-    configured = true;
+    int sms = 0, per_sm = 0;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, (kAttnWarps + 1) * 32, smem_bytes);
+    if (e != cudaSuccess) return e;
+    resident[dev] = sms * (per_sm > 0 ? per_sm : 1);
   }
-  dim3 grid(total_chunks, p.Hkv, p.nlayers);
+  const int64_t units = static_cast<int64_t>(total_chunks) * p.Hkv * p.nlayers;
+  const unsigned grid = static_cast<unsigned>(units < resident[dev] ? units : resident[dev]);
   kern<<<grid, (kAttnWarps + 1) * 32, smem_bytes, s>>>(p);
   return cudaGetLastError();
 }
@@ -1359,11 +1467,11 @@ cudaError_t launch_typed(const AttnParams& p, int total_chunks, cudaStream_t s, 
     return cudaLaunchKernelEx(&cfg, attn_combine_kernel<T, G, D>, p);
   }
   if constexpr (sizeof(T) == 2 && G >= 2) {
-    static bool configured = false;
-    return launch_kernel(attn_split_mma_kernel<G, D>, L::TOTAL, p, total_chunks, s, configured);
+    static int resident[64] = {};
+    return launch_kernel(attn_split_mma_kernel<G, D>, L::TOTAL, p, total_chunks, s, resident);
   } else {
-    static bool configured = false;
-    return launch_kernel(attn_split_fma_kernel<T, G, D>, L::TOTAL, p, total_chunks, s, configured);
+    static int resident[64] = {};
+    return launch_kernel(attn_split_fma_kernel<T, G, D>, L::TOTAL, p, total_chunks, s, resident);
   }
 }
 
