@@ -529,14 +529,15 @@ __device__ __forceinline__ float t2_scale(const char* stage_scales, bool per_hea
 __device__ __forceinline__ void store_out(float* p, float v) { *p = v; }
 __device__ __forceinline__ void store_out(__nv_bfloat16* p, float v) { *p = __float2bfloat16_rn(v); }
 
-// The epilogue of one (chunk, KV head) of a finished layer, run by NT threads
-// (tid < NT, NT a multiple of 32): global (M, Z) of each head from the
-// sequence's chunk partials (one warp per head), this chunk's slice of the
-// merged output, and the exact softmax weights alpha = exp2(l - M) / Z of this
-// chunk's slots, summed over the G heads and added to the score accumulator at
-// slot 16 * k + row of the sequence's page list (the fused score epilogue of
+// The epilogue of one (layer, sequence, KV head) group of a finished layer, run
+// by NT threads (tid < NT, NT a multiple of 32): global (M, Z) of each head from
+// the group's chunk partials (one warp per head), the merged output, and the
+// exact softmax weights alpha = exp2(l - M) / Z of every slot of the sequence's
+// pages, summed over the G heads and added to the score accumulator at slot
+// 16 * k + row of the sequence's page list (the fused score epilogue of
 // Methodology 2). Masked slots hold -inf logits, so they add exactly 0 and no
-// page metadata is read. `sync` synchronises the NT threads.
+// page metadata is read. `sync` synchronises the NT threads. `wk` describes the
+// group: its first chunk, with k0 = 0 and npg = all the sequence's pages.
 struct LayerBufs {
   const float* part_o;
   const float* part_m;
@@ -544,6 +545,7 @@ struct LayerBufs {
   const float* spill;
   void* out;
   float* acc;   // score accumulator slice of the launch's first layer
+  bool first;   // the launch is a step's first: its items write the slices instead of adding to them
 };
 
 // Every epilogue item is read after the grid that wrote it has finished, so the
@@ -591,9 +593,8 @@ __device__ void layer_epilogue(const AttnParams& p, const LayerBufs& lb, const W
   }
   sync();
   {
-    // this chunk's slice of the G * D outputs
-    const int lo = static_cast<int>((static_cast<int64_t>(wk.jc) * G * D) / nch);
-    const int hi = static_cast<int>((static_cast<int64_t>(wk.jc + 1) * G * D) / nch);
+    // the G * D outputs
+    const int lo = 0, hi = G * D;
     T* out = reinterpret_cast<T*>(lb.out) + wk.z * p.out_stride_l + static_cast<int64_t>(wk.b) * p.out_stride_b +
              static_cast<int64_t>(wk.kvh) * G * D;
     for (int idx = lo + tid; idx < hi; idx += NT) {
@@ -632,7 +633,7 @@ __device__ void layer_epilogue(const AttnParams& p, const LayerBufs& lb, const W
         const int k = wk.k0 + (item >> 4), row = item & 15;
 #pragma unroll
         for (int g = 0; g < G; ++g) l[u][g] = ld_part(spill_b + (static_cast<int64_t>(k) * G + g) * kPage + row);
-        old[u] = __ldcg(accb + static_cast<int64_t>(k) * kPage + row);  // neighbouring chunks share lines
+        old[u] = lb.first ? 0.f : __ldcg(accb + static_cast<int64_t>(k) * kPage + row);  // neighbouring chunks share lines
       }
     }
 #pragma unroll
@@ -649,8 +650,20 @@ __device__ void layer_epilogue(const AttnParams& p, const LayerBufs& lb, const W
   }
 }
 
-// Epilogue item `item` of a launch is its work unit `item`.
-__device__ __forceinline__ Work epilogue_work(const AttnParams& p, int item) { return unit_work(p, item); }
+// Epilogue item `item` of a launch: group (layer z, sequence b, KV head) with
+// item = (z * B + b) * Hkv + kvh, covering all of the sequence's pages. One item
+// per group computes the global (M, Z) once and streams the group's logits in
+// one pass (latency-bound work: fewer, larger items keep more loads in flight).
+__device__ __forceinline__ Work epilogue_work(const AttnParams& p, int item) {
+  const int kvh = item % p.Hkv, rest = item / p.Hkv;
+  const int b = rest % p.B, z = rest / p.B;
+  Work wk = find_work_at(p, p.chunk_first[b], kvh, z);
+  wk.jc = 0;
+  wk.k0 = 0;
+  wk.npg = wk.ntot;
+  return wk;
+}
+__device__ __forceinline__ int epilogue_items_per_layer(const AttnParams& p) { return p.B * p.Hkv; }
 
 // Claims an epilogue item of a finished launch: the next unclaimed (KV head,
 // chunk) of its first layer that has one left, as layer * per_layer + index,
@@ -665,20 +678,19 @@ __device__ __forceinline__ int claim_item(EpCounters* ctr, int nlayers, int per_
   return -1;
 }
 
-// The epilogue of a launch's items left over after its own CTAs, as a kernel of
-// its own launched as a programmatic dependent of that attention launch (for a
-// lone call, and for the last launch of a decode step): CTAs claim the items
-// still unclaimed in the launch's counters.
+// The epilogue of a launch's items, as a kernel of its own launched as a
+// programmatic dependent of that attention launch (for a lone call, and for the
+// last launch of a decode step): CTAs claim the launch's items.
 constexpr int kCombineThreads = 256;
 
 template <typename T, int G, int D>
 __global__ void __launch_bounds__(kCombineThreads) attn_combine_kernel(const __grid_constant__ AttnParams p) {
   __shared__ float sM[8], sIZ[8];
   __shared__ int s_item;
-  const int per_layer = p.total_chunks * p.Hkv;
+  const int per_layer = epilogue_items_per_layer(p);
   // wait here until the attention kernel's partials and spilled logits are complete and visible
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  const LayerBufs lb{p.part_o, p.part_m, p.part_z, p.spill, p.out, p.acc};
+  const LayerBufs lb{p.part_o, p.part_m, p.part_z, p.spill, p.out, p.acc, p.first_of_step != 0};
   for (;;) {
     __syncthreads();
     if (threadIdx.x == 0) s_item = claim_item(p.ep_own, p.nlayers, per_layer);
@@ -691,13 +703,10 @@ __global__ void __launch_bounds__(kCombineThreads) attn_combine_kernel(const __g
 }
 
 // The previous launch's epilogue, run by all warps of an attention CTA once its
-// own pages are done and its partial is written: CTAs that finish early do it
-// while the last ones still stream, and it never holds up the ring. Same
-// (chunk, KV head) split, since every layer of a step has the same chunk plan.
-// The items — one per (layer, KV head, chunk) of the previous launch — are
-// handed out by that launch's counters, so CTAs that finish their pages early
-// take most of them and the last CTAs to finish find none left. (Taking items
-// of this launch's own completed layers as well, with per-layer completion
+// own work units are done: CTAs that finish early do it while the last ones
+// still stream. The items — one per (layer, sequence, KV head) group of the
+// previous launch — are handed out by that launch's counters. (Taking items of
+// this launch's own completed layers as well, with per-layer completion
 // counts, measured slower: those items then displace page streaming instead of
 // filling the launch's tail.)
 template <typename T, int G, int D>
@@ -705,8 +714,9 @@ __device__ __forceinline__ void prev_launch_epilogue(const AttnParams& p, int ti
                                                      volatile int* s_item) {
   if (!p.has_prev) return;
   constexpr int NT = (kAttnWarps + 1) * 32;
-  const int per_layer = p.total_chunks * p.Hkv;
-  const LayerBufs lb{p.prev_part_o, p.prev_part_m, p.prev_part_z, p.prev_spill, p.prev_out, p.acc};
+  const int per_layer = epilogue_items_per_layer(p);
+  const LayerBufs lb{p.prev_part_o, p.prev_part_m, p.prev_part_z, p.prev_spill, p.prev_out, p.acc,
+                     p.prev_first_of_step != 0};
   for (;;) {
     __syncthreads();
     if (tid == 0) *s_item = claim_item(p.ep_prev, p.prev_nlayers, per_layer);

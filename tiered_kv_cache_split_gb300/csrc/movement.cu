@@ -320,7 +320,8 @@ __global__ void __launch_bounds__(kMoveThreads) move_kernel(const __grid_constan
 // ---------------------------------------------------------------- fold
 // One thread per slot of a sequence's attention page list: the slot's position
 // gets (sum over layer slices and KV heads of the accumulated weights) /
-// (L * Hq) in float64; the accumulator is cleared for the next step.
+// (L * Hq) in float64. The next step's first launch overwrites the slots, so
+// they are only read here (independent loads, no read-after-write chain).
 __global__ void fold_kernel(const __grid_constant__ FoldParams p) {
   const int b = blockIdx.y;
   const int64_t slot = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -339,12 +340,9 @@ __global__ void fold_kernel(const __grid_constant__ FoldParams p) {
   const int page = p.table[src][static_cast<int64_t>(b) * p.table_stride + k];
   const int64_t at = static_cast<int64_t>(p.page_base[b]) * kPage + slot;
   double sum = 0.0;
+  const float* __restrict__ acc = p.acc;
   for (int z = 0; z < p.nslices; ++z)
-    for (int h = 0; h < p.Hkv; ++h) {
-      float* a = p.acc + z * p.acc_stride_l + h * p.acc_stride_h + at;
-      sum += static_cast<double>(*a);
-      *a = 0.f;
-    }
+    for (int h = 0; h < p.Hkv; ++h) sum += static_cast<double>(__ldg(acc + z * p.acc_stride_l + h * p.acc_stride_h + at));
   if ((p.mask[src][page] >> row) & 1u) {
     const int pos = p.posmap[src][static_cast<int64_t>(page) * kPage + row];
     if (pos >= 0) p.s[static_cast<int64_t>(b) * p.s_stride + pos] += sum * p.inv_lh;

@@ -774,6 +774,8 @@ tkv_status decode_step_device(tkv_ctx* h, const void* q, const void* k_new, cons
     p.has_prev = l0 > 0;
     p.prev_nlayers = p.nlayers;
     p.nlayers = nl;
+    p.prev_first_of_step = p.first_of_step;
+    p.first_of_step = l0 == 0;
     // counters rotate over four launches: this one's, the previous one's
     // (leftover items), and the one after next, which this launch zeroes
     p.ep_own = ring + h->attn_launch_seq % 4;

@@ -120,6 +120,11 @@ struct AttnParams {
   // (has_prev != 0); it covered prev_nlayers layers.
   int32_t has_prev;
   int32_t prev_nlayers;
+  // The first launch of a step covers layers 0 .. Lg-1, so its epilogue items
+  // are the first to touch every accumulator slot of the step: they write
+  // instead of adding (and the fold does not clear). 0 for a stateless call.
+  int32_t first_of_step;
+  int32_t prev_first_of_step;
   EpCounters* ep_own;     // this launch's counters (zero at launch; claimed by the next launch or the combine)
   EpCounters* ep_prev;    // the previous launch's counters (its epilogue items)
   EpCounters* ep_clear;   // counters of the launch after next, zeroed by this launch (or null)
@@ -231,7 +236,8 @@ cudaError_t launch_move(const MoveParams& p, const Mover* movers, int64_t count,
 
 // s[b][pos] += (sum over layer slices and KV heads of acc at the slot holding
 // pos) / (L * Hq); slots follow the attention page order (T0, T1, then T2 page
-// lists) from the sequence's page base; the accumulator is cleared.
+// lists) from the sequence's page base. The step's first launch wrote every
+// slot it reads, so nothing is cleared.
 struct FoldParams {
   int32_t B, Hkv, nslices;
   int32_t npages[3][kMaxBatch];
