@@ -149,3 +149,17 @@ def test_proposition_1_bitwise_on_the_tensor_core_path():
         ref = paged_attention(q[0, layer].unsqueeze(0).to(DEV), tp, table, mask_t, [len(layout)])
         assert torch.equal(ref[0].cpu(), out[0, layer].cpu()), f"layer {layer}"
     cache.close()
+
+
+def test_sixty_four_sequences_of_ragged_tiny_lengths():
+    # the batch limit (64 sequences), a one-token sequence and lengths around page
+    # boundaries, eight query heads per KV head at d = 64 (the tensor-core kernel's
+    # G = 8 variant), counted budgets so that even the shortest sequences tier
+    w = CHAIN7B.replace(n_layers=3, n_q_heads=16, n_kv_heads=2, head_dim=64, batch=64,
+                        context=("uniform", 1, 90), prompt_len=4, n_sink=2, recent_window=3,
+                        budget_mode="count", budgets=(12, 20, 8, 0), reclassify_interval=4, n_steps=12)
+    lens = w.context_lens()
+    assert min(lens) <= 3 and max(lens) >= 60
+    oc, stats = _lockstep(w, 12, [("stream", 0), ("mirror", 2), ("zerocopy", 1)])
+    counts = np.bincount(np.concatenate([oc.seqs[b].tier for b in range(w.batch)]), minlength=4)
+    assert np.all(counts > 0), counts

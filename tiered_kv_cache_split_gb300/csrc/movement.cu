@@ -26,19 +26,6 @@ __device__ __forceinline__ float load_elem(const char* p, int kv_dtype) {
   return *reinterpret_cast<const float*>(p);
 }
 
-__device__ __forceinline__ void store_elem(char* p, float v, int kv_dtype) {
-  if (kv_dtype == 1)
-    *reinterpret_cast<__nv_bfloat16*>(p) = __float2bfloat16_rn(v);
-  else
-    *reinterpret_cast<float*>(p) = v;
-}
-
-// Rounds a float32 to what the KV dtype stores (identity for float32).
-__device__ __forceinline__ float storage_round(float v, int kv_dtype) {
-  if (kv_dtype == 1) return __bfloat162float(__float2bfloat16_rn(v));
-  return v;
-}
-
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
   for (int m = 16; m >= 1; m >>= 1) v = fmaxf(v, __shfl_xor_sync(kFull, v, m));
