@@ -125,9 +125,9 @@ typedef struct {
   int64_t d2h_move_bytes;      /* bytes moved device -> host at reclassify */
   int64_t tier_counts[4];      /* current tokens per tier over all sequences */
   double attn_ms;              /* summed attention kernel time; each launch also finishes the
-                                  previous layer's output merge and score epilogue (TKV_FLAG_TIMING) */
-  double combine_ms;           /* summed time of the last layer's epilogue kernel, one launch per
-                                  step (TKV_FLAG_TIMING) */
+                                  previous launch's output merge and score epilogue (TKV_FLAG_TIMING) */
+  double combine_ms;           /* summed time of the epilogue kernel of each step's last launch
+                                  (TKV_FLAG_TIMING) */
   double prefetch_ms;          /* summed prefetch copy time      (TKV_FLAG_TIMING) */
   double reclassify_ms;        /* summed reclassify wall time    (TKV_FLAG_TIMING) */
   int64_t kernel_launches;     /* kernels this handle launched (steps, reclassify, prefill) */
@@ -202,6 +202,67 @@ TKV_API tkv_status tkv_synchronize(tkv_handle h);
  * publishes an empty partial, and the next synchronising call returns
  * TKV_ERR_TIMEOUT and marks h broken. No kernel traps or hangs. */
 TKV_API tkv_status tkv_test_stall_next_attention(tkv_handle h, uint64_t wait_limit_ns);
+
+/* Host-side fault injection (library plumbing for failure tests; the paper has
+ * none). Each site is a host call the library makes; when an armed site fires,
+ * the library reports that call as failed instead of making it. No device code
+ * is involved and nothing faults, traps or hangs on the GPU. */
+typedef enum {
+  TKV_FAULT_NONE = 0,
+  /* the workspace set-up inside tkv_create (event creation, clearing and
+   * initialising the device workspace): tkv_create returns TKV_ERR_CUDA,
+   * *out stays NULL and nothing the attempt created is left behind */
+  TKV_FAULT_ALLOC = 1,
+  /* a copy of caller host data to the device: the three input copies of
+   * tkv_decode_step_host and the copy of tkv_set_scores. Both run before
+   * anything changes: TKV_ERR_CUDA, state unchanged, handle usable */
+  TKV_FAULT_H2D = 2,
+  /* a copy of device data to a caller host buffer: tkv_get_scores,
+   * tkv_get_kv_row of a T0 row and the output of tkv_decode_step_host.
+   * TKV_ERR_CUDA, buffer not written, handle usable; for
+   * tkv_decode_step_host the step itself has taken effect */
+  TKV_FAULT_D2H = 3,
+  /* the enqueue of one layer group's T1/T2 prefetch (STREAM mode; a decode
+   * step makes one per layer group, tkv_prefetch one): a decode step stops
+   * half done, so TKV_ERR_CUDA marks the handle broken; the work already
+   * enqueued drains and tkv_destroy returns */
+  TKV_FAULT_PREFETCH = 4,
+  /* the allocator of the next reassignment finds a pool full: TKV_ERR_CAPACITY
+   * with tiers, page tables and scores unchanged, handle usable */
+  TKV_FAULT_CLASSIFY_OVERFLOW = 5
+} tkv_fault_site;
+
+/* Arms `site` so that the countdown-th time it is reached from now on
+ * (1 = the next time) it fails; one site per handle is armed at a time and
+ * firing disarms it; TKV_FAULT_NONE disarms. TKV_FAULT_ALLOC takes h = NULL
+ * and counts the set-up calls of the next tkv_create only (a countdown beyond
+ * them is dropped). The environment variable TKV_FAULT="<site>[:<countdown>]"
+ * with site alloc | h2d | d2h | prefetch | classify_overflow arms the same
+ * faults at each tkv_create (alloc: that create; others: the new handle).
+ * Errors: TKV_ERR_INVALID_ARG for an unknown site, a countdown < 1, or a
+ * handle given with TKV_FAULT_ALLOC / missing for the others. */
+TKV_API tkv_status tkv_test_inject_fault(tkv_handle h, int32_t site, int32_t countdown);
+
+/* 1 when this library is the debug build (compiled with TKV_DEBUG), else 0.
+ * The debug build checks on the device every page id, page-list index, score
+ * position and staging row a kernel derives from the bookkeeping against the
+ * area it indexes; a failed check records the check, the index and its bound
+ * and skips the access it guards (no trap), and the next synchronising call
+ * returns TKV_ERR_INTERNAL with those details and marks the handle broken.
+ * Release builds compile the checks away. */
+TKV_API int32_t tkv_debug_build(void);
+
+/* Test hook of the debug build (the paper has no counterpart): overwrites
+ * entry `index` of sequence seq's tier-`tier` page list (tier 0..2) in the
+ * device page table with that tier pool's capacity, the first page id past
+ * the pool's end, and returns it in *planted. Every address such an id can
+ * form lies inside the workspace that holds the pool (later regions of it
+ * follow each pool), so even an unchecked use would read allocated memory. The host
+ * bookkeeping keeps the true entry and the next metadata upload (an append or
+ * a reassignment) restores it; until then the index checks catch the id at
+ * the next decode step. Errors: TKV_ERR_STATE in a release build (nothing is
+ * written); TKV_ERR_INVALID_ARG for a bad sequence, tier or index. */
+TKV_API tkv_status tkv_test_plant_bad_page(tkv_handle h, int32_t seq, int32_t tier, int64_t index, int32_t* planted);
 
 /* Introspection and test hooks (host buffers; each synchronises). The scores
  * are the s_i of Methodology 2, the tiers those of Methodology 1; page tables

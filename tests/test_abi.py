@@ -124,3 +124,23 @@ def test_invalid_mode_fields_are_rejected(lib, field, value):
 def test_test_hook_and_status_calls_fail_cleanly_without_a_handle(lib):
     assert lib.tkv_test_stall_next_attention(None, 5_000_000) == L.ERR_INVALID_ARG
     assert lib.tkv_paged_attention_noalloc_status(None, None) == L.ERR_INVALID_ARG
+
+
+def test_fault_injection_arguments_are_checked_without_a_device(lib):
+    F = L.FAULT_SITES
+    assert lib.tkv_test_inject_fault(None, 9, 1) == L.ERR_INVALID_ARG           # unknown site
+    assert lib.tkv_test_inject_fault(None, -1, 1) == L.ERR_INVALID_ARG
+    assert lib.tkv_test_inject_fault(None, F["alloc"], 0) == L.ERR_INVALID_ARG  # countdown < 1
+    for site in ("h2d", "d2h", "prefetch", "classify_overflow"):               # need a handle
+        assert lib.tkv_test_inject_fault(None, F[site], 1) == L.ERR_INVALID_ARG
+        assert b"null handle" in lib.tkv_last_error(None)
+    # the allocation site is process-wide: arming and disarming touch no device
+    assert lib.tkv_test_inject_fault(None, F["alloc"], 3) == L.OK
+    assert lib.tkv_test_inject_fault(None, F["none"], 0) == L.OK
+
+
+def test_the_release_library_has_no_index_checks(lib):
+    assert lib.tkv_debug_build() == 0
+    planted = ctypes.c_int32(-7)
+    assert lib.tkv_test_plant_bad_page(None, 0, 1, 0, ctypes.byref(planted)) == L.ERR_INVALID_ARG
+    assert planted.value == -7

@@ -8,7 +8,9 @@ import ctypes
 import os
 
 HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(HERE, "libtkv.so")
+# TKV_LIB=debug selects the debug build (device index checks; build(debug=True))
+DEBUG = os.environ.get("TKV_LIB", "") == "debug"
+LIB_PATH = os.path.join(HERE, "libtkv_debug.so" if DEBUG else "libtkv.so")
 
 OK, ERR_INVALID_ARG, ERR_CAPACITY, ERR_STATE, ERR_CUDA, ERR_TIMEOUT, ERR_INTERNAL = range(7)
 STATUS_NAMES = ["OK", "INVALID_ARG", "CAPACITY", "STATE", "CUDA", "TIMEOUT", "INTERNAL"]
@@ -19,6 +21,7 @@ SCALE_F32, SCALE_F16 = 0, 1
 T2_ATTEND, T2_MASK = 0, 1
 HOST_TIERS = {"stream": 0, "mirror": 1, "zerocopy": 2}
 FLAG_TIMING = 1
+FAULT_SITES = {"none": 0, "alloc": 1, "h2d": 2, "d2h": 3, "prefetch": 4, "classify_overflow": 5}
 
 c_i32, c_i64, c_sz, c_vp = ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t, ctypes.c_void_p
 
@@ -81,6 +84,8 @@ _SIGS = {
                                     c_vp, c_vp, c_vp],
     "tkv_paged_attention_noalloc_status": [ctypes.POINTER(c_i32), c_vp],
     "tkv_test_stall_next_attention": [c_vp, ctypes.c_uint64],
+    "tkv_test_inject_fault": [c_vp, c_i32, c_i32],
+    "tkv_test_plant_bad_page": [c_vp, c_i32, c_i32, c_i64, ctypes.POINTER(c_i32)],
     "tkv_classify_scratch_size": [c_i32, c_i64, ctypes.POINTER(c_sz)],
     "tkv_classify": [c_i32, c_vp, c_vp, c_vp, c_i64, c_vp, c_i32, c_i32, c_vp, c_sz, c_vp],
     "tkv_quantize_rows": [c_vp, c_i32, c_i64, c_i32, c_vp, c_vp, c_i32, c_vp],
@@ -104,6 +109,8 @@ def load() -> ctypes.CDLL:
         fn.restype = ctypes.c_int
     lib.tkv_last_error.argtypes = [c_vp]
     lib.tkv_last_error.restype = ctypes.c_char_p
+    lib.tkv_debug_build.argtypes = []
+    lib.tkv_debug_build.restype = c_i32
     _lib = lib
     return lib
 
@@ -115,4 +122,4 @@ def check(status: int, handle=None) -> None:
 
 
 def exported_symbols() -> list[str]:
-    return sorted(list(_SIGS) + ["tkv_last_error"])
+    return sorted(list(_SIGS) + ["tkv_last_error", "tkv_debug_build"])

@@ -146,6 +146,20 @@ class TieredKVCache:
         bounded device wait (limit wait_limit_ns) runs out; see tkv.h."""
         self._check(self.lib.tkv_test_stall_next_attention(self.h, int(wait_limit_ns)))
 
+    def test_inject_fault(self, site: str, countdown: int = 1):
+        """Test hook: the countdown-th visit of host call site `site` ("h2d",
+        "d2h", "prefetch", "classify_overflow"; "none" disarms) is reported as
+        failed; see tkv.h."""
+        self._check(self.lib.tkv_test_inject_fault(self.h, L.FAULT_SITES[site], int(countdown)))
+
+    def test_plant_bad_page(self, seq: int, tier: int, index: int) -> int:
+        """Debug-build test hook: page-list entry `index` of (seq, tier) in the
+        device table becomes the pool's capacity (one past its end); returns
+        that id. See tkv.h."""
+        planted = ctypes.c_int32()
+        self._check(self.lib.tkv_test_plant_bad_page(self.h, seq, tier, index, ctypes.byref(planted)))
+        return planted.value
+
     def num_sequences(self) -> int:
         n = ctypes.c_int32()
         self._check(self.lib.tkv_num_sequences(self.h, ctypes.byref(n)))
@@ -213,6 +227,16 @@ class TieredKVCache:
 
     def reset_stats(self):
         self._check(self.lib.tkv_reset_stats(self.h))
+
+
+def inject_create_fault(countdown: int = 1):
+    """Test hook: the countdown-th set-up call of the next tkv_create is
+    reported as failed (0 disarms); see tkv.h."""
+    lib = L.load()
+    if countdown == 0:
+        L.check(lib.tkv_test_inject_fault(None, 0, 0))
+    else:
+        L.check(lib.tkv_test_inject_fault(None, L.FAULT_SITES["alloc"], int(countdown)))
 
 
 # ------------------------------------------------------------ stateless calls

@@ -204,7 +204,8 @@ __device__ __forceinline__ void page_ref(const AttnParams& p, int b, int k, int&
       src = 2;
     }
   }
-  page = p.src[src].table[static_cast<int64_t>(b) * p.table_stride + kk];
+  page = index_ok(p.err, DBG_ATTN_LIST, kk, p.table_stride) ? p.src[src].table[static_cast<int64_t>(b) * p.table_stride + kk]
+                                                              : -1;
 }
 
 // What a CTA needs to know about its work item.
@@ -319,9 +320,12 @@ __device__ __forceinline__ void resolve_page(const AttnParams& p, const Work& wk
   int src, page;
   page_ref(p, wk.b, k, src, page);
   const PageSource& ps = p.src[src];
+  // debug build: a page id outside its pool reads page 0 with no valid slot instead
+  const bool page_ok = index_ok(p.err, DBG_ATTN_PAGE, page, ps.pages);
+  if (!page_ok) page = 0;
   meta_k[slot] = k;
   const bool i8 = ps.kind == SRC_INT8;
-  meta_f[slot] = page_flags(ps.mask[page], i8, ps.scale_per_head != 0, ps.swz, ps.host != 0);
+  meta_f[slot] = page_flags(page_ok ? ps.mask[page] : 0u, i8, ps.scale_per_head != 0, ps.swz, ps.host != 0);
   PageCopy c;
   c.src = reinterpret_cast<unsigned long long>(ps.base + wk.z * ps.layer_bytes + static_cast<int64_t>(page) * ps.page_bytes +
                                                static_cast<int64_t>(wk.kvh) * ps.head_bytes) |

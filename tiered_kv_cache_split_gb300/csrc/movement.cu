@@ -58,6 +58,10 @@ __device__ __forceinline__ int8_t quant_code(float x, float divisor) {
 __global__ void append_kernel(const __grid_constant__ AppendParams p) {
   const int b = blockIdx.x, l = blockIdx.y;
   const int page = p.page[b], slot = p.slot[b];
+  // debug build: a page outside the pool or a page list that would outgrow its row skips the block
+  if (!index_ok(p.err, DBG_APPEND_PAGE, page, p.cap0) ||
+      (p.new_page[b] && !index_ok(p.err, DBG_APPEND_LIST, p.np0[b], p.table_stride)))
+    return;
   const int row_bytes = p.D * p.esz;
   const int vec_per_row = row_bytes / 16;
   const int total = p.Hkv * 2 * vec_per_row;
@@ -101,6 +105,7 @@ __global__ void prefill_kernel(const __grid_constant__ PrefillParams p) {
   if (t >= p.n) return;
   const int loc = p.loc[t];
   const int page = loc >> 4, slot = loc & 15;
+  if (!index_ok(p.err, DBG_PREFILL_PAGE, page, p.cap0)) return;  // debug build only
   const int row_bytes = p.D * p.esz;
   const int vec_per_row = row_bytes / 16;
   const int total = p.Hkv * 2 * vec_per_row;
@@ -177,6 +182,11 @@ __global__ void __launch_bounds__(kMoveThreads) move_kernel(const __grid_constan
   // staging row of this (mover, layer): one per mover when the launch covers one
   // layer, one per (mover, layer) when it covers several
   const int trow = mv.temp_row * static_cast<int>(gridDim.y) + static_cast<int>(blockIdx.y);
+  // debug build: the mover's pages and staging row against their areas (skips the block)
+  if (!(st < 0 || index_ok(p.err, DBG_MOVE_SRC, mv.src_loc >> 4, P.cap[st])) ||
+      !(dt < 0 || index_ok(p.err, DBG_MOVE_DST, mv.dst_loc >> 4, P.cap[dt])) ||
+      !((st >= 0 && dt >= 0) || index_ok(p.err, DBG_MOVE_TEMP, trow, p.temp_rows)))
+    return;
   // With a device mirror of T1 / T2, sources there are read from the mirror (no
   // host-link read) and destinations there are written to the pool and the mirror.
   const bool src_mirror = st >= 1 && P.mirror[st] != nullptr;
@@ -325,6 +335,7 @@ __global__ void fold_kernel(const __grid_constant__ FoldParams p) {
     }
   }
   const int page = p.table[src][static_cast<int64_t>(b) * p.table_stride + k];
+  if (!index_ok(p.err, DBG_FOLD_PAGE, page, p.cap[src])) return;  // debug build only
   const int64_t at = static_cast<int64_t>(p.page_base[b]) * kPage + slot;
   double sum = 0.0;
   const float* __restrict__ acc = p.acc;
@@ -332,7 +343,8 @@ __global__ void fold_kernel(const __grid_constant__ FoldParams p) {
     for (int h = 0; h < p.Hkv; ++h) sum += static_cast<double>(__ldg(acc + z * p.acc_stride_l + h * p.acc_stride_h + at));
   if ((p.mask[src][page] >> row) & 1u) {
     const int pos = p.posmap[src][static_cast<int64_t>(page) * kPage + row];
-    if (pos >= 0) p.s[static_cast<int64_t>(b) * p.s_stride + pos] += sum * p.inv_lh;
+    if (pos >= 0 && index_ok(p.err, DBG_FOLD_POS, pos, p.s_stride))
+      p.s[static_cast<int64_t>(b) * p.s_stride + pos] += sum * p.inv_lh;
   }
 }
 

@@ -20,10 +20,13 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <chrono>
 #include <cmath>
 #include <cstdarg>
+#include <cstdint>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <functional>
 #include <mutex>
@@ -49,6 +52,8 @@ static_assert(kEpOffset + 4 * sizeof(EpCounters) <= kErrRegion, "error region to
 size_t align_up(size_t x, size_t a = kAlign) { return (x + a - 1) / a * a; }
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+// a pool capacity as the int32 page bound of the device index checks
+int32_t cap32(int64_t pages) { return static_cast<int32_t>(std::min<int64_t>(pages, INT32_MAX)); }
 
 using MinHeap = std::priority_queue<int64_t, std::vector<int64_t>, std::greater<int64_t>>;
 
@@ -258,6 +263,8 @@ struct tkv_ctx {
   int64_t last_launch_seq = 0;    // number of the last attention launch actually enqueued (0: none)
   bool stall_next = false;        // test hook: the next attention launch withholds one page
   unsigned long long wait_limit_ns = 2000000000ull;  // bounded device waits give up after this long
+  int32_t fault_site = TKV_FAULT_NONE;  // test hook: host call reported as failed when its countdown ends
+  int32_t fault_countdown = 0;
   int64_t span_from = 0;          // first attention launch counted in attn_span_ms
   // Copy-stream gate: a prefetch waits (stream memory wait) until the previous
   // attention launch has started, so that launch is not made behind a host
@@ -299,6 +306,59 @@ tkv_status fail_cuda(tkv_ctx* h, const char* what, cudaError_t e) {
   if (h) h->broken = true;
   return fail(h, TKV_ERR_CUDA, "%s failed: %s", what, cudaGetErrorString(e));
 }
+
+// ---- host-side fault injection (tkv_test_inject_fault, TKV_FAULT)
+
+// Set-up calls of the next tkv_create until one is reported as failed (0: off).
+std::atomic<int32_t> g_create_fault{0};
+
+// True when `site` is armed on h and its countdown ends with this visit.
+bool fault_fires(tkv_ctx* h, int32_t site) {
+  if (!h || site == TKV_FAULT_NONE || h->fault_site != site) return false;
+  if (--h->fault_countdown > 0) return false;
+  h->fault_site = TKV_FAULT_NONE;
+  return true;
+}
+
+tkv_status injected(tkv_ctx* h, const char* what) {
+  return fail(h, TKV_ERR_CUDA, "%s failed: injected host-side fault", what);
+}
+
+// TKV_FAULT="<site>[:<countdown>]"; false when unset or malformed.
+bool fault_from_env(int32_t* site, int32_t* countdown) {
+  const char* v = std::getenv("TKV_FAULT");
+  if (!v || !*v) return false;
+  static const struct { const char* name; int32_t site; } names[] = {
+      {"alloc", TKV_FAULT_ALLOC}, {"h2d", TKV_FAULT_H2D}, {"d2h", TKV_FAULT_D2H},
+      {"prefetch", TKV_FAULT_PREFETCH}, {"classify_overflow", TKV_FAULT_CLASSIFY_OVERFLOW}};
+  const char* colon = std::strchr(v, ':');
+  const size_t n = colon ? size_t(colon - v) : std::strlen(v);
+  long cd = 1;
+  if (colon) {
+    char* end = nullptr;
+    cd = std::strtol(colon + 1, &end, 10);
+    if (end == colon + 1 || *end != '\0' || cd < 1 || cd > INT32_MAX) return false;
+  }
+  for (const auto& e : names)
+    if (std::strlen(e.name) == n && std::strncmp(v, e.name, n) == 0) {
+      *site = e.site;
+      *countdown = static_cast<int32_t>(cd);
+      return true;
+    }
+  return false;
+}
+
+// A copy between caller memory and the device made before anything changes or
+// after everything has: its failure leaves the handle usable (a failure that
+// took the context down shows again at the next synchronising call).
+#define CK_SOFT(h, what, call)                                                              \
+  do {                                                                                      \
+    cudaError_t e_ = (call);                                                                \
+    if (e_ != cudaSuccess) {                                                                \
+      (void)cudaGetLastError();                                                             \
+      return fail((h), TKV_ERR_CUDA, "%s failed: %s", (what), cudaGetErrorString(e_));      \
+    }                                                                                       \
+  } while (0)
 
 #define CK(h, call)                                            \
   do {                                                         \
@@ -354,12 +414,28 @@ tkv_status timed_pair(tkv_ctx* h, int kind, TimedPair* out) {
 tkv_status sync_all(tkv_ctx* h) {
   CK(h, cudaStreamSynchronize(h->cs));
   if (h->xs != h->cs) CK(h, cudaStreamSynchronize(h->xs));
-  int32_t e = 0;
-  CK(h, cudaMemcpy(&e, h->D(h->y.o_err), 4, cudaMemcpyDeviceToHost));
+  // error word, site, index, bound (the last three written by the debug build's index checks)
+  int32_t rec[6] = {0, 0, 0, 0, 0, 0};
+  CK(h, cudaMemcpy(rec, h->D(h->y.o_err), sizeof rec, cudaMemcpyDeviceToHost));
+  const int32_t e = rec[0];
   harvest(h);
   if (e == DEV_TIMEOUT) {
     h->broken = true;
     return fail(h, TKV_ERR_TIMEOUT, "a bounded device wait gave up (copy never landed)");
+  }
+  if (e == DEV_BAD_INDEX) {
+    h->broken = true;
+    static const char* const kSite[kDebugSites] = {
+        "attention chunk larger than the page limit", "attention page-list index", "attention page id",
+        "score fold page id", "score fold position", "append page id", "append page-list length",
+        "prefill page id", "mover source page", "mover destination page", "mover staging row"};
+    const int site = rec[1];
+    long long idx = 0, bound = 0;
+    std::memcpy(&idx, rec + 2, 8);
+    std::memcpy(&bound, rec + 4, 8);
+    if (site <= DBG_NONE || site >= kDebugSites)
+      return fail(h, TKV_ERR_INTERNAL, "device index check failed: %s", kSite[0]);
+    return fail(h, TKV_ERR_INTERNAL, "device index check failed: %s %lld outside [0, %lld)", kSite[site], idx, bound);
   }
   if (e != 0) {
     h->broken = true;
@@ -451,10 +527,6 @@ void vacate(tkv_ctx* h, Seq& sq, int t, int64_t pos) {
   h->posmap[t][page * kPage + slot] = -1;
   sq.holes[t].push(code);
   sq.loc[pos] = -1;
-}
-
-int64_t total_pages(const Seq& sq, bool with_t2) {
-  return int64_t(sq.pages[0].size() + sq.pages[1].size()) + (with_t2 ? int64_t(sq.pages[2].size()) : 0);
 }
 
 tkv_status upload_metadata(tkv_ctx* h) {
@@ -563,6 +635,10 @@ int plan_chunks(const std::vector<int64_t>& ntot, const std::vector<int64_t>& co
 tkv_status enqueue_prefetch(tkv_ctx* h, int l0, int nl, int slot, uint32_t gate_seq = 0) {
   const Layout& y = h->y;
   if (y.mode != TKV_HOST_TIERS_STREAM) return TKV_OK;
+  if (fault_fires(h, TKV_FAULT_PREFETCH)) {
+    h->broken = true;  // a decode step stops half done
+    return injected(h, "T1/T2 prefetch enqueue");
+  }
   const bool timing = h->cfg.flags & TKV_FLAG_TIMING;
   TimedPair tp{};
   if (h->xs != h->cs) CK(h, cudaStreamWaitEvent(h->xs, h->ev_free[slot], 0));
@@ -631,12 +707,12 @@ void fill_sources(tkv_ctx* h, int l0, int slot, AttnParams& p) {
     host = 1;
   }
   p.src[0] = PageSource{h->D(y.o_pool0) + size_t(l0) * lb0, lb0, y.plb[0], head_full, d_table(h, 0), d_mask(h, 0),
-                        d_posmap(h, 0), nullptr, 0, 0, 0, SRC_FULL, kSwizzle, 0};
+                        d_posmap(h, 0), nullptr, 0, 0, 0, SRC_FULL, kSwizzle, 0, cap32(y.cap[0])};
   p.src[1] = PageSource{b1, lb1, y.plb[1], head_full, d_table(h, 1), d_mask(h, 1), d_posmap(h, 1), nullptr, 0, 0, 0,
-                        SRC_FULL, kSwizzle, host};
+                        SRC_FULL, kSwizzle, host, cap32(y.cap[1])};
   p.src[2] = PageSource{b2, lb2, y.plb[2], int64_t(2) * kPage * y.D, d_table(h, 2), d_mask(h, 2), d_posmap(h, 2),
                         b2s, lbs, y.scale_rec, h->cfg.t2_scale_gran == TKV_SCALE_PER_TOKEN_HEAD ? 1 : 0, SRC_INT8, 0,
-                        host};
+                        host, cap32(y.cap[2])};
   p.nsrc = 3;
 }
 
@@ -681,6 +757,8 @@ tkv_status decode_step_device(tkv_ctx* h, const void* q, const void* k_new, cons
   ap.pool0 = h->D(y.o_pool0); ap.layer_bytes = y.cap[0] * y.plb[0]; ap.page_bytes = y.plb[0];
   ap.mask0 = d_mask(h, 0); ap.posmap0 = d_posmap(h, 0); ap.table0 = d_table(h, 0);
   ap.table_stride = static_cast<int32_t>(y.maxp);
+  ap.err = reinterpret_cast<int32_t*>(h->D(y.o_err));
+  ap.cap0 = cap32(y.cap[0]);
   for (int b = 0; b < B; ++b) {
     Seq& sq = h->seqs[b];
     const int64_t pos = sq.N;
@@ -846,6 +924,8 @@ tkv_status decode_step_device(tkv_ctx* h, const void* q, const void* k_new, cons
   fp.acc_stride_h = p.acc_stride_h;
   fp.acc_stride_l = p.acc_stride_l;
   fp.inv_lh = 1.0 / (double(y.L) * double(y.Hq));
+  fp.err = reinterpret_cast<int32_t*>(h->D(y.o_err));
+  for (int t = 0; t < 3; ++t) fp.cap[t] = cap32(y.cap[t]);
   LK(h, launch_fold(fp, h->cs), fp.B > 0 && fp.max_slots > 0);
 
   h->steps += 1;
@@ -935,6 +1015,7 @@ tkv_status do_reclassify(tkv_ctx* h) {
 
   std::vector<Mover> phase1, phase2, compaction;
   int64_t d2h = 0, h2d = 0;
+  const bool overflow = fault_fires(h, TKV_FAULT_CLASSIFY_OVERFLOW);
   const int64_t row_full = int64_t(y.L) * 2 * y.Hkv * y.D * y.esz;
   const int64_t row_i8 = int64_t(y.L) * (2 * y.Hkv * y.D + (h->cfg.t2_scale_gran == TKV_SCALE_PER_TOKEN ? 8 : 4 * y.Hkv));
   for (int b = 0; b < B; ++b) {
@@ -972,9 +1053,13 @@ tkv_status do_reclassify(tkv_ctx* h) {
           idx.push_back(m);
         }
       std::vector<int32_t> locs;
-      if (!place(h, sq, b, t, arrivals, &locs)) {
+      // an injected overflow fires at the last placement, after every other sequence's
+      // vacates, placements and compaction have touched the bookkeeping
+      const bool inject_now = overflow && b == B - 1 && t == 2;
+      if (inject_now || !place(h, sq, b, t, arrivals, &locs)) {
         restore();
-        return fail(h, TKV_ERR_CAPACITY, "tier %d pool or page list full during reassignment", t);
+        return fail(h, TKV_ERR_CAPACITY, "tier %d pool or page list full during reassignment%s", t,
+                    inject_now ? " (injected host-side fault)" : "");
       }
       for (size_t a = 0; a < idx.size(); ++a) dst_loc[idx[a]] = locs[a];
     }
@@ -1040,7 +1125,10 @@ tkv_status do_reclassify(tkv_ctx* h) {
     mp.pools.mirror_scales = h->D(y.o_mirror2s);
   }
   mp.pools.scale_f16 = h->cfg.t2_scale_dtype == TKV_SCALE_F16;
+  for (int t = 0; t < 3; ++t) mp.pools.cap[t] = cap32(y.cap[t]);
   mp.temp = h->D(y.o_temp);
+  mp.temp_rows = y.temp_rows;
+  mp.err = reinterpret_cast<int32_t*>(h->D(y.o_err));
   // Every source is read before any slot is written that a mover vacated:
   // phase 1 (destinations no mover vacated) reads its sources and writes at
   // once, for all layers; then, layer by layer, phase 2 gathers its sources
@@ -1115,6 +1203,11 @@ tkv_status tkv_create(const tkv_config* cfg, void* dev_ws, size_t dev_bytes, voi
   if (dev_bytes < y.dev_bytes || pinned_bytes < y.pinned_bytes)
     return fail(nullptr, TKV_ERR_CAPACITY, "workspace too small: need %zu device and %zu pinned bytes",
                 y.dev_bytes, y.pinned_bytes);
+  // fault injection: the set-up call that fails (0: none), and a site the environment arms on the handle
+  int32_t setup_fault = g_create_fault.exchange(0);
+  int32_t env_site = TKV_FAULT_NONE, env_countdown = 0;
+  if (fault_from_env(&env_site, &env_countdown) && env_site == TKV_FAULT_ALLOC && setup_fault == 0)
+    setup_fault = env_countdown;
   tkv_ctx* h = new (std::nothrow) tkv_ctx();
   if (!h) return fail(nullptr, TKV_ERR_INTERNAL, "out of host memory");
   h->cfg = *cfg;
@@ -1123,23 +1216,32 @@ tkv_status tkv_create(const tkv_config* cfg, void* dev_ws, size_t dev_bytes, voi
   h->pin = static_cast<char*>(pinned_ws);
   h->cs = static_cast<cudaStream_t>(compute);
   h->xs = copy ? static_cast<cudaStream_t>(copy) : h->cs;
+  bool enqueued = false;  // clearing of the caller's workspace was enqueued on the compute stream
   auto bail = [&](tkv_status st) {
+    if (enqueued) (void)cudaStreamSynchronize(h->cs);  // the workspace goes back to the caller idle
     for (int i = 0; i < 2; ++i) {
       if (h->ev_ready[i]) cudaEventDestroy(h->ev_ready[i]);
       if (h->ev_free[i]) cudaEventDestroy(h->ev_free[i]);
     }
     delete h;
+    (void)cudaGetLastError();
     return st;
   };
+  // the set-up calls below, counted for fault injection
+  auto setup_fails = [&]() { return setup_fault > 0 && --setup_fault == 0; };
   cudaError_t e = cudaGetDevice(&h->device);
   if (e != cudaSuccess) return bail(fail_cuda(nullptr, "cudaGetDevice", e));
   void* mapped = nullptr;
+  if (setup_fails()) return bail(injected(nullptr, "cudaHostGetDevicePointer"));
   e = cudaHostGetDevicePointer(&mapped, pinned_ws, 0);
   if (e != cudaSuccess) return bail(fail_cuda(nullptr, "cudaHostGetDevicePointer (pinned workspace must be page-locked)", e));
   h->pin_dev = static_cast<char*>(mapped);
   for (int i = 0; i < 2; ++i) {
-    if ((e = cudaEventCreateWithFlags(&h->ev_ready[i], cudaEventDisableTiming)) != cudaSuccess ||
-        (e = cudaEventCreateWithFlags(&h->ev_free[i], cudaEventDisableTiming)) != cudaSuccess)
+    if (setup_fails()) return bail(injected(nullptr, "cudaEventCreate"));
+    if ((e = cudaEventCreateWithFlags(&h->ev_ready[i], cudaEventDisableTiming)) != cudaSuccess)
+      return bail(fail_cuda(nullptr, "cudaEventCreate", e));
+    if (setup_fails()) return bail(injected(nullptr, "cudaEventCreate"));
+    if ((e = cudaEventCreateWithFlags(&h->ev_free[i], cudaEventDisableTiming)) != cudaSuccess)
       return bail(fail_cuda(nullptr, "cudaEventCreate", e));
   }
   h->d_tier = reinterpret_cast<uint8_t*>(h->D(y.o_tier));
@@ -1168,20 +1270,30 @@ tkv_status tkv_create(const tkv_config* cfg, void* dev_ws, size_t dev_bytes, voi
       {y.o_mirror1, y.mode == TKV_HOST_TIERS_MIRROR ? size_t(y.L) * y.cap[1] * y.plb[1] : 0, 0},
       {y.o_mirror2c, y.mode == TKV_HOST_TIERS_MIRROR ? size_t(y.L) * y.cap[2] * y.plb[2] : 0, 0},
       {y.o_mirror2s, y.mode == TKV_HOST_TIERS_MIRROR ? size_t(y.L) * y.cap[2] * y.scale_rec : 0, 0}};
-  for (const Z& z : zs)
-    if (z.bytes && (e = cudaMemsetAsync(h->D(z.off), z.val, z.bytes, h->cs)) != cudaSuccess)
+  for (const Z& z : zs) {
+    if (!z.bytes) continue;
+    if (setup_fails()) return bail(injected(nullptr, "cudaMemsetAsync"));
+    enqueued = true;
+    if ((e = cudaMemsetAsync(h->D(z.off), z.val, z.bytes, h->cs)) != cudaSuccess)
       return bail(fail_cuda(nullptr, "cudaMemsetAsync", e));
+  }
   {
     std::vector<unsigned long long> init(2 * size_t(kSpanSlots), 0ull);
     for (int i = 0; i < kSpanSlots; ++i) init[2 * size_t(i)] = ~0ull;
+    if (setup_fails()) return bail(injected(nullptr, "cudaMemcpy"));
     if ((e = cudaMemcpy(h->D(y.o_span), init.data(), init.size() * 8, cudaMemcpyHostToDevice)) != cudaSuccess)
       return bail(fail_cuda(nullptr, "cudaMemcpy", e));
   }
+  if (setup_fails()) return bail(injected(nullptr, "cudaStreamSynchronize"));
   if ((e = cudaStreamSynchronize(h->cs)) != cudaSuccess) return bail(fail_cuda(nullptr, "cudaStreamSynchronize", e));
   for (int t = 0; t < 3; ++t) {
     h->mask[t].assign(size_t(y.cap[t]), 0u);
     h->posmap[t].assign(size_t(y.cap[t]) * kPage, -1);
     h->table[t].assign(size_t(y.maxb) * y.maxp, 0);
+  }
+  if (env_site != TKV_FAULT_NONE && env_site != TKV_FAULT_ALLOC) {
+    h->fault_site = env_site;
+    h->fault_countdown = env_countdown;
   }
   *out = h;
   return TKV_OK;
@@ -1242,6 +1354,8 @@ tkv_status tkv_append(tkv_handle h, int32_t seq, const void* k, const void* v, i
   pp.L = y.L; pp.Hkv = y.Hkv; pp.D = y.D; pp.esz = y.esz; pp.n = n_tokens;
   pp.k = static_cast<const char*>(k); pp.v = static_cast<const char*>(v); pp.loc = dl;
   pp.pool0 = h->D(y.o_pool0); pp.layer_bytes = y.cap[0] * y.plb[0]; pp.page_bytes = y.plb[0];
+  pp.err = reinterpret_cast<int32_t*>(h->D(y.o_err));
+  pp.cap0 = cap32(y.cap[0]);
   LK(h, launch_prefill(pp, h->cs), n_tokens > 0);
   if (tkv_status st = upload_metadata(h)) return st;
   return sync_all(h);
@@ -1267,11 +1381,30 @@ tkv_status tkv_decode_step_host(tkv_handle h, const void* q, const void* k_new, 
   char* dk = io + y.io_k;
   char* dv = dk + align_up(size_t(y.maxb) * y.L * y.Hkv * y.D * y.esz);
   char* dout = io + y.io_out;
-  CK(h, cudaMemcpyAsync(dq, q, qb, cudaMemcpyHostToDevice, h->cs));
-  CK(h, cudaMemcpyAsync(dk, k_new, kb, cudaMemcpyHostToDevice, h->cs));
-  CK(h, cudaMemcpyAsync(dv, v_new, kb, cudaMemcpyHostToDevice, h->cs));
+  // the inputs land in the I/O area, which holds no state: a failed copy changes nothing
+  const struct { char* dst; const void* src; size_t n; const char* what; } in[] = {
+      {dq, q, qb, "cudaMemcpyAsync (query to device)"},
+      {dk, k_new, kb, "cudaMemcpyAsync (new keys to device)"},
+      {dv, v_new, kb, "cudaMemcpyAsync (new values to device)"}};
+  bool issued = false;
+  for (const auto& c : in) {
+    tkv_status st = TKV_OK;
+    if (fault_fires(h, TKV_FAULT_H2D)) {
+      st = injected(h, c.what);
+    } else if (cudaError_t e = cudaMemcpyAsync(c.dst, c.src, c.n, cudaMemcpyHostToDevice, h->cs); e != cudaSuccess) {
+      (void)cudaGetLastError();
+      st = fail(h, TKV_ERR_CUDA, "%s failed: %s", c.what, cudaGetErrorString(e));
+    }
+    if (st) {
+      // earlier copies may still read the caller's buffers: let them land before returning
+      if (issued && cudaStreamSynchronize(h->cs) != cudaSuccess) h->broken = true;
+      return st;
+    }
+    issued = true;
+  }
   if (tkv_status st = decode_step_device(h, dq, dk, dv, dout)) return st;
-  CK(h, cudaMemcpyAsync(out, dout, qb, cudaMemcpyDeviceToHost, h->cs));
+  if (fault_fires(h, TKV_FAULT_D2H)) return injected(h, "cudaMemcpyAsync (output to host)");
+  CK_SOFT(h, "cudaMemcpyAsync (output to host)", cudaMemcpyAsync(out, dout, qb, cudaMemcpyDeviceToHost, h->cs));
   CK(h, cudaStreamSynchronize(h->cs));
   return TKV_OK;
 }
@@ -1301,6 +1434,42 @@ tkv_status tkv_test_stall_next_attention(tkv_handle h, uint64_t wait_limit_ns) {
   return TKV_OK;
 }
 
+tkv_status tkv_test_inject_fault(tkv_handle h, int32_t site, int32_t countdown) {
+  if (site < TKV_FAULT_NONE || site > TKV_FAULT_CLASSIFY_OVERFLOW) return fail(h, TKV_ERR_INVALID_ARG, "unknown fault site %d", site);
+  if (site != TKV_FAULT_NONE && countdown < 1) return fail(h, TKV_ERR_INVALID_ARG, "countdown must be >= 1");
+  if (site == TKV_FAULT_ALLOC) {
+    if (h) return fail(h, TKV_ERR_INVALID_ARG, "the allocation site arms the next tkv_create: pass no handle");
+    g_create_fault.store(countdown);
+    return TKV_OK;
+  }
+  if (!h) {
+    if (site != TKV_FAULT_NONE) return fail(nullptr, TKV_ERR_INVALID_ARG, "null handle");
+    g_create_fault.store(0);
+    return TKV_OK;
+  }
+  h->fault_site = site;
+  h->fault_countdown = site == TKV_FAULT_NONE ? 0 : countdown;
+  return TKV_OK;
+}
+
+int32_t tkv_debug_build(void) { return kDebugBuild ? 1 : 0; }
+
+tkv_status tkv_test_plant_bad_page(tkv_handle h, int32_t seq, int32_t tier, int64_t index, int32_t* planted) {
+  if (tkv_status st = check_usable(h)) return st;
+  if (!kDebugBuild) return fail(h, TKV_ERR_STATE, "the page-table test hook needs the debug build (TKV_DEBUG)");
+  if (tkv_status st = seq_ok(h, seq)) return st;
+  if (tier < 0 || tier > 2) return fail(h, TKV_ERR_INVALID_ARG, "tier must be 0, 1 or 2");
+  if (index < 0 || index >= int64_t(h->seqs[seq].pages[tier].size()))
+    return fail(h, TKV_ERR_INVALID_ARG, "index %lld outside the page list", (long long)index);
+  if (!planted) return fail(h, TKV_ERR_INVALID_ARG, "null output");
+  if (tkv_status st = sync_all(h)) return st;
+  const int32_t id = cap32(h->y.cap[tier]);
+  int32_t* at = d_table(h, tier) + size_t(seq) * h->y.maxp + size_t(index);
+  CK(h, cudaMemcpy(at, &id, 4, cudaMemcpyHostToDevice));
+  *planted = id;
+  return TKV_OK;
+}
+
 tkv_status tkv_num_sequences(tkv_handle h, int32_t* n) {
   if (!h || !n) return fail(h, TKV_ERR_INVALID_ARG, "null argument");
   *n = static_cast<int32_t>(h->seqs.size());
@@ -1319,7 +1488,9 @@ tkv_status tkv_get_scores(tkv_handle h, int32_t seq, double* host_out, int64_t n
   if (tkv_status st = seq_ok(h, seq)) return st;
   if (!host_out || n < 0 || n > h->seqs[seq].N) return fail(h, TKV_ERR_INVALID_ARG, "bad output or n");
   if (tkv_status st = sync_all(h)) return st;
-  CK(h, cudaMemcpy(host_out, h->D(h->y.o_s) + size_t(seq) * h->y.maxtok * 8, size_t(n) * 8, cudaMemcpyDeviceToHost));
+  if (fault_fires(h, TKV_FAULT_D2H)) return injected(h, "cudaMemcpy (scores to host)");
+  CK_SOFT(h, "cudaMemcpy (scores to host)",
+          cudaMemcpy(host_out, h->D(h->y.o_s) + size_t(seq) * h->y.maxtok * 8, size_t(n) * 8, cudaMemcpyDeviceToHost));
   return TKV_OK;
 }
 
@@ -1333,7 +1504,9 @@ tkv_status tkv_set_scores(tkv_handle h, int32_t seq, const double* host_in, int6
     if (x == 0.0) x = 0.0;
   }
   if (tkv_status st = sync_all(h)) return st;
-  CK(h, cudaMemcpy(h->D(h->y.o_s) + size_t(seq) * h->y.maxtok * 8, s.data(), size_t(n) * 8, cudaMemcpyHostToDevice));
+  if (fault_fires(h, TKV_FAULT_H2D)) return injected(h, "cudaMemcpy (scores to device)");
+  CK_SOFT(h, "cudaMemcpy (scores to device)",
+          cudaMemcpy(h->D(h->y.o_s) + size_t(seq) * h->y.maxtok * 8, s.data(), size_t(n) * 8, cudaMemcpyHostToDevice));
   return TKV_OK;
 }
 
@@ -1404,13 +1577,14 @@ tkv_status tkv_get_kv_row(tkv_handle h, int32_t seq, int64_t pos, void* k, void*
   const int64_t page = sq.loc[pos] / kPage, slot = sq.loc[pos] % kPage;
   const size_t rb = size_t(y.D) * y.esz;
   std::vector<char> raw(rb);
+  if (t == 0 && fault_fires(h, TKV_FAULT_D2H)) return injected(h, "cudaMemcpy (T0 row to host)");
   for (int l = 0; l < y.L; ++l)
     for (int kv = 0; kv < 2; ++kv)
       for (int hh = 0; hh < y.Hkv; ++hh) {
         char* dst = static_cast<char*>(kv ? v : k) + (size_t(l) * y.Hkv + hh) * rb;
         const size_t off = (size_t(l) * y.cap[t] + page) * y.plb[t] + ((size_t(hh) * 2 + kv) * kPage + slot) * rb;
         if (t == 0)
-          CK(h, cudaMemcpy(raw.data(), h->D(y.o_pool0) + off, rb, cudaMemcpyDeviceToHost));
+          CK_SOFT(h, "cudaMemcpy (T0 row to host)", cudaMemcpy(raw.data(), h->D(y.o_pool0) + off, rb, cudaMemcpyDeviceToHost));
         else
           std::memcpy(raw.data(), h->P(y.p_pool1) + off, rb);
         for (size_t c = 0; c < rb / 16; ++c)  // undo the chunk swizzle of the stored row
@@ -1518,8 +1692,9 @@ tkv_status tkv_paged_attention(int32_t batch, int32_t n_q_heads, int32_t n_kv_he
   p.chunk_pages = plan_chunks(ntot, cost, n_kv_heads, 0, resident_attention_ctas(kv_dtype, G, head_dim), p.chunk_first);
   if (p.chunk_first[batch] > s.max_chunks) return fail(nullptr, TKV_ERR_INTERNAL, "chunk plan exceeds the scratch");
   const int64_t head_full = int64_t(2) * kPage * head_dim * esz;
+  // the caller's pool size is not passed in: its page ids are the caller's to keep in range
   p.src[0] = PageSource{static_cast<const char*>(pool), 0, head_full * n_kv_heads, head_full, page_table, slot_mask,
-                        nullptr, nullptr, 0, 0, 0, SRC_FULL, 0, 0};
+                        nullptr, nullptr, 0, 0, 0, SRC_FULL, 0, 0, INT32_MAX};
   p.nsrc = 1;
   p.total_chunks = p.chunk_first[batch];
   p.nlayers = 1;

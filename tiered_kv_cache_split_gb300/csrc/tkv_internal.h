@@ -45,6 +45,43 @@ constexpr int64_t kMaxChunkCost = static_cast<int64_t>(kCostFull) * (kMaxChunkPa
 // Device-side error codes written into the handle's error word.
 enum DevError : int { DEV_OK = 0, DEV_TIMEOUT = 1, DEV_BAD_INDEX = 2 };
 
+// Index checks of the debug build (compiled with -DTKV_DEBUG; release builds
+// compile them away). A failing check stores DEV_BAD_INDEX in the error word,
+// then the site, the index and its bound after it (the first failure wins),
+// and the access it guards is skipped; the next synchronising call reports
+// TKV_ERR_INTERNAL with those details. No check traps.
+enum DebugSite : int {
+  DBG_NONE = 0,
+  DBG_ATTN_LIST = 1,   // attention: page-list index against the table row
+  DBG_ATTN_PAGE = 2,   // attention: page id against its pool
+  DBG_FOLD_PAGE = 3,   // score fold: page id against its pool
+  DBG_FOLD_POS = 4,    // score fold: position held by a slot against the score row
+  DBG_APPEND_PAGE = 5, // append: page id of the new token against the T0 pool
+  DBG_APPEND_LIST = 6, // append: T0 page list length against the table row
+  DBG_PREFILL_PAGE = 7,// prefill: page id against the T0 pool
+  DBG_MOVE_SRC = 8,    // mover: source page id against its pool
+  DBG_MOVE_DST = 9,    // mover: destination page id against its pool
+  DBG_MOVE_TEMP = 10   // mover: staging row against the staging area
+};
+constexpr int kDebugSites = 11;
+// error word layout: int32 [0] code, [1] site; int64 [1] index, [2] bound
+
+#ifdef TKV_DEBUG
+constexpr bool kDebugBuild = true;
+__device__ __forceinline__ bool index_ok(int32_t* err, int site, int64_t i, int64_t bound) {
+  if (i >= 0 && i < bound) return true;
+  if (err && atomicCAS(err, 0, DEV_BAD_INDEX) == 0) {
+    err[1] = site;
+    reinterpret_cast<long long*>(err)[1] = static_cast<long long>(i);
+    reinterpret_cast<long long*>(err)[2] = static_cast<long long>(bound);
+  }
+  return false;
+}
+#else
+constexpr bool kDebugBuild = false;
+__device__ __forceinline__ bool index_ok(int32_t*, int, int64_t, int64_t) { return true; }
+#endif
+
 enum SrcKind : int { SRC_FULL = 0, SRC_INT8 = 1 };
 
 // Full-precision K and V blocks of a page (16 rows of head_dim elements) are
@@ -82,6 +119,7 @@ struct PageSource {
   int32_t swz;               // full-precision blocks: kSwizzle (library pools) or 0 (plain)
   int32_t host;              // 1: pages sit in pinned host memory (device-mapped) and are read
                              // in place with plain loads, never with bulk copies
+  int32_t pages;             // pool capacity in pages (debug index checks; INT32_MAX: unknown)
 };
 
 // One attention launch covers `nlayers` consecutive layers (gridDim.z) of the
@@ -192,6 +230,8 @@ struct AppendParams {
   int32_t page[kMaxBatch], slot[kMaxBatch], np0[kMaxBatch], new_page[kMaxBatch];
   int32_t insert_at[kMaxBatch];  // list index the new page takes (-1: none); later entries shift right
   int64_t pos[kMaxBatch];
+  int32_t* err;            // error word (debug index checks)
+  int32_t cap0;            // T0 pool capacity in pages
 };
 cudaError_t launch_append(const AppendParams& p, cudaStream_t s);
 
@@ -203,6 +243,8 @@ struct PrefillParams {
   const int32_t* loc;      // [n] page * 16 + slot
   char* pool0;
   int64_t layer_bytes, page_bytes;
+  int32_t* err;            // error word (debug index checks)
+  int32_t cap0;            // T0 pool capacity in pages
 };
 cudaError_t launch_prefill(const PrefillParams& p, cudaStream_t s);
 
@@ -221,6 +263,7 @@ struct TierPools {
   char* t2_scales;         // layer-major scale records
   int64_t t2_scale_layer_bytes, t2_scale_page_bytes;
   int32_t scale_per_head, scale_f16;
+  int32_t cap[3];          // pool capacities in pages
 };
 
 enum MoveMode : int { MOVE_DIRECT = 0, MOVE_GATHER = 1, MOVE_SCATTER = 2 };
@@ -231,6 +274,8 @@ struct MoveParams {
   char* temp;              // staging rows of one layer: [rows][2][Hkv][D] in the KV dtype
   int32_t mode;
   int32_t layer0;          // the launch covers layers [layer0, layer0 + gridDim.y)
+  int32_t* err;            // error word (debug index checks)
+  int64_t temp_rows;       // staging rows `temp` holds
 };
 cudaError_t launch_move(const MoveParams& p, const Mover* movers, int64_t count, int layers, cudaStream_t s);
 
@@ -252,6 +297,8 @@ struct FoldParams {
   float* acc;              // [nslices][Hkv][acc_stride_h]
   int64_t acc_stride_l, acc_stride_h;
   double inv_lh;           // 1 / (L * Hq)
+  int32_t* err;            // error word (debug index checks)
+  int32_t cap[3];          // pool capacities in pages
 };
 cudaError_t launch_fold(const FoldParams& p, cudaStream_t s);
 
