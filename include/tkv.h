@@ -302,7 +302,7 @@ TKV_API const char* tkv_last_error(tkv_handle h);
  *   slot_mask  device uint32 [n_pages]      bit j set = slot j holds a token
  *   page_counts HOST int32 [B]              pages used by each sequence (max_pages <= 16384)
  *   out      device [B][Hq][d]           (KV dtype)
- *   alpha_sum device float [B][Hkv][max_pages * 16] or NULL: adds, for each slot,
+ *   alpha_sum device float [B][Hkv][max_pages * 16] (16-byte aligned) or NULL: adds, for each slot,
  *            the softmax weight summed over the G query heads of KV head h (slot order = page
  *            table order); multiply by 1/(L * Hq) and sum over layers for s.
  *   scratch  device, tkv_paged_attention_scratch_size bytes (256-aligned); its

@@ -170,12 +170,16 @@ struct Shape {
   static_assert(D % 32 == 0, "head_dim must be a multiple of 32");
 };
 
+// Shared-memory floats an epilogue item needs for its per-chunk output factors.
+constexpr int kEpilogueFactors = kMaxChunksPerSeq * 8;
+
 // Shared-memory layout of the attention CTA. The fp32 kernel also keeps the
 // scaled query and per-warp probabilities in shared memory.
 template <typename T, int G, int D, bool FMA>
 struct Smem {
   using S = Shape<T, G, D>;
   static constexpr int RING = kAttnStages * S::STAGE;
+  static_assert(RING >= kEpilogueFactors * 4, "the idle ring must hold the epilogue's chunk factors");
   static constexpr int QS = FMA ? S::GP * D * 4 : 0;
   static constexpr int PSW = S::GP * kPage + 8;   // floats per warp: p[GP][16], corr[GP]
   static constexpr int PS = FMA ? kAttnWarps * PSW * 4 : 0;
@@ -241,13 +245,37 @@ __device__ __forceinline__ Work find_work_at(const AttnParams& p, int chunk, int
   return wk;
 }
 
-// Work unit u of a launch. Units run layer by layer and within a layer over
-// (KV head, chunk); a persistent CTA takes units blockIdx.x, blockIdx.x +
-// gridDim.x, ..., which with whole waves of units per layer is the same
-// (KV head, chunk) in every layer of the launch.
+// Metadata ring records other than pages (meta_k >= 0): a pad, the end of the
+// CTA's last unit, or the end of a unit that names the CTA's next unit n (-3 - n).
+constexpr int kMetaPad = -2, kMetaLast = -1;
+__device__ __forceinline__ int end_marker(int next) { return next < 0 ? kMetaLast : -3 - next; }
+__device__ __forceinline__ int marker_next(int k) { return -3 - k; }
+
+// A CTA's first unit, and the unit it runs after unit u: the next unhanded one
+// of the launch's counter, or with no counter a static stride.
+__device__ __forceinline__ int first_unit(const AttnParams& p) {
+  if (p.ep_own == nullptr) return static_cast<int>(blockIdx.x);
+  return atomicAdd(&p.ep_own->units, 1);
+}
+__device__ __forceinline__ int claim_next_unit(const AttnParams& p, int u) {
+  if (p.ep_own == nullptr) return u + static_cast<int>(gridDim.x);
+  return atomicAdd(&p.ep_own->units, 1);
+}
+
+// Work unit u of a launch, in hand-out order: the sequences by decreasing chunk
+// cost (p.order), and within a sequence over (layer, KV head, chunk), chunk
+// fastest. A persistent CTA claims its units one at a time (first_unit,
+// claim_next_unit), so the largest units go first and the CTAs finish close
+// together. A unit's result does not depend on the CTA that runs it.
 __device__ __forceinline__ Work unit_work(const AttnParams& p, int u) {
-  const int cu = u % p.total_chunks, rest = u / p.total_chunks;
-  return find_work_at(p, cu, rest % p.Hkv, rest / p.Hkv);
+  const int per = p.Hkv * p.nlayers;  // units per chunk of a sequence
+  int r = 0;
+  while (r + 1 < p.B && p.order_chunk_first[r + 1] * per <= u) ++r;
+  const int b = p.order[r];
+  const int nch = p.chunk_first[b + 1] - p.chunk_first[b];
+  const int v = u - p.order_chunk_first[r] * per;
+  const int rest = v / nch;
+  return find_work_at(p, p.chunk_first[b] + v % nch, rest % p.Hkv, rest / p.Hkv);
 }
 __device__ __forceinline__ int launch_units(const AttnParams& p) { return p.total_chunks * p.Hkv * p.nlayers; }
 
@@ -370,19 +398,19 @@ __device__ __forceinline__ void load_host_page(const PageCopy& c, char* stage, i
   __syncwarp();
 }
 
-// The producer warp's job, for each work unit of this persistent CTA in turn:
-// resolve the unit's pages (one lane per page, 32 per round; the first round's
-// copies go out at once, later rounds are resolved while the ring is full) and
-// keep the ring full; then pad positions (page index -2) up to a multiple of
-// the consumer warp count, and one unit-end marker per consumer warp (page
-// index -1, flags word = the first marker's position), each completed by a
-// plain arrive. Every unit thus starts at a multiple of the warp count, so its
-// page j always goes to consumer warp j % warps and the result does not depend
-// on which CTA runs the unit. The ring runs on across units, so the next unit's
-// pages stream in while the consumers merge the last one. Returns the ring
-// positions handled (lane 0).
+// The producer warp's job, for each work unit of this persistent CTA in turn
+// (from `first`; at the start of each unit it claims the next): resolve the unit's pages (one lane per page, 32 per round; the first
+// round's copies go out at once, later rounds are resolved while the ring is
+// full) and keep the ring full; then pad positions (kMetaPad) up to a multiple
+// of the consumer warp count, and one unit-end marker per consumer warp (the
+// claimed next unit, or kMetaLast; flags word = the first marker's position),
+// each completed by a plain arrive. Every unit thus starts at a multiple of the
+// warp count, so its page j always goes to consumer warp j % warps and the
+// result does not depend on which CTA runs the unit. The ring runs on across
+// units, so the next unit's pages stream in while the consumers merge the last
+// one. Returns the ring positions handled (lane 0).
 template <typename S>
-__device__ int produce(const AttnParams& p, int32_t* meta_k, uint32_t* meta_f, PageCopy* desc, char* ring,
+__device__ int produce(const AttnParams& p, int first, int32_t* meta_k, uint32_t* meta_f, PageCopy* desc, char* ring,
                        uint32_t full0, uint32_t empty0, volatile int* abort_flag) {
   static_assert(kMeta >= 32 + kAttnStages + 2 * kAttnWarps, "metadata ring too small");
   const int lane = threadIdx.x & 31;
@@ -393,9 +421,9 @@ __device__ int produce(const AttnParams& p, int32_t* meta_k, uint32_t* meta_f, P
   auto stage_free = [&](int i) {  // position i's stage has been released by position i - stages
     return i < kAttnStages || mbar_wait(empty0 + (i % kAttnStages) * 8, ((i / kAttnStages) - 1) & 1, p.wait_limit_ns);
   };
-  // test hook: the first CTA withholds its first page, so that a consumer's
-  // bounded wait runs out (nothing is in flight for that stage)
-  const bool stall = p.stall_first_page && blockIdx.x == 0;
+  // test hook: the CTA that runs unit 0 withholds its first page, so that a
+  // consumer's bounded wait runs out (nothing is in flight for that stage)
+  const bool stall = p.stall_first_page && first == 0;
   // Lane 0 waits for each stage and issues its bulk copy; a page in pinned host
   // memory is instead read by the whole warp with plain loads (load_host_page)
   // and its stage completed with a plain arrive.
@@ -428,7 +456,12 @@ __device__ int produce(const AttnParams& p, int32_t* meta_k, uint32_t* meta_f, P
     __syncwarp();
   };
   const int units = launch_units(p);
-  for (int u = blockIdx.x; u < units; u += gridDim.x) {
+  for (int u = first; u < units;) {
+    // claim the unit to run after this one now, so the claim's latency hides behind this unit's pages
+    int next = 0;
+    if (lane == 0) next = claim_next_unit(p, u);
+    next = __shfl_sync(kFull, next, 0);
+    if (next >= units) next = -1;
     const Work wk = unit_work(p, u);
     for (int r = 0; r < wk.npg; r += 32) {
       const int n = min(32, wk.npg - r);
@@ -445,7 +478,7 @@ __device__ int produce(const AttnParams& p, int32_t* meta_k, uint32_t* meta_f, P
           *abort_flag = 1;
           break;
         }
-        meta_k[i % kMeta] = j < pad ? -2 : -1;
+        meta_k[i % kMeta] = j < pad ? kMetaPad : end_marker(next);
         meta_f[i % kMeta] = static_cast<uint32_t>(pos + pad);
         mbar_arrive(full0 + (i % kAttnStages) * 8);
         ++issued;
@@ -453,7 +486,8 @@ __device__ int produce(const AttnParams& p, int32_t* meta_k, uint32_t* meta_f, P
     }
     pos += pad + kAttnWarps;
     __syncwarp();
-    if (!__shfl_sync(kFull, ok ? 1 : 0, 0)) break;
+    if (!__shfl_sync(kFull, ok ? 1 : 0, 0) || next < 0) break;
+    u = next;
   }
   return issued;
 }
@@ -555,10 +589,21 @@ struct LayerBufs {
 // Every epilogue item is read after the grid that wrote it has finished, so the
 // read-only path is safe.
 __device__ __forceinline__ float ld_part(const float* p) { return __ldg(p); }
+#ifndef TKV_EPILOGUE_QUADS
+#define TKV_EPILOGUE_QUADS 2
+#endif
+constexpr int kEpilogueQuads = TKV_EPILOGUE_QUADS;  // four-row groups in flight per thread in the logit pass
+// four consecutive floats; p is 16-byte aligned (page slots start on multiples of 16 floats)
+__device__ __forceinline__ float4 ld_part4(const float* p) { return __ldg(reinterpret_cast<const float4*>(p)); }
 
+// One epilogue item: (1) the group's (M, 1/Z) per head from its chunk partials,
+// and each chunk's output factor exp2(m_j - M) / Z into sF ([chunk][8], -1 for a
+// chunk with no valid slot); (2) the G * D outputs, sum over chunks of factor x
+// partial output, every thread's loads independent of one another; (3) the
+// logit pass into the score accumulator.
 template <typename T, int G, int D, int NT, typename Sync>
 __device__ void layer_epilogue(const AttnParams& p, const LayerBufs& lb, const Work& wk, int tid,
-                               float* sM, float* sIZ, Sync sync) {
+                               float* sM, float* sIZ, float* sF, Sync sync) {
   const int warp = tid >> 5, lane = tid & 31;
   const int64_t base = unit_index(p, wk.z, wk.cf, wk.kvh);  // partial of chunk j: base + j * Hkv
   const int nch = wk.nch;
@@ -590,30 +635,46 @@ __device__ void layer_epilogue(const AttnParams& p, const LayerBufs& lb, const W
     }
 #pragma unroll
     for (int m = 16; m >= 1; m >>= 1) Z += __shfl_xor_sync(kFull, Z, m);
+    const float IZ = Z > 0.f ? 1.f / Z : 0.f;
     if (lane == 0) {
       sM[g] = M;
-      sIZ[g] = Z > 0.f ? 1.f / Z : 0.f;
+      sIZ[g] = IZ;
+    }
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const int j = lane + 32 * r;
+      if (j < nch) sF[j * 8 + g] = (M != -INFINITY && mj[r] != -INFINITY) ? exp2f(mj[r] - M) * IZ : -1.f;
+    }
+    for (int j = lane + 64; j < nch; j += 32) {
+      const float m2 = ld_part(lb.part_m + (base + static_cast<int64_t>(j) * p.Hkv) * G + g);
+      sF[j * 8 + g] = (M != -INFINITY && m2 != -INFINITY) ? exp2f(m2 - M) * IZ : -1.f;
     }
   }
   sync();
   {
-    // the G * D outputs
-    const int lo = 0, hi = G * D;
+    // the G * D outputs: each thread's EPT elements, chunk by chunk
+    constexpr int EPT = (G * D + NT - 1) / NT;
     T* out = reinterpret_cast<T*>(lb.out) + wk.z * p.out_stride_l + static_cast<int64_t>(wk.b) * p.out_stride_b +
              static_cast<int64_t>(wk.kvh) * G * D;
-    for (int idx = lo + tid; idx < hi; idx += NT) {
-      const int g = idx / D;
-      const float Mg = sM[g], IZg = sIZ[g];
-      float o = 0.f;
-      if (Mg != -INFINITY) {
-#pragma unroll 4
-        for (int j = 0; j < nch; ++j) {
-          const int64_t pj = base + static_cast<int64_t>(j) * p.Hkv;
-          const float mj = ld_part(lb.part_m + pj * G + g);
-          if (mj != -INFINITY) o += ld_part(lb.part_o + pj * G * D + idx) * (exp2f(mj - Mg) * IZg);
+    float o[EPT];
+#pragma unroll
+    for (int e = 0; e < EPT; ++e) o[e] = 0.f;
+#pragma unroll 2
+    for (int j = 0; j < nch; ++j) {
+      const float* po = lb.part_o + (base + static_cast<int64_t>(j) * p.Hkv) * G * D;
+#pragma unroll
+      for (int e = 0; e < EPT; ++e) {
+        const int idx = tid + e * NT;
+        if (idx < G * D) {
+          const float f = sF[j * 8 + idx / D];
+          if (f >= 0.f) o[e] += ld_part(po + idx) * f;
         }
       }
-      store_out(out + idx, o);
+    }
+#pragma unroll
+    for (int e = 0; e < EPT; ++e) {
+      const int idx = tid + e * NT;
+      if (idx < G * D) store_out(out + idx, o[e]);
     }
   }
   if (lb.acc == nullptr) return;
@@ -626,29 +687,41 @@ __device__ void layer_epilogue(const AttnParams& p, const LayerBufs& lb, const W
     M[g] = sM[g];
     IZ[g] = sIZ[g];
   }
-  constexpr int U = 4;
-  const int items = wk.npg * kPage;
-  for (int first = tid; first < items; first += NT * U) {
-    float l[U][G], old[U];
+  // Each thread takes four consecutive rows of a page at a time (16-byte loads
+  // of every head's logits and of the accumulator), U quads in flight: the
+  // pass is bound by load latency, so bytes in flight per load decide its speed.
+  constexpr int U = kEpilogueQuads;
+  const int quads = wk.npg * (kPage / 4);
+  for (int first = tid; first < quads; first += NT * U) {
+    float4 l[U][G], old[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      const int item = first + u * NT;
-      if (item < items) {
-        const int k = wk.k0 + (item >> 4), row = item & 15;
+      const int qd = first + u * NT;
+      if (qd < quads) {
+        const int64_t k = wk.k0 + (qd >> 2);
+        const int r0 = (qd & 3) * 4;
 #pragma unroll
-        for (int g = 0; g < G; ++g) l[u][g] = ld_part(spill_b + (static_cast<int64_t>(k) * G + g) * kPage + row);
-        old[u] = lb.first ? 0.f : __ldcg(accb + static_cast<int64_t>(k) * kPage + row);  // neighbouring chunks share lines
+        for (int g = 0; g < G; ++g) l[u][g] = ld_part4(spill_b + (k * G + g) * kPage + r0);
+        old[u] = lb.first ? make_float4(0.f, 0.f, 0.f, 0.f)
+                          : __ldcg(reinterpret_cast<const float4*>(accb + k * kPage + r0));  // chunks share lines
       }
     }
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      const int item = first + u * NT;
-      if (item < items) {
-        const int k = wk.k0 + (item >> 4), row = item & 15;
-        float a = 0.f;
+      const int qd = first + u * NT;
+      if (qd < quads) {
+        const int64_t k = wk.k0 + (qd >> 2);
+        const int r0 = (qd & 3) * 4;
+        float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-        for (int g = 0; g < G; ++g) a += exp2f(l[u][g] - M[g]) * IZ[g];
-        accb[static_cast<int64_t>(k) * kPage + row] = old[u] + a;
+        for (int g = 0; g < G; ++g) {
+          a.x += exp2f(l[u][g].x - M[g]) * IZ[g];
+          a.y += exp2f(l[u][g].y - M[g]) * IZ[g];
+          a.z += exp2f(l[u][g].z - M[g]) * IZ[g];
+          a.w += exp2f(l[u][g].w - M[g]) * IZ[g];
+        }
+        *reinterpret_cast<float4*>(accb + k * kPage + r0) =
+            make_float4(old[u].x + a.x, old[u].y + a.y, old[u].z + a.z, old[u].w + a.w);
       }
     }
   }
@@ -690,6 +763,7 @@ constexpr int kCombineThreads = 256;
 template <typename T, int G, int D>
 __global__ void __launch_bounds__(kCombineThreads) attn_combine_kernel(const __grid_constant__ AttnParams p) {
   __shared__ float sM[8], sIZ[8];
+  __shared__ float sF[kEpilogueFactors];
   __shared__ int s_item;
   const int per_layer = epilogue_items_per_layer(p);
   // wait here until the attention kernel's partials and spilled logits are complete and visible
@@ -701,7 +775,7 @@ __global__ void __launch_bounds__(kCombineThreads) attn_combine_kernel(const __g
     __syncthreads();
     const int item = s_item;
     if (item < 0) break;
-    layer_epilogue<T, G, D, kCombineThreads>(p, lb, epilogue_work(p, item), threadIdx.x, sM, sIZ,
+    layer_epilogue<T, G, D, kCombineThreads>(p, lb, epilogue_work(p, item), threadIdx.x, sM, sIZ, sF,
                                              [] { __syncthreads(); });
   }
 }
@@ -715,7 +789,7 @@ __global__ void __launch_bounds__(kCombineThreads) attn_combine_kernel(const __g
 // filling the launch's tail.)
 template <typename T, int G, int D>
 __device__ __forceinline__ void prev_launch_epilogue(const AttnParams& p, int tid, float* sM, float* sIZ,
-                                                     volatile int* s_item) {
+                                                     float* sF, volatile int* s_item) {
   if (!p.has_prev) return;
   constexpr int NT = (kAttnWarps + 1) * 32;
   const int per_layer = epilogue_items_per_layer(p);
@@ -727,7 +801,7 @@ __device__ __forceinline__ void prev_launch_epilogue(const AttnParams& p, int ti
     __syncthreads();
     const int item = *s_item;
     if (item < 0) break;
-    layer_epilogue<T, G, D, NT>(p, lb, epilogue_work(p, item), tid, sM, sIZ, [] { __syncthreads(); });
+    layer_epilogue<T, G, D, NT>(p, lb, epilogue_work(p, item), tid, sM, sIZ, sF, [] { __syncthreads(); });
   }
 }
 
@@ -795,6 +869,7 @@ __global__ void __launch_bounds__((kAttnWarps + 1) * 32, 3)
   __shared__ volatile int s_abort;
   __shared__ float s_epM[8], s_epIZ[8];  // previous launch's (M, 1 / Z) per head
   __shared__ volatile int s_item;
+  __shared__ int s_first;
 
   const int tid = threadIdx.x;
   const int w = tid >> 5, lane = tid & 31;
@@ -806,14 +881,23 @@ __global__ void __launch_bounds__((kAttnWarps + 1) * 32, 3)
       p.span_next[0] = ~0ull;
       p.span_next[1] = 0ull;
     }
-    if (p.ep_clear)  // counters of the launch after next
+    if (p.ep_clear) {  // counters of the launch after next
       for (int z = 0; z < kMaxLaunchLayers; ++z) p.ep_clear->claim[z] = 0;
+      p.ep_clear->units = 0;
+    }
     if (p.started) {                  // tells the copy stream this launch is under way
       asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p.started), "r"(p.launch_seq) : "memory");
     }
   }
   init_barriers<L>(smem);
   __syncthreads();
+  // the first ep_first_ctas CTAs take epilogue items of the previous launch
+  // before any unit (the ring is still idle), while the others start streaming
+  if (static_cast<int>(blockIdx.x) < p.ep_first_ctas)
+    prev_launch_epilogue<T, G, D>(p, tid, s_epM, s_epIZ, reinterpret_cast<float*>(smem), &s_item);
+  if (tid == 0) s_first = first_unit(p);
+  __syncthreads();
+  const int first = s_first;
 
   int32_t* meta_k = reinterpret_cast<int32_t*>(smem + L::off_pg);
   uint32_t* meta_f = reinterpret_cast<uint32_t*>(meta_k + kMeta);
@@ -824,11 +908,11 @@ __global__ void __launch_bounds__((kAttnWarps + 1) * 32, 3)
   const bool consumer = w < kAttnWarps;
   int issued = 0;
   if (!consumer)
-    issued = produce<S>(p, meta_k, meta_f, reinterpret_cast<PageCopy*>(smem + L::off_desc), ring, full0, empty0,
-                        &s_abort);
+    issued = produce<S>(p, first, meta_k, meta_f, reinterpret_cast<PageCopy*>(smem + L::off_desc), ring, full0,
+                        empty0, &s_abort);
 
   const int units = launch_units(p);
-  int u = blockIdx.x;
+  int u = first;
   Work wk{};
   uint32_t qa[KS][2];                    // Q fragments (A operand, heads as rows; rows 8..15 zero)
   float* spill_b = nullptr;
@@ -867,8 +951,8 @@ __global__ void __launch_bounds__((kAttnWarps + 1) * 32, 3)
       break;
     }
     char* stage = ring + st * S::STAGE;
-    const int k = meta_k[i % kMeta];  // page index in the sequence's list; -1 ends the unit, -2 pads
-    if (k == -2) {
+    const int k = meta_k[i % kMeta];  // page index in the sequence's list, or a pad or unit-end record
+    if (k == kMetaPad) {
       __syncwarp();
       if (lane == 0) mbar_arrive(empty0 + st * 8);
       continue;
@@ -906,8 +990,8 @@ __global__ void __launch_bounds__((kAttnWarps + 1) * 32, 3)
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // generic writes before the next copy
         mbar_arrive(empty0 + st * 8);
       }
-      u += gridDim.x;
-      if (u >= units) break;
+      if (k == kMetaLast) break;  // the producer claimed no further unit
+      u = marker_next(k);
       start_unit();
       m_run = -INFINITY;
       z_run = 0.f;
@@ -1029,7 +1113,8 @@ __global__ void __launch_bounds__((kAttnWarps + 1) * 32, 3)
     }
   }
   __syncthreads();
-  prev_launch_epilogue<T, G, D>(p, tid, s_epM, s_epIZ, &s_item);
+  // items left over once the units ran out (the ring is idle again)
+  prev_launch_epilogue<T, G, D>(p, tid, s_epM, s_epIZ, reinterpret_cast<float*>(smem), &s_item);
   if (tid == 0 && p.span) atomicMax(p.span + 1, global_ns());
 }
 
@@ -1121,6 +1206,7 @@ __global__ void __launch_bounds__((kAttnWarps + 1) * 32)
   __shared__ volatile int s_abort;
   __shared__ float s_epM[8], s_epIZ[8];  // previous layer's (M, 1 / Z) per head
   __shared__ volatile int s_item;
+  __shared__ int s_first;
 
   const int tid = threadIdx.x;
   const int w = tid >> 5, lane = tid & 31;
@@ -1132,14 +1218,23 @@ __global__ void __launch_bounds__((kAttnWarps + 1) * 32)
       p.span_next[0] = ~0ull;
       p.span_next[1] = 0ull;
     }
-    if (p.ep_clear)  // counters of the launch after next
+    if (p.ep_clear) {  // counters of the launch after next
       for (int z = 0; z < kMaxLaunchLayers; ++z) p.ep_clear->claim[z] = 0;
+      p.ep_clear->units = 0;
+    }
     if (p.started) {                  // tells the copy stream this launch is under way
       asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p.started), "r"(p.launch_seq) : "memory");
     }
   }
   init_barriers<L>(smem);
   __syncthreads();
+  // the first ep_first_ctas CTAs take epilogue items of the previous launch
+  // before any unit (the ring is still idle), while the others start streaming
+  if (static_cast<int>(blockIdx.x) < p.ep_first_ctas)
+    prev_launch_epilogue<T, G, D>(p, tid, s_epM, s_epIZ, reinterpret_cast<float*>(smem), &s_item);
+  if (tid == 0) s_first = first_unit(p);
+  __syncthreads();
+  const int first = s_first;
 
   int32_t* meta_k = reinterpret_cast<int32_t*>(smem + L::off_pg);
   uint32_t* meta_f = reinterpret_cast<uint32_t*>(meta_k + kMeta);
@@ -1150,14 +1245,14 @@ __global__ void __launch_bounds__((kAttnWarps + 1) * 32)
   const bool consumer = w < kAttnWarps;
   int issued = 0;
   if (!consumer)
-    issued = produce<S>(p, meta_k, meta_f, reinterpret_cast<PageCopy*>(smem + L::off_desc), ring, full0, empty0,
-                        &s_abort);
+    issued = produce<S>(p, first, meta_k, meta_f, reinterpret_cast<PageCopy*>(smem + L::off_desc), ring, full0,
+                        empty0, &s_abort);
 
   float* q_s = reinterpret_cast<float*>(smem + L::off_q);
   float* p_s = reinterpret_cast<float*>(smem + L::off_p) + w * L::PSW;
   float* corr_s = p_s + S::GP * kPage;
   const int units = launch_units(p);
-  int u = blockIdx.x;
+  int u = first;
   Work wk{};
   float* spill_b = nullptr;
   // the unit's scaled query (shared by the consumer warps) and logit spill
@@ -1201,8 +1296,8 @@ __global__ void __launch_bounds__((kAttnWarps + 1) * 32)
       if (lane == 0) s_abort = 1;
       break;
     }
-    const int k = meta_k[i % kMeta];  // page index in the sequence's list; -1 ends the unit, -2 pads
-    if (k == -2) {
+    const int k = meta_k[i % kMeta];  // page index in the sequence's list, or a pad or unit-end record
+    if (k == kMetaPad) {
       __syncwarp();
       if (lane == 0) mbar_arrive(empty0 + st * 8);
       continue;
@@ -1232,8 +1327,8 @@ __global__ void __launch_bounds__((kAttnWarps + 1) * 32)
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // generic writes before the next copy
         mbar_arrive(empty0 + st * 8);
       }
-      u += gridDim.x;
-      if (u >= units) break;
+      if (k == kMetaLast) break;  // the producer claimed no further unit
+      u = marker_next(k);
       start_unit();
       if (!consumers_meet(merge_bar, mphase, lane, p.wait_limit_ns)) {  // the new query is in place
         if (lane == 0) s_abort = 1;
@@ -1432,13 +1527,14 @@ __global__ void __launch_bounds__((kAttnWarps + 1) * 32)
     }
   }
   __syncthreads();
-  prev_launch_epilogue<T, G, D>(p, tid, s_epM, s_epIZ, &s_item);
+  // items left over once the units ran out (the ring is idle again)
+  prev_launch_epilogue<T, G, D>(p, tid, s_epM, s_epIZ, reinterpret_cast<float*>(smem), &s_item);
   if (tid == 0 && p.span) atomicMax(p.span + 1, global_ns());
 }
 
 // Persistent launch: as many CTAs as fit on the device at once (found once per
-// kernel and device), at most one per work unit; each CTA runs units
-// blockIdx.x, blockIdx.x + gridDim.x, ...
+// kernel and device), at most one per work unit; each CTA claims its units one
+// at a time from the launch's counter (first_unit, claim_next_unit).
 template <typename K>
 cudaError_t launch_kernel(K kern, int smem_bytes, const AttnParams& p, int total_chunks, cudaStream_t s,
                           int (&resident)[64]) {

@@ -94,12 +94,14 @@ __host__ __device__ inline int64_t swz_offset(int row, int64_t byte_in_row, int 
   return (((byte_in_row >> 4) ^ (row & swz)) << 4) | (byte_in_row & 15);
 }
 
-// Epilogue work counters of one attention launch: claim[z] hands out the
-// (KV head, chunk) epilogue items of its layer z (fetch-and-add; values past
-// the item count mean none is left). Four sets rotate over consecutive launches.
+// Work counters of one attention launch: claim[z] hands out the epilogue
+// items of its layer z, and units hands out the launch's work units after each
+// CTA's first (fetch-and-add; values past the count mean none is left). Four
+// sets rotate over consecutive launches.
 constexpr int kMaxLaunchLayers = 32;
 struct EpCounters {
   int32_t claim[kMaxLaunchLayers];
+  int32_t units;
 };
 
 // One page source of the attention kernel: a page pool (or one layer of it).
@@ -134,6 +136,12 @@ struct AttnParams {
   int32_t table_stride;
   int32_t npages[3][kMaxBatch];
   int32_t chunk_first[kMaxBatch + 1];   // prefix sums of chunks per sequence
+  // Order in which the launch's units are handed out: the sequences by
+  // decreasing chunk cost (order[r] = sequence of rank r), and prefix sums of
+  // their chunk counts in that order. Largest units first keeps the CTAs'
+  // finishing times close.
+  int32_t order[kMaxBatch];
+  int32_t order_chunk_first[kMaxBatch + 1];
   int32_t page_base[kMaxBatch + 1];     // spill / score slot base of each sequence, in pages
   int32_t chunk_pages;                  // upper bound of pages per chunk
   int32_t total_chunks;                 // chunk_first[B]
@@ -152,12 +160,16 @@ struct AttnParams {
   int64_t acc_stride_l, acc_stride_b, acc_stride_h;         //  + h * acc_stride_h + (page_base[b] + k) * 16 (may be null)
   int32_t* err;
   unsigned long long wait_limit_ns;     // bounded waits give up after this long
-  int32_t stall_first_page;             // test hook: CTA (0, 0, 0) never issues its first page's copy
+  int32_t stall_first_page;             // test hook: the CTA running unit 0 never issues its first page's copy
   // The previous launch of the same step (same chunk plan), whose output merge
   // and score epilogue each CTA of this launch runs after its own pages
   // (has_prev != 0); it covered prev_nlayers layers.
   int32_t has_prev;
   int32_t prev_nlayers;
+  // CTAs blockIdx.x < ep_first_ctas take the previous launch's epilogue items
+  // before their first unit, overlapping them with the others' page streams;
+  // every CTA takes items left over once the units run out
+  int32_t ep_first_ctas;
   // The first launch of a step covers layers 0 .. Lg-1, so its epilogue items
   // are the first to touch every accumulator slot of the step: they write
   // instead of adding (and the fold does not clear). 0 for a stateless call.
