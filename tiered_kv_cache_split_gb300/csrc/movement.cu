@@ -336,13 +336,28 @@ __global__ void fold_kernel(const __grid_constant__ FoldParams p) {
   }
   const int page = p.table[src][static_cast<int64_t>(b) * p.table_stride + k];
   if (!index_ok(p.err, DBG_FOLD_PAGE, page, p.cap[src])) return;  // debug build only
-  const int64_t at = static_cast<int64_t>(p.page_base[b]) * kPage + slot;
+  // the slot's metadata, then its (slice, KV head) values: every load is
+  // independent, so they go out in batches of U and are added in slice order
+  const uint32_t mword = p.mask[src][page];
+  const int pos = p.posmap[src][static_cast<int64_t>(page) * kPage + row];
+  const float* __restrict__ acc = p.acc + static_cast<int64_t>(p.page_base[b]) * kPage + slot;
+  const int n = p.nslices * p.Hkv;
+  constexpr int U = 16;
   double sum = 0.0;
-  const float* __restrict__ acc = p.acc;
-  for (int z = 0; z < p.nslices; ++z)
-    for (int h = 0; h < p.Hkv; ++h) sum += static_cast<double>(__ldg(acc + z * p.acc_stride_l + h * p.acc_stride_h + at));
-  if ((p.mask[src][page] >> row) & 1u) {
-    const int pos = p.posmap[src][static_cast<int64_t>(page) * kPage + row];
+  for (int i0 = 0; i0 < n; i0 += U) {
+    float v[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int i = i0 + u;
+      v[u] = i < n ? __ldg(acc + static_cast<int64_t>(i / p.Hkv) * p.acc_stride_l +
+                           static_cast<int64_t>(i % p.Hkv) * p.acc_stride_h)
+                   : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+      if (i0 + u < n) sum += static_cast<double>(v[u]);
+  }
+  if ((mword >> row) & 1u) {
     if (pos >= 0 && index_ok(p.err, DBG_FOLD_POS, pos, p.s_stride))
       p.s[static_cast<int64_t>(b) * p.s_stride + pos] += sum * p.inv_lh;
   }
