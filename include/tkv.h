@@ -113,7 +113,8 @@ typedef struct {
   int32_t layers_per_launch;                          /* layers one attention launch covers (and one
                                                          prefetch copies in STREAM mode), at most 32;
                                                          0 = auto: the largest divisor of n_layers
-                                                         up to 7 */
+                                                         up to 7 (up to 14 when one layer's K and V
+                                                         at full capacity are under 64 MB) */
 } tkv_config;
 
 typedef struct {

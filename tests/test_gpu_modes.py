@@ -77,12 +77,13 @@ def test_chain7b_shape_in_every_host_tier_mode_and_layer_grouping():
     # first reassignment on and tokens move between them every 16 steps.
     w = CHAIN7B.replace(context=("fixed", 600), prompt_len=64, recent_window=32, reclassify_interval=16,
                         n_steps=48)
-    configs = [("stream", 1), ("stream", 0), ("mirror", 0), ("zerocopy", 28), ("mirror", 3), ("zerocopy", 0)]
+    configs = [("stream", 1), ("stream", 0), ("mirror", 7), ("zerocopy", 28), ("mirror", 3), ("zerocopy", 0)]
     oc, stats = _lockstep(w, 48, configs)
     counts = np.bincount(oc.seqs[0].tier, minlength=4)
     assert np.all(counts > 0), counts
     launches = [s["attn_launches"] for s in stats]
-    assert launches == [48 * 28, 48 * 4, 48 * 4, 48 * 1, 48 * 10, 48 * 4], launches
+    # the automatic grouping takes 14 layers per launch here: one layer's K and V are small
+    assert launches == [48 * 28, 48 * 2, 48 * 4, 48 * 1, 48 * 10, 48 * 2], launches
     # per-step copies only in STREAM mode; a mirror moves T1 / T2 sources on the device
     assert stats[0]["prefetch_bytes"] > 0 and stats[2]["prefetch_bytes"] == 0 and stats[3]["prefetch_bytes"] == 0
     assert stats[2]["h2d_move_bytes"] == 0 and stats[0]["h2d_move_bytes"] > 0

@@ -148,14 +148,19 @@ std::string validate(const tkv_config& c) {
 }
 
 // Layers per attention launch: the configured count (at most L), else the
-// largest divisor of L up to 7. Each launch pays a fixed start-up, tail and
-// launch cost; on the batch-32 workload one layer per launch ran the kernel at
-// 60 % of the measured HBM peak, 4 layers at 67 % and 7 at 72 %. In STREAM mode
+// largest divisor of L up to 7, or up to 14 when one layer's K and V at full
+// capacity are under 64 MB. Each launch pays a fixed start-up, tail and launch
+// cost; on the batch-32 workload one layer per launch ran the kernel at 60 % of
+// the measured HBM peak, 4 layers at 67 % and 7 at 72 %; a single 2k-token
+// request, where a launch is ~20 us of fixed cost, took 142 us per 28-layer step
+// with 7 layers per launch, 111 us with 14 and 117 us with 28. In STREAM mode
 // the staging ring holds two groups, so the grouping costs 2 x 7 layers of the
 // used T1 / T2 range in HBM.
 int layers_per_launch(const tkv_config& c) {
   if (c.layers_per_launch > 0) return std::min({c.layers_per_launch, c.n_layers, kMaxLaunchLayers});
-  const int cap = 7;
+  const int64_t esz = c.kv_dtype == TKV_DTYPE_BF16 ? 2 : 4;
+  const int64_t layer_bytes = int64_t(c.max_batch) * c.max_tokens * 2 * c.n_kv_heads * c.head_dim * esz;
+  const int cap = layer_bytes < (int64_t(64) << 20) ? 14 : 7;
   int best = 1;
   for (int g = 1; g <= std::min(cap, c.n_layers); ++g)
     if (c.n_layers % g == 0) best = g;
