@@ -170,8 +170,11 @@ TKV_API tkv_status tkv_append(tkv_handle h, int32_t seq, const void* k, const vo
  * attend over T0 + T1 + T2 with T3 absent (Methodology 3) with the score
  * update of Methodology 2 fused in, fold the step's score increments into s,
  * and reassign tiers when the step count reaches a multiple of Delta
- * (Methodology 4). Errors: TKV_ERR_CAPACITY when a sequence or pool is full
- * (state unchanged); TKV_ERR_CUDA marks the handle broken. */
+ * (Methodology 4). In STREAM mode a step that ends without a reassignment
+ * also enqueues the next step's first layer-group prefetch (T1 and T2 change
+ * only at a reassignment), so the host link stays busy between calls.
+ * Errors: TKV_ERR_CAPACITY when a sequence or pool is full (state unchanged);
+ * TKV_ERR_CUDA marks the handle broken. */
 TKV_API tkv_status tkv_decode_step(tkv_handle h, const void* q, const void* k_new, const void* v_new,
                            void* out);
 

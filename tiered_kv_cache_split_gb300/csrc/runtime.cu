@@ -279,6 +279,8 @@ struct tkv_ctx {
   int64_t last_launch_seq = 0;    // number of the last attention launch actually enqueued (0: none)
   bool stall_next = false;        // test hook: the next attention launch withholds one page
   unsigned long long wait_limit_ns = 2000000000ull;  // bounded device waits give up after this long
+  bool ahead_valid = false;       // the next step's first layer group is staged in ahead_slot
+  int ahead_slot = 0;
   int32_t fault_site = TKV_FAULT_NONE;  // test hook: host call reported as failed when its countdown ends
   int32_t fault_countdown = 0;
   int64_t span_from = 0;          // first attention launch counted in attn_span_ms
@@ -869,8 +871,12 @@ tkv_status decode_step_device(tkv_ctx* h, const void* q, const void* k_new, cons
   // epilogue is a launch of its own after the loop.
   for (int l0 = 0; l0 < y.L; l0 += y.Lg) {
     const int nl = std::min(y.Lg, y.L - l0);
-    const int slot = h->slot_rr;
-    if (stream) {
+    int slot = h->slot_rr;
+    if (stream && l0 == 0 && h->ahead_valid) {
+      slot = h->ahead_slot;  // staged at the end of the previous step
+      h->ahead_valid = false;
+      if (h->xs != h->cs) CK(h, cudaStreamWaitEvent(h->cs, h->ev_ready[slot], 0));
+    } else if (stream) {
       h->slot_rr ^= 1;
       tkv_status st = enqueue_prefetch(h, l0, nl, slot, static_cast<uint32_t>(h->last_launch_seq));
       if (st) return st;
@@ -888,7 +894,12 @@ tkv_status decode_step_device(tkv_ctx* h, const void* q, const void* k_new, cons
       p.span_next = spans + 2 * ((h->attn_launch_seq + 1) % kSpanSlots);
     }
     p.has_prev = l0 > 0;
-    p.ep_first_ctas = p.has_prev && kEpFirstDiv > 0 && ep_share >= kEpFirstShare ? h->resident_ctas / kEpFirstDiv : 0;
+    {
+      // a share of the launch's grid (resident CTAs, at most one per unit)
+      const int64_t grid = std::min<int64_t>(h->resident_ctas, int64_t(total_chunks) * y.Hkv * nl);
+      p.ep_first_ctas = p.has_prev && kEpFirstDiv > 0 && ep_share >= kEpFirstShare
+                            ? static_cast<int32_t>(grid / kEpFirstDiv) : 0;
+    }
     p.prev_nlayers = p.nlayers;
     p.nlayers = nl;
     p.prev_first_of_step = p.first_of_step;
@@ -975,12 +986,24 @@ tkv_status decode_step_device(tkv_ctx* h, const void* q, const void* k_new, cons
     harvest(h);
   }
   if (h->steps % h->cfg.reclassify_interval == 0) return do_reclassify(h);
+  // T1 / T2 change only at a reassignment: stage the next step's first layer
+  // group now, so the host link stays busy while this step's tail runs and
+  // while a caller waits for it (the next step uses the staged slot)
+  if (stream && h->xs != h->cs) {
+    const int slot = h->slot_rr;
+    h->slot_rr ^= 1;
+    if (tkv_status st = enqueue_prefetch(h, 0, std::min(y.Lg, y.L), slot, static_cast<uint32_t>(h->last_launch_seq)))
+      return st;
+    h->ahead_valid = true;
+    h->ahead_slot = slot;
+  }
   return TKV_OK;
 }
 
 tkv_status do_reclassify(tkv_ctx* h) {
   const Layout& y = h->y;
   const int B = static_cast<int>(h->seqs.size());
+  h->ahead_valid = false;  // the reassignment may move T1 / T2 pages: restage
   if (B == 0) return fail(h, TKV_ERR_STATE, "no sequence to reclassify");
   // the reassignment reads the scores of every step enqueued so far: drain them
   // first (this also keeps queued decode work out of the reassignment's time)
@@ -1456,6 +1479,7 @@ tkv_status tkv_reclassify(tkv_handle h) {
 tkv_status tkv_prefetch(tkv_handle h, int32_t layer, int32_t slot) {
   if (tkv_status st = check_usable(h)) return st;
   if (layer < 0 || layer >= h->y.L || slot < 0 || slot > 1) return fail(h, TKV_ERR_INVALID_ARG, "bad layer or slot");
+  h->ahead_valid = false;  // the caller may overwrite the staged slot
   return enqueue_prefetch(h, layer, std::min(h->y.Lg, h->y.L - layer), slot);
 }
 
