@@ -780,13 +780,14 @@ __global__ void __launch_bounds__(kCombineThreads) attn_combine_kernel(const __g
   }
 }
 
-// The previous launch's epilogue, run by all warps of an attention CTA once its
-// own work units are done: CTAs that finish early do it while the last ones
-// still stream. The items — one per (layer, sequence, KV head) group of the
-// previous launch — are handed out by that launch's counters. (Taking items of
-// this launch's own completed layers as well, with per-layer completion
-// counts, measured slower: those items then displace page streaming instead of
-// filling the launch's tail.)
+// The previous launch's epilogue, run by all warps of an attention CTA: before
+// its first unit (CTAs blockIdx.x < ep_first_ctas, while the others stream) and
+// once the launch's units run out (any items left). The items — one per
+// (layer, sequence, KV head) group of the previous launch — are handed out by
+// that launch's counters. While a CTA runs items its page ring is idle, so the
+// items' chunk factors sit in the ring's first stages. (Running each group's
+// item in its own launch, by the CTA that finishes the group, measured slower:
+// the last groups' items form a tail and an item stalls its CTA's ring.)
 template <typename T, int G, int D>
 __device__ __forceinline__ void prev_launch_epilogue(const AttnParams& p, int tid, float* sM, float* sIZ,
                                                      float* sF, volatile int* s_item) {
