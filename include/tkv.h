@@ -247,6 +247,24 @@ typedef enum {
  * handle given with TKV_FAULT_ALLOC / missing for the others. */
 TKV_API tkv_status tkv_test_inject_fault(tkv_handle h, int32_t site, int32_t countdown);
 
+/* Test hook, host only (no device work; the paper has no counterpart): the
+ * attention work plan a decode step uses. Sequence b has full_pages[b] T0 + T1
+ * pages and i8_pages[b] T2 pages (a T2 page costs 1.5 full pages). Writes
+ * chunk_first[0..B] (prefix sums of the chunks each sequence's page list is
+ * split into, equal in cost; one work unit per chunk, KV head and layer),
+ * order[0..B) (the sequences by decreasing chunk cost, ties by index: the
+ * order in which units are handed out), order_chunk_first[0..B] (prefix sums
+ * of the chunk counts in that order) and *page_bound (pages of the largest
+ * chunk, an upper bound). resident_ctas: attention CTAs resident at once;
+ * split_pages: pages per chunk, 0 = automatic (whole waves of resident CTAs).
+ * Errors: TKV_ERR_INVALID_ARG for batch outside 1..64, a page count outside
+ * 0..16384, n_kv_heads < 1, resident_ctas < 1, split_pages < 0 or a null
+ * pointer. */
+TKV_API tkv_status tkv_test_plan_attention(int32_t batch, const int64_t* full_pages, const int64_t* i8_pages,
+                                           int32_t n_kv_heads, int32_t split_pages, int32_t resident_ctas,
+                                           int32_t* chunk_first, int32_t* order, int32_t* order_chunk_first,
+                                           int32_t* page_bound);
+
 /* 1 when this library is the debug build (compiled with TKV_DEBUG), else 0.
  * The debug build checks on the device every page id, page-list index, score
  * position and staging row a kernel derives from the bookkeeping against the

@@ -85,6 +85,7 @@ _SIGS = {
     "tkv_paged_attention_noalloc_status": [ctypes.POINTER(c_i32), c_vp],
     "tkv_test_stall_next_attention": [c_vp, ctypes.c_uint64],
     "tkv_test_inject_fault": [c_vp, c_i32, c_i32],
+    "tkv_test_plan_attention": [c_i32, c_vp, c_vp, c_i32, c_i32, c_i32, c_vp, c_vp, c_vp, ctypes.POINTER(c_i32)],
     "tkv_test_plant_bad_page": [c_vp, c_i32, c_i32, c_i64, ctypes.POINTER(c_i32)],
     "tkv_classify_scratch_size": [c_i32, c_i64, ctypes.POINTER(c_sz)],
     "tkv_classify": [c_i32, c_vp, c_vp, c_vp, c_i64, c_vp, c_i32, c_i32, c_vp, c_sz, c_vp],

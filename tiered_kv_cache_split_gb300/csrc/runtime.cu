@@ -1533,6 +1533,27 @@ tkv_status tkv_test_plant_bad_page(tkv_handle h, int32_t seq, int32_t tier, int6
   return TKV_OK;
 }
 
+tkv_status tkv_test_plan_attention(int32_t batch, const int64_t* full_pages, const int64_t* i8_pages,
+                                   int32_t n_kv_heads, int32_t split_pages, int32_t resident_ctas,
+                                   int32_t* chunk_first, int32_t* order, int32_t* order_chunk_first,
+                                   int32_t* page_bound) {
+  if (batch < 1 || batch > kMaxBatch) return fail(nullptr, TKV_ERR_INVALID_ARG, "batch must be 1..64");
+  if (!full_pages || !i8_pages || !chunk_first || !order || !order_chunk_first || !page_bound)
+    return fail(nullptr, TKV_ERR_INVALID_ARG, "null pointer");
+  if (n_kv_heads < 1 || resident_ctas < 1 || split_pages < 0)
+    return fail(nullptr, TKV_ERR_INVALID_ARG, "bad n_kv_heads, resident_ctas or split_pages");
+  std::vector<int64_t> ntot(batch), cost(batch);
+  for (int b = 0; b < batch; ++b) {
+    if (full_pages[b] < 0 || i8_pages[b] < 0 || full_pages[b] + i8_pages[b] > kMaxSeqPages)
+      return fail(nullptr, TKV_ERR_INVALID_ARG, "page count of sequence %d outside 0..16384", b);
+    ntot[b] = full_pages[b] + i8_pages[b];
+    cost[b] = int64_t(kCostFull) * full_pages[b] + int64_t(kCostI8) * i8_pages[b];
+  }
+  *page_bound = plan_chunks(ntot, cost, n_kv_heads, split_pages, resident_ctas, chunk_first);
+  plan_unit_order(cost, chunk_first, order, order_chunk_first);
+  return TKV_OK;
+}
+
 tkv_status tkv_num_sequences(tkv_handle h, int32_t* n) {
   if (!h || !n) return fail(h, TKV_ERR_INVALID_ARG, "null argument");
   *n = static_cast<int32_t>(h->seqs.size());
