@@ -894,8 +894,12 @@ __global__ void __launch_bounds__((kAttnWarps + 1) * 32, 3)
   __syncthreads();
   // the first ep_first_ctas CTAs take epilogue items of the previous launch
   // before any unit (the ring is still idle), while the others start streaming
-  if (static_cast<int>(blockIdx.x) < p.ep_first_ctas)
+  if (static_cast<int>(blockIdx.x) < p.ep_first_ctas) {
     prev_launch_epilogue<T, G, D>(p, tid, s_epM, s_epIZ, reinterpret_cast<float*>(smem), &s_item);
+    // the items wrote the ring's first stage through the generic proxy: order
+    // those writes before the bulk copies that will fill it
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
   if (tid == 0) s_first = first_unit(p);
   __syncthreads();
   const int first = s_first;
@@ -1231,8 +1235,12 @@ __global__ void __launch_bounds__((kAttnWarps + 1) * 32)
   __syncthreads();
   // the first ep_first_ctas CTAs take epilogue items of the previous launch
   // before any unit (the ring is still idle), while the others start streaming
-  if (static_cast<int>(blockIdx.x) < p.ep_first_ctas)
+  if (static_cast<int>(blockIdx.x) < p.ep_first_ctas) {
     prev_launch_epilogue<T, G, D>(p, tid, s_epM, s_epIZ, reinterpret_cast<float*>(smem), &s_item);
+    // the items wrote the ring's first stage through the generic proxy: order
+    // those writes before the bulk copies that will fill it
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
   if (tid == 0) s_first = first_unit(p);
   __syncthreads();
   const int first = s_first;
